@@ -1,0 +1,195 @@
+"""Python binding of libdspark.so (ctypes): argument marshalling only.
+
+Every function here forwards torch CUDA tensors to the C ABI in include/dspark.h as raw
+device pointers plus the current CUDA stream. Nothing is computed in Python and there
+is no fallback: if the library is missing or the call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libdspark.so")
+
+GREEDY, PROBABILISTIC = 0, 1
+FLAG_SKIP_ARRIVAL_CTA0 = 0x1
+FLAG_FORCE_CUDA_CORES = 0x2
+FLAG_FORCE_TENSOR_CORES = 0x4
+RANK = 256
+MAX_BS = 64
+MAX_K = 32
+
+STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "COOP_TOO_LARGE",
+          5: "TIMEOUT", 6: "BAD_TOKEN", 7: "NONFINITE_W2", 8: "WORKSPACE"}
+
+
+class DsparkError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        detail = ""
+        if status == 3:
+            detail = ": " + lib().dspark_last_cuda_error().decode()
+        super().__init__(f"{what} failed with {STATUS.get(status, status)}{detail}")
+
+
+class WalkArgs(C.Structure):
+    _fields_ = [
+        ("base_logits", C.c_void_p), ("w1", C.c_void_p), ("w2", C.c_void_p),
+        ("w2q", C.c_void_p), ("w2_scales", C.c_void_p), ("prev_tokens", C.c_void_p),
+        ("seeds", C.c_void_p), ("V", C.c_int64), ("rank", C.c_int32), ("bs", C.c_int32),
+        ("K", C.c_int32), ("mode", C.c_int32), ("temperature", C.c_float),
+        ("top_k", C.c_int32), ("draft_tokens", C.c_void_p), ("draft_logits", C.c_void_p),
+        ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t),
+        ("status_dev", C.c_void_p), ("flags", C.c_uint32), ("resident_rows_cap", C.c_int32),
+        ("timeout_us", C.c_uint32),
+    ]
+
+
+_lib = None
+
+
+def lib():
+    """Load libdspark.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "dspark_markov_draft_gb300.build.build() (nvcc, sm_103a)")
+        L = C.CDLL(LIB_PATH)
+        vp, i32, i64 = C.c_void_p, C.c_int32, C.c_int64
+        L.dspark_quantize_w2.argtypes = [vp, i64, i32, vp, vp, vp, vp]
+        L.dspark_walk.argtypes = [C.POINTER(WalkArgs), vp]
+        L.dspark_walk_topk.argtypes = [C.POINTER(WalkArgs), vp]
+        L.dspark_walk_from_host.argtypes = [C.POINTER(WalkArgs), vp, vp, vp, vp, vp, vp]
+        L.dspark_walk_workspace_size.argtypes = [i64, i32, i32, i32]
+        L.dspark_walk_workspace_size.restype = C.c_size_t
+        L.dspark_query_capacity.argtypes = [i32, i64, i32, i32, C.POINTER(C.c_int32),
+                                            C.POINTER(C.c_int64)]
+        L.dspark_gumbel_noise.argtypes = [vp, i32, i32, i64, vp, vp, vp]
+        L.dspark_status_string.argtypes = [i32]
+        L.dspark_status_string.restype = C.c_char_p
+        L.dspark_last_cuda_error.argtypes = []
+        L.dspark_last_cuda_error.restype = C.c_char_p
+        for f in ("dspark_quantize_w2", "dspark_walk", "dspark_walk_topk",
+                  "dspark_walk_from_host", "dspark_query_capacity", "dspark_gumbel_noise"):
+            getattr(L, f).restype = C.c_int32
+        _lib = L
+    return _lib
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libdspark must be contiguous")
+    return t.data_ptr()
+
+
+def _dev_ptr(t: torch.Tensor | None):
+    if t is not None and not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    return _ptr(t)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise DsparkError(status, what)
+
+
+def workspace_size(V: int, bs: int, K: int, top_k: int = 0) -> int:
+    return int(lib().dspark_walk_workspace_size(V, bs, K, top_k))
+
+
+def alloc_workspace(V: int, bs: int, K: int, top_k: int = 0, device=None) -> torch.Tensor:
+    """A zeroed workspace tensor (uint8) of the size the walk needs."""
+    n = workspace_size(V, bs, K, top_k)
+    return torch.zeros(n + 256, dtype=torch.uint8, device=device or "cuda")
+
+
+def _ws_view(ws: torch.Tensor):
+    """(pointer aligned to 256 bytes, usable bytes)."""
+    p = ws.data_ptr()
+    off = (-p) % 256
+    return p + off, ws.numel() - off
+
+
+def query_capacity(device: int, V: int, int8: bool, bs: int):
+    g, r = C.c_int32(), C.c_int64()
+    _check(lib().dspark_query_capacity(device, V, int(int8), bs, C.byref(g), C.byref(r)),
+           "dspark_query_capacity")
+    return g.value, r.value
+
+
+def quantize_w2(w2: torch.Tensor, q: torch.Tensor | None = None, scales: torch.Tensor | None = None,
+                status: torch.Tensor | None = None, stream=None):
+    """bf16 [V, 256] -> (int8 [V, 256], fp32 [V]) via dspark_quantize_w2."""
+    V = w2.shape[0]
+    q = q if q is not None else torch.empty((V, RANK), dtype=torch.int8, device=w2.device)
+    scales = scales if scales is not None else torch.empty(V, dtype=torch.float32, device=w2.device)
+    _check(lib().dspark_quantize_w2(_dev_ptr(w2), V, w2.shape[1], _dev_ptr(q), _dev_ptr(scales),
+                                    _dev_ptr(status), _stream(stream)), "dspark_quantize_w2")
+    return q, scales
+
+
+def make_args(base, w1, prev, tokens, workspace, *, w2=None, w2q=None, scales=None, seeds=None,
+              mode=GREEDY, temperature=1.0, top_k=0, logits=None, status=None, flags=0,
+              resident_rows_cap=-1, timeout_us=0) -> WalkArgs:
+    bs, K, V = base.shape
+    wsp, wsn = _ws_view(workspace)
+    return WalkArgs(
+        _dev_ptr(base), _dev_ptr(w1), _dev_ptr(w2), _dev_ptr(w2q), _dev_ptr(scales),
+        _dev_ptr(prev), _dev_ptr(seeds), V, w1.shape[1], bs, K, mode, temperature, top_k,
+        _dev_ptr(tokens), _dev_ptr(logits), wsp, wsn, _dev_ptr(status), flags,
+        resident_rows_cap, timeout_us)
+
+
+def walk(base, w1, prev, *, w2=None, w2q=None, scales=None, seeds=None, mode=GREEDY,
+         temperature=1.0, top_k=0, tokens=None, logits=None, want_logits=False, workspace=None,
+         status=None, flags=0, resident_rows_cap=-1, timeout_us=0, stream=None):
+    """Run dspark_walk (or dspark_walk_topk when top_k > 0). Returns (tokens, logits)."""
+    bs, K, V = base.shape
+    dev = base.device
+    if tokens is None:
+        tokens = torch.empty((bs, K), dtype=torch.int32, device=dev)
+    if want_logits and logits is None:
+        logits = torch.empty((bs, K, V), dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(V, bs, K, top_k, device=dev)
+    a = make_args(base, w1, prev, tokens, workspace, w2=w2, w2q=w2q, scales=scales,
+                  seeds=seeds, mode=mode, temperature=temperature, top_k=top_k, logits=logits,
+                  status=status, flags=flags, resident_rows_cap=resident_rows_cap,
+                  timeout_us=timeout_us)
+    _check(lib().dspark_walk(C.byref(a), _stream(stream)), "dspark_walk")
+    return tokens, logits
+
+
+def walk_args_call(args: WalkArgs, stream=None, topk: bool = False) -> int:
+    """Call dspark_walk / dspark_walk_topk on prepared arguments; returns the status."""
+    f = lib().dspark_walk_topk if topk else lib().dspark_walk
+    return int(f(C.byref(args), _stream(stream)))
+
+
+def walk_from_host(args: WalkArgs, base_host, prev_host, seeds_host, tokens_host,
+                   logits_host=None, stream=None):
+    _check(lib().dspark_walk_from_host(C.byref(args), _ptr(base_host), _ptr(prev_host),
+                                       _ptr(seeds_host), _ptr(tokens_host), _ptr(logits_host),
+                                       _stream(stream)), "dspark_walk_from_host")
+
+
+def gumbel_noise(seeds: torch.Tensor, K: int, V: int, stream=None):
+    """(words uint32 as int32, gumbel fp32), each [bs, K, V]."""
+    bs = seeds.shape[0]
+    words = torch.empty((bs, K, V), dtype=torch.int32, device=seeds.device)
+    g = torch.empty((bs, K, V), dtype=torch.float32, device=seeds.device)
+    _check(lib().dspark_gumbel_noise(_dev_ptr(seeds), bs, K, V, _dev_ptr(words), _dev_ptr(g),
+                                     _stream(stream)), "dspark_gumbel_noise")
+    return words, g

@@ -1,0 +1,298 @@
+// The C ABI of libdspark.so: argument checks, the cached device capacity query, the
+// launch plan (cooperative grid, shared-memory-resident W2 rows) and the launches.
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "walk_params.cuh"
+
+namespace dspark {
+
+const void* walk_cc_kernel_ptr(bool int8, bool prob, bool logits);
+const void* topk_walk_kernel_ptr(bool prob, bool logits);
+cudaError_t launch_topk_select(const uint16_t* base, int64_t V, int k, int rows, int32_t* cand,
+                               uint16_t* logits, cudaStream_t stream);
+cudaError_t launch_quantize_w2(const uint16_t* w2, int64_t V, int8_t* q, float* scales,
+                               int32_t* status_dev, cudaStream_t stream);
+cudaError_t launch_gumbel_noise(const uint64_t* seeds, int bs, int K, int64_t V, uint32_t* words,
+                                float* gumbel, cudaStream_t stream);
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+int32_t cuda_fail(cudaError_t e, const char* where) {
+  std::snprintf(g_last_error, sizeof g_last_error, "%s: %s", where, cudaGetErrorString(e));
+  return DSPARK_ERR_CUDA;
+}
+
+struct DeviceCaps {
+  bool valid = false;
+  int sms = 0;
+  int smem_optin = 0;
+  int coop = 0;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceCaps g_caps[kMaxDevices];
+std::mutex g_caps_mu;
+
+int32_t get_caps(int device, DeviceCaps* out) {
+  if (device < 0 || device >= kMaxDevices) return DSPARK_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_caps_mu);
+  DeviceCaps& c = g_caps[device];
+  if (!c.valid) {
+    cudaError_t e;
+    if ((e = cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    if ((e = cudaDeviceGetAttribute(&c.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(smem opt-in)");
+    if ((e = cudaDeviceGetAttribute(&c.coop, cudaDevAttrCooperativeLaunch, device)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(cooperative launch)");
+    c.valid = true;
+  }
+  *out = c;
+  return DSPARK_OK;
+}
+
+int32_t current_caps(DeviceCaps* caps) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  return get_caps(dev, caps);
+}
+
+struct Plan {
+  int grid;
+  int resident_rows;  // per CTA
+  size_t smem;
+};
+
+// One CTA per SM; the shared memory left after the fixed working set holds W2 rows.
+Plan plan_dense(const DeviceCaps& caps, int64_t V, bool int8, int bs, int cap_rows) {
+  Plan pl{};
+  pl.grid = caps.sms;
+  const int row_bytes = int8 ? kRank : 2 * kRank;
+  const size_t fixed = walk_cc_fixed_smem(bs);
+  const int64_t per_cta = (V + pl.grid - 1) / pl.grid;
+  int64_t rows = caps.smem_optin > static_cast<int>(fixed)
+                     ? (static_cast<int64_t>(caps.smem_optin) - static_cast<int64_t>(fixed)) / row_bytes
+                     : 0;
+  rows = rows & ~31LL;
+  const int64_t need = (per_cta + 31) & ~31LL;
+  if (rows > need) rows = need;
+  if (cap_rows >= 0 && rows > cap_rows) rows = cap_rows & ~31;
+  pl.resident_rows = static_cast<int>(rows);
+  pl.smem = fixed + static_cast<size_t>(rows) * row_bytes;
+  return pl;
+}
+
+int32_t check_common(const dspark_walk_args* a) {
+  if (!a) return DSPARK_ERR_INVALID_ARG;
+  if (!a->base_logits || !a->w1 || !a->prev_tokens || !a->draft_tokens) return DSPARK_ERR_INVALID_ARG;
+  if (a->rank != DSPARK_RANK) return DSPARK_ERR_INVALID_ARG;
+  if (a->V <= 0 || a->V > DSPARK_MAX_V) return DSPARK_ERR_INVALID_ARG;
+  if (a->bs < 1 || a->bs > DSPARK_MAX_BS || a->K < 1 || a->K > DSPARK_MAX_K) return DSPARK_ERR_INVALID_ARG;
+  if (a->mode != DSPARK_GREEDY && a->mode != DSPARK_PROBABILISTIC) return DSPARK_ERR_INVALID_ARG;
+  if (a->mode == DSPARK_PROBABILISTIC) {
+    if (!a->seeds) return DSPARK_ERR_INVALID_ARG;
+    if (!(a->temperature > 0.f) || !(a->temperature < 3.4e38f)) return DSPARK_ERR_INVALID_ARG;
+  }
+  const bool have_bf16 = a->w2 != nullptr;
+  const bool have_int8 = a->w2q != nullptr;
+  if (have_bf16 == have_int8) return DSPARK_ERR_INVALID_ARG;
+  if (have_int8 && !a->w2_scales) return DSPARK_ERR_INVALID_ARG;
+  if (a->top_k < 0 || a->top_k > a->V) return DSPARK_ERR_INVALID_ARG;
+  if (!a->workspace) return DSPARK_ERR_WORKSPACE;
+  if (a->workspace_bytes < ws_total(a->K, a->bs, a->top_k)) return DSPARK_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return DSPARK_ERR_WORKSPACE;
+  // 16-byte vector loads of W1 / W2 rows
+  if ((reinterpret_cast<uintptr_t>(a->w1) | reinterpret_cast<uintptr_t>(a->w2) |
+       reinterpret_cast<uintptr_t>(a->w2q)) & 15u)
+    return DSPARK_ERR_INVALID_ARG;
+  return DSPARK_OK;
+}
+
+StepSync make_sync(const dspark_walk_args* a, int grid) {
+  StepSync s{};
+  char* ws = static_cast<char*>(a->workspace);
+  s.hdr = reinterpret_cast<WsHeader*>(ws);
+  s.counters = reinterpret_cast<uint32_t*>(ws + ws_counters_off());
+  s.slots = reinterpret_cast<uint64_t*>(ws + ws_slots_off(a->K));
+  s.status_dev = a->status_dev;
+  s.grid = static_cast<uint32_t>(grid);
+  s.timeout_ns = 1000ull * (a->timeout_us ? a->timeout_us : 1000000u);
+  s.flags = a->flags;
+  return s;
+}
+
+WalkParams make_params(const dspark_walk_args* a, int grid, int resident_rows) {
+  WalkParams p{};
+  p.base = a->base_logits;
+  p.w1 = a->w1;
+  p.w2 = a->w2;
+  p.w2q = a->w2q;
+  p.scales = a->w2_scales;
+  p.prev = a->prev_tokens;
+  p.seeds = a->seeds;
+  p.tokens = a->draft_tokens;
+  p.logits = a->draft_logits;
+  p.cand = reinterpret_cast<const int32_t*>(static_cast<char*>(a->workspace) + ws_cand_off(a->K, a->bs));
+  p.V = a->V;
+  p.bs = a->bs;
+  p.K = a->K;
+  p.top_k = a->top_k;
+  p.temperature = a->temperature;
+  p.temp_is_one = a->temperature == 1.0f ? 1 : 0;
+  p.resident_rows = resident_rows;
+  p.sync = make_sync(a, grid);
+  return p;
+}
+
+int32_t launch_coop(const void* fn, int grid, size_t smem, WalkParams& p, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kWalkThreads, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  if (per_sm < 1) return DSPARK_ERR_COOP_TOO_LARGE;
+  void* args[] = {&p};
+  e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kWalkThreads), args, smem, stream);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    cudaGetLastError();
+    return DSPARK_ERR_COOP_TOO_LARGE;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchCooperativeKernel");
+  return DSPARK_OK;
+}
+
+}  // namespace
+}  // namespace dspark
+
+using namespace dspark;
+
+extern "C" {
+
+const char* dspark_status_string(int32_t status) {
+  switch (status) {
+    case DSPARK_OK: return "ok";
+    case DSPARK_ERR_INVALID_ARG: return "invalid argument";
+    case DSPARK_ERR_UNSUPPORTED: return "unsupported combination";
+    case DSPARK_ERR_CUDA: return "CUDA runtime error";
+    case DSPARK_ERR_COOP_TOO_LARGE: return "cooperative grid cannot be co-resident";
+    case DSPARK_ERR_TIMEOUT: return "device wait timed out";
+    case DSPARK_ERR_BAD_TOKEN: return "previous token outside [0, V)";
+    case DSPARK_ERR_NONFINITE_W2: return "non-finite W2 entry";
+    case DSPARK_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    default: return "unknown status";
+  }
+}
+
+const char* dspark_last_cuda_error(void) { return g_last_error; }
+
+size_t dspark_walk_workspace_size(int64_t V, int32_t bs, int32_t K, int32_t top_k) {
+  (void)V;
+  if (bs < 1 || K < 1 || top_k < 0) return 0;
+  return ws_total(K, bs, top_k);
+}
+
+int32_t dspark_query_capacity(int32_t device, int64_t V, int32_t w2_is_int8, int32_t bs,
+                              int32_t* grid_ctas, int64_t* resident_rows) {
+  if (V <= 0 || bs < 1 || bs > DSPARK_MAX_BS) return DSPARK_ERR_INVALID_ARG;
+  DeviceCaps caps;
+  int32_t st = get_caps(device, &caps);
+  if (st != DSPARK_OK) return st;
+  const Plan pl = plan_dense(caps, V, w2_is_int8 != 0, bs, -1);
+  if (grid_ctas) *grid_ctas = pl.grid;
+  if (resident_rows) {
+    int64_t tot = 0;
+    for (int c = 0; c < pl.grid; ++c) {
+      const int64_t n = (static_cast<int64_t>(c + 1) * V / pl.grid) - (static_cast<int64_t>(c) * V / pl.grid);
+      tot += n < (pl.resident_rows) ? (n & ~31LL) : pl.resident_rows;
+    }
+    *resident_rows = tot;
+  }
+  return DSPARK_OK;
+}
+
+int32_t dspark_quantize_w2(const uint16_t* w2, int64_t V, int32_t rank, int8_t* w2q, float* scales,
+                           int32_t* status_dev, dspark_stream_t stream) {
+  if (!w2 || !w2q || !scales || V <= 0 || rank != DSPARK_RANK) return DSPARK_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(w2) & 15u) || (reinterpret_cast<uintptr_t>(w2q) & 7u))
+    return DSPARK_ERR_INVALID_ARG;
+  const int64_t blocks = (V + 7) / 8;
+  if (blocks > 0x7FFFFFFF) return DSPARK_ERR_INVALID_ARG;
+  cudaError_t e = launch_quantize_w2(w2, V, w2q, scales, status_dev, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSPARK_OK : cuda_fail(e, "quantize_w2_kernel launch");
+}
+
+int32_t dspark_walk_topk(const dspark_walk_args* a, dspark_stream_t stream) {
+  int32_t st = check_common(a);
+  if (st != DSPARK_OK) return st;
+  if (a->top_k < 1) return DSPARK_ERR_INVALID_ARG;
+  if (!a->w2) return DSPARK_ERR_UNSUPPORTED;
+  DeviceCaps caps;
+  if ((st = current_caps(&caps)) != DSPARK_OK) return st;
+  if (!caps.coop) return DSPARK_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int rows = a->bs * a->K;
+  WalkParams p = make_params(a, caps.sms, 0);
+  cudaError_t e = launch_topk_select(a->base_logits, a->V, a->top_k, rows,
+                                     const_cast<int32_t*>(p.cand), a->draft_logits, s);
+  if (e != cudaSuccess) return cuda_fail(e, "topk_select_kernel launch");
+  const size_t smem = static_cast<size_t>(a->bs) * kRank * 4 + 64 * 4 + kWalkWarps * 8 + 64 + 256;
+  const bool prob = a->mode == DSPARK_PROBABILISTIC, lg = a->draft_logits != nullptr;
+  const void* fn = topk_walk_kernel_ptr(prob, lg);
+  return launch_coop(fn, caps.sms, smem, p, s);
+}
+
+int32_t dspark_walk(const dspark_walk_args* a, dspark_stream_t stream) {
+  int32_t st = check_common(a);
+  if (st != DSPARK_OK) return st;
+  if (a->top_k > 0) return dspark_walk_topk(a, stream);
+  DeviceCaps caps;
+  if ((st = current_caps(&caps)) != DSPARK_OK) return st;
+  if (!caps.coop) return DSPARK_ERR_UNSUPPORTED;
+  const bool int8 = a->w2q != nullptr;
+  const Plan pl = plan_dense(caps, a->V, int8, a->bs, a->resident_rows_cap);
+  WalkParams p = make_params(a, pl.grid, pl.resident_rows);
+  const bool lg = a->draft_logits != nullptr;
+  const void* fn = walk_cc_kernel_ptr(int8, a->mode == DSPARK_PROBABILISTIC, lg);
+  return launch_coop(fn, pl.grid, pl.smem, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int32_t dspark_walk_from_host(const dspark_walk_args* a, const uint16_t* base_host,
+                              const int32_t* prev_host, const uint64_t* seeds_host,
+                              int32_t* tokens_host, uint16_t* logits_host, dspark_stream_t stream) {
+  int32_t st = check_common(a);
+  if (st != DSPARK_OK) return st;
+  if (!base_host || !prev_host || !tokens_host) return DSPARK_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t nb = static_cast<size_t>(a->bs) * a->K * static_cast<size_t>(a->V) * 2;
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(const_cast<uint16_t*>(a->base_logits), base_host, nb, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "copy base_logits to device");
+  if ((e = cudaMemcpyAsync(const_cast<int32_t*>(a->prev_tokens), prev_host, 4ull * a->bs, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "copy prev_tokens to device");
+  if (seeds_host && a->seeds &&
+      (e = cudaMemcpyAsync(const_cast<uint64_t*>(a->seeds), seeds_host, 8ull * a->bs, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "copy seeds to device");
+  if ((st = dspark_walk(a, stream)) != DSPARK_OK) return st;
+  if ((e = cudaMemcpyAsync(tokens_host, a->draft_tokens, 4ull * a->bs * a->K, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(e, "copy draft_tokens to host");
+  if (logits_host && a->draft_logits &&
+      (e = cudaMemcpyAsync(logits_host, a->draft_logits, nb, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(e, "copy draft_logits to host");
+  return DSPARK_OK;
+}
+
+int32_t dspark_gumbel_noise(const uint64_t* seeds, int32_t bs, int32_t K, int64_t V, uint32_t* words,
+                            float* gumbel, dspark_stream_t stream) {
+  if (!seeds || bs < 1 || K < 1 || V <= 0 || (!words && !gumbel)) return DSPARK_ERR_INVALID_ARG;
+  cudaError_t e = launch_gumbel_noise(seeds, bs, K, V, words, gumbel, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSPARK_OK : cuda_fail(e, "gumbel_noise_kernel launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,217 @@
+// Device helpers shared by the walk kernels: bf16 handling, Philox4x32-10 Gumbel
+// noise, the orderable argmax word, the device status word and the bounded
+// grid-wide step barrier.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+constexpr int kRank = DSPARK_RANK;
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+// ---------------------------------------------------------------- bf16
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// ---------------------------------------------------------------- Philox / Gumbel
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two 32x32->64
+// multiplies whose halves are xored with the other two words and the round key; the
+// key advances by the Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// The four words for vocabulary entries 4m .. 4m+3 of draft position i, row b.
+__device__ __forceinline__ uint4 philox_block(uint64_t seed, int b, int i, uint32_t m) {
+  return philox4x32_10(make_uint4(m, static_cast<uint32_t>(i), static_cast<uint32_t>(b), 0u),
+                       static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+}
+
+__device__ __forceinline__ uint32_t uint4_get(const uint4& w, int j) {
+  return j == 0 ? w.x : j == 1 ? w.y : j == 2 ? w.z : w.w;
+}
+
+// u = (2 * (w >> 9) + 1) * 2^-24 lies strictly inside (0, 1) and is exact in fp32;
+// g = -log(-log(u)) with the full-precision logf (its accuracy near u -> 1 matters,
+// since that is where the largest noise values come from).
+__device__ __forceinline__ float gumbel_from_word(uint32_t w) {
+  const float u = static_cast<float>(2u * (w >> 9) + 1u) * 5.9604644775390625e-08f;
+  return -logf(-logf(u));
+}
+
+// ---------------------------------------------------------------- argmax words
+
+// Monotone map of fp32 to uint32 for the max reduction. NaN maps above every number
+// (so a NaN wins) and -0 maps to the key of +0 (so they tie).
+__device__ __forceinline__ uint32_t order_key(float x) {
+  uint32_t u = __float_as_uint(x);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0xFFFFFFFFu;  // NaN
+  if ((u & 0x7FFFFFFFu) == 0u) u = 0u;                         // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// One 64-bit word per candidate: key in the high half, the complement of the index
+// in the low half, so the integer maximum is the largest key and, among equal keys,
+// the smallest index (torch.argmax order).
+__device__ __forceinline__ uint64_t pack_best(uint32_t key, uint32_t idx) {
+  return (static_cast<uint64_t>(key) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - idx);
+}
+__device__ __forceinline__ int32_t unpack_idx(uint64_t word) {
+  return static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(word));
+}
+__device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+
+__device__ __forceinline__ uint64_t warp_max64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = umax64(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+// ---------------------------------------------------------------- status and memory
+
+__device__ __forceinline__ void report(int32_t* status_dev, int32_t code) {
+  if (status_dev) atomicCAS(status_dev, 0, code);
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- workspace
+
+// Workspace layout (bytes), shared by the dense and the top-k walk:
+//   [0, 256)                 header: abort flag, exit counter
+//   [256, 256 + 128*K)       per-step arrival counters, one 128-byte line each
+//   next 8*K*bs              per-step argmax words slot[i][b]
+//   next (aligned to 256)    top-k candidate lists int32 [bs, K, top_k]
+struct WsHeader {
+  uint32_t abort;
+  uint32_t exit_count;
+};
+constexpr size_t kWsHeader = 256;
+constexpr size_t kWsCounterStride = 128;
+
+__host__ __device__ inline size_t ws_counters_off() { return kWsHeader; }
+__host__ __device__ inline size_t ws_slots_off(int K) {
+  return kWsHeader + kWsCounterStride * static_cast<size_t>(K);
+}
+__host__ __device__ inline size_t ws_cand_off(int K, int bs) {
+  size_t end = ws_slots_off(K) + 8ull * K * bs;
+  return (end + 255) & ~static_cast<size_t>(255);
+}
+__host__ __device__ inline size_t ws_total(int K, int bs, int top_k) {
+  return ws_cand_off(K, bs) + 4ull * bs * K * static_cast<size_t>(top_k);
+}
+
+// ---------------------------------------------------------------- step barrier
+
+struct StepSync {
+  WsHeader* hdr;
+  uint32_t* counters;  // stride kWsCounterStride bytes
+  uint64_t* slots;     // [K][bs]
+  int32_t* status_dev;
+  uint32_t grid;
+  uint64_t timeout_ns;
+  uint32_t flags;
+
+  __device__ __forceinline__ uint32_t* counter(int i) const {
+    return reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(counters) + kWsCounterStride * i);
+  }
+};
+
+// Arrive at step i's barrier and wait for the whole grid. Every thread of the CTA
+// calls it; the argmax atomics of the CTA must have been issued before. Returns
+// false when the wait gave up (timeout or another CTA's abort); the caller then
+// returns from the kernel. The wait is bounded by timeout_ns of wall-clock time.
+__device__ __forceinline__ bool grid_step_barrier(const StepSync& s, int i, bool skip_arrival,
+                                                  int* sh_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    uint32_t* ctr = s.counter(i);
+    __threadfence();
+    if (!skip_arrival) atomicAdd(ctr, 1u);
+    uint64_t t0 = 0;
+    uint32_t it = 0;
+    while (ld_acquire_u32(ctr) < s.grid) {
+      if ((++it & 63u) == 0u) {
+        if (t0 == 0) t0 = globaltimer_ns();
+        if (*reinterpret_cast<volatile uint32_t*>(&s.hdr->abort) != 0u) { ok = 0; break; }
+        if (globaltimer_ns() - t0 > s.timeout_ns) {
+          atomicExch(&s.hdr->abort, 1u);
+          report(s.status_dev, DSPARK_ERR_TIMEOUT);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    __threadfence();
+    *sh_flag = ok;
+  }
+  __syncthreads();
+  return *sh_flag != 0;
+}
+
+// Reset-behind: once every CTA has passed step i+1's barrier nobody reads step i's
+// counter or slots again, so CTA 0 zeroes them for the next call. The last CTA to
+// finish zeroes the final step's state and the exit counter.
+__device__ __forceinline__ void reset_behind(const StepSync& s, int i, int bs) {
+  if (blockIdx.x == 0 && i >= 1) {
+    for (int t = threadIdx.x; t < bs; t += blockDim.x) s.slots[static_cast<size_t>(i - 1) * bs + t] = 0ull;
+    if (threadIdx.x == 0) *s.counter(i - 1) = 0u;
+  }
+}
+
+__device__ __forceinline__ void finish_walk(const StepSync& s, int K, int bs, int* sh_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    *sh_flag = (atomicAdd(&s.hdr->exit_count, 1u) == s.grid - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (*sh_flag) {
+    __threadfence();
+    for (int t = threadIdx.x; t < bs; t += blockDim.x) s.slots[static_cast<size_t>(K - 1) * bs + t] = 0ull;
+    if (threadIdx.x == 0) {
+      *s.counter(K - 1) = 0u;
+      s.hdr->exit_count = 0u;
+    }
+  }
+}
+
+}  // namespace dspark

@@ -1,0 +1,355 @@
+// Full-vocabulary Markov draft walk on CUDA cores: one persistent cooperative kernel
+// for all K draft positions (vLLM PR #62958, "Overview": the whole walk in one
+// cooperative kernel, W2 mostly resident in shared memory, the rest streamed from L2,
+// one packed atomic per step for the cross-CTA argmax).
+//
+// Work split. CTA c owns the contiguous vocabulary slice [c*V/G, (c+1)*V/G). The first
+// `resident_rows` rows of the slice are copied into shared memory while draft position
+// 0 streams them from HBM, and are read from shared memory at every later position;
+// the remaining rows are re-read from global memory (L2) at each position.
+//
+// Contraction. Eight lanes share one W2 row; lane j owns the 16-byte chunks j, j+8
+// (int8: 32 values) or j, j+8, j+16, j+24 (bf16: 32 values) of every row, so the
+// embedding slice it multiplies with stays in registers. Each 8-lane group handles 8
+// rows at a time and a 3-stage xor butterfly leaves lane j with the total of row j.
+//   * int8 W2: the embedding row e is scaled by a power of two 2^s to a 24-bit
+//     integer and split into one signed and two unsigned byte limbs; dp4a then gives
+//     the exact integer sum_k q[v,k] * round(e_k 2^s), and the bias is
+//     scale_v * 2^-s * sum. bf16 e has 8 significant bits, so every entry within
+//     2^16 of max|e| is represented exactly; the result is at least as accurate as an
+//     fp32 accumulation and is independent of summation order.
+//   * bf16 W2: fp32 FMA in a fixed order (lane-local k order, then the butterfly),
+//     identical for every row, so identical rows give identical bias values.
+//
+// Per-position cross-CTA argmax: each CTA reduces its (orderable key, first index)
+// word per request row, issues one 64-bit atomicMax into slot[i][b], and the grid
+// meets at a bounded barrier; then every CTA reads the winning token.
+#include <cstdint>
+
+#include "common.cuh"
+#include "walk_params.cuh"
+
+namespace dspark {
+
+namespace {
+
+__device__ __forceinline__ int dp4a_ss(int a, int b, int c) {
+  int d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_su(int a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Reduce-scatter of 8 per-row partials over the 8 lanes of a group: afterwards lane
+// j (j = lane & 7) holds the sum over the group of partial j in v[0]. Every row's
+// sum is formed by the same pairing tree (commutative adds only), so identical rows
+// give identical results.
+template <typename T>
+__device__ __forceinline__ T butterfly8(T (&v)[8], int lane) {
+  const bool u4 = lane & 4, u2 = lane & 2, u1 = lane & 1;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const T send = u4 ? v[t] : v[t + 4];
+    const T keep = u4 ? v[t + 4] : v[t];
+    v[t] = keep + __shfl_xor_sync(kFull, send, 4);
+  }
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const T send = u2 ? v[t] : v[t + 2];
+    const T keep = u2 ? v[t + 2] : v[t];
+    v[t] = keep + __shfl_xor_sync(kFull, send, 2);
+  }
+  const T send = u1 ? v[0] : v[1];
+  const T keep = u1 ? v[1] : v[0];
+  return keep + __shfl_xor_sync(kFull, send, 1);
+}
+
+__device__ __forceinline__ uint4 ld_row_chunk(const unsigned char* row_global, int chunk) {
+  return __ldg(reinterpret_cast<const uint4*>(row_global) + chunk);
+}
+
+// Limbs of the 16 integers of one chunk: hi (signed byte), mid and lo (unsigned).
+struct Limbs {
+  int hi[4];
+  uint32_t mid[4], lo[4];
+};
+
+__device__ __forceinline__ void make_limbs(const uint16_t* e16, int shift, Limbs& L) {
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t h = 0, m = 0, l = 0;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float x = bf16_to_f32(e16[4 * w + t]);
+      const int xi = __float2int_rn(ldexpf(x, shift));
+      h |= (static_cast<uint32_t>(xi >> 16) & 0xFFu) << (8 * t);
+      m |= (static_cast<uint32_t>(xi >> 8) & 0xFFu) << (8 * t);
+      l |= (static_cast<uint32_t>(xi) & 0xFFu) << (8 * t);
+    }
+    L.hi[w] = static_cast<int>(h);
+    L.mid[w] = m;
+    L.lo[w] = l;
+  }
+}
+
+__device__ __forceinline__ void dot_int8_chunk(const uint4& q, const Limbs& L, int& h, int& m,
+                                               int& l) {
+  const int qw[4] = {static_cast<int>(q.x), static_cast<int>(q.y), static_cast<int>(q.z),
+                     static_cast<int>(q.w)};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    h = dp4a_ss(qw[w], L.hi[w], h);
+    m = dp4a_su(qw[w], L.mid[w], m);
+    l = dp4a_su(qw[w], L.lo[w], l);
+  }
+}
+
+__device__ __forceinline__ float dot_int8_chunk_f32(const uint4& q, const float* e, float acc) {
+  const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w)
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int qi = static_cast<int>(static_cast<int8_t>((qw[w] >> (8 * t)) & 0xFFu));
+      acc = __fmaf_rn(static_cast<float>(qi), e[4 * w + t], acc);
+    }
+  return acc;
+}
+
+__device__ __forceinline__ float dot_bf16_chunk(const uint4& q, const float* e, float acc) {
+  const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    acc = __fmaf_rn(bf16_lo(qw[w]), e[2 * w], acc);
+    acc = __fmaf_rn(bf16_hi(qw[w]), e[2 * w + 1], acc);
+  }
+  return acc;
+}
+
+// Score of one vocabulary entry and its argmax word.
+template <bool PROB, bool LOGITS>
+__device__ __forceinline__ uint64_t score_entry(const WalkParams& p, int b, int i, int64_t v,
+                                                float bias, uint64_t seed) {
+  const size_t o = (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v;
+  const float l = __fadd_rn(bf16_to_f32(p.base[o]), bias);
+  if (LOGITS) p.logits[o] = f32_to_bf16_bits(l);
+  float s = l;
+  if (PROB) {
+    const float lb = bf16_to_f32(f32_to_bf16_bits(l));
+    const float x = p.temp_is_one ? lb : __fdiv_rn(lb, p.temperature);
+    const uint4 w = philox_block(seed, b, i, static_cast<uint32_t>(v >> 2));
+    s = __fadd_rn(x, gumbel_from_word(uint4_get(w, static_cast<int>(v & 3))));
+  }
+  return pack_best(order_key(s), static_cast<uint32_t>(v));
+}
+
+}  // namespace
+
+template <bool INT8, bool PROB, bool LOGITS>
+__global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int kRowBytes = INT8 ? kRank : 2 * kRank;
+  const int G = gridDim.x;
+  const int cta = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int j8 = lane & 7, grp = lane >> 3;
+
+  const int64_t v0 = static_cast<int64_t>(cta) * p.V / G;
+  const int64_t v1 = static_cast<int64_t>(cta + 1) * p.V / G;
+  const int n = static_cast<int>(v1 - v0);
+  const int res = min(p.resident_rows, n & ~31);
+
+  unsigned char* w2s = smem;
+  uint16_t* e_s = reinterpret_cast<uint16_t*>(smem + static_cast<size_t>(p.resident_rows) * kRowBytes);
+  int* sh_shift = reinterpret_cast<int*>(e_s + static_cast<size_t>(p.bs) * kRank);
+  int* prev_s = sh_shift + 64;
+  uint64_t* red = reinterpret_cast<uint64_t*>(prev_s + 64);
+  int* flag = reinterpret_cast<int*>(red + kWalkWarps);
+
+  const unsigned char* w2g = INT8 ? reinterpret_cast<const unsigned char*>(p.w2q)
+                                  : reinterpret_cast<const unsigned char*>(p.w2);
+  w2g += static_cast<size_t>(v0) * kRowBytes;
+
+  const bool skip0 = (p.sync.flags & DSPARK_FLAG_SKIP_ARRIVAL_CTA0) && cta == 0;
+
+  for (int t = threadIdx.x; t < p.bs; t += blockDim.x) {
+    const int32_t tok = p.prev[t];
+    const bool ok = tok >= 0 && static_cast<int64_t>(tok) < p.V;
+    prev_s[t] = ok ? tok : -1;
+    if (!ok && cta == 0) report(p.sync.status_dev, DSPARK_ERR_BAD_TOKEN);
+  }
+  bool filled = false;
+
+  for (int i = 0; i < p.K; ++i) {
+    __syncthreads();
+    // Markov embeddings of the previous tokens (bf16 rows into shared memory) and,
+    // for int8 W2, the power-of-two shift that makes each row a 24-bit integer vector.
+    for (int b = warp; b < p.bs; b += kWalkWarps) {
+      const int tok = prev_s[b];
+      float amax = 0.f;
+      if (tok >= 0) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.w1 + static_cast<size_t>(tok) * kRank) + lane);
+        reinterpret_cast<uint4*>(e_s + static_cast<size_t>(b) * kRank)[lane] = w;
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          amax = fmaxf(amax, fabsf(bf16_lo(ww[t])));
+          amax = fmaxf(amax, fabsf(bf16_hi(ww[t])));
+          if (!isfinite(bf16_lo(ww[t])) || !isfinite(bf16_hi(ww[t]))) amax = __int_as_float(0x7F800000);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+      if (lane == 0) {
+        int shift = 0;
+        if (!isfinite(amax)) {
+          shift = 1 << 30;  // marks a non-finite embedding row: fp32 fallback
+        } else if (amax > 0.f) {
+          int ex;
+          frexpf(amax, &ex);  // amax = f * 2^ex, f in [0.5, 1)
+          shift = 23 - ex;    // amax * 2^shift in [2^22, 2^23)
+        }
+        sh_shift[b] = shift;
+      }
+    }
+    __syncthreads();
+
+    for (int b = 0; b < p.bs; ++b) {
+      if (prev_s[b] < 0) continue;  // uniform over the CTA
+      const uint64_t seed = PROB ? p.seeds[b] : 0ull;
+      const uint16_t* eb = e_s + static_cast<size_t>(b) * kRank;
+      const int shift = sh_shift[b];
+      const bool float_path = INT8 && shift == (1 << 30);
+      const bool fill = !filled;
+
+      Limbs LA, LB;
+      float ef[32];
+      if (INT8 && !float_path) {
+        make_limbs(eb + 16 * j8, shift, LA);
+        make_limbs(eb + 16 * (j8 + 8), shift, LB);
+      } else {
+        const int cw = INT8 ? 16 : 8;  // values per chunk
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int chunk = j8 + 8 * (c / cw);
+          ef[c] = bf16_to_f32(eb[chunk * cw + (c % cw)]);
+        }
+      }
+
+      uint64_t best = 0ull;
+      // Warp-blocks of 32 rows: warp w takes blocks w, w + 16, ...
+      for (int r0 = 32 * warp; r0 < n; r0 += 32 * kWalkWarps) {
+        const bool from_smem = (i > 0 || !fill) && (r0 + 32 <= res);
+        const bool store_smem = fill && (r0 + 32 <= res);
+        const int rbase = r0 + 8 * grp;
+        float fpart[8];
+        int hpart[8], mpart[8];
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) {
+          const int r = rbase + rr;
+          constexpr int kChunks = INT8 ? 2 : 4;
+          uint4 q[kChunks];
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) {
+            if (r < n) {
+              if (from_smem)
+                q[c] = reinterpret_cast<const uint4*>(w2s + static_cast<size_t>(r) * kRowBytes)[j8 + 8 * c];
+              else
+                q[c] = ld_row_chunk(w2g + static_cast<size_t>(r) * kRowBytes, j8 + 8 * c);
+              if (store_smem)
+                reinterpret_cast<uint4*>(w2s + static_cast<size_t>(r) * kRowBytes)[j8 + 8 * c] = q[c];
+            } else {
+              q[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+          if (INT8 && !float_path) {
+            int h = 0, m = 0, l = 0;
+            dot_int8_chunk(q[0], LA, h, m, l);
+            dot_int8_chunk(q[1], LB, h, m, l);
+            hpart[rr] = h;
+            mpart[rr] = m * 256 + l;
+          } else if (INT8) {
+            float a = 0.f;
+            a = dot_int8_chunk_f32(q[0], ef, a);
+            a = dot_int8_chunk_f32(q[1], ef + 16, a);
+            fpart[rr] = a;
+          } else {
+            float a = 0.f;
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) a = dot_bf16_chunk(q[c], ef + 8 * c, a);
+            fpart[rr] = a;
+          }
+        }
+        float bias_raw;
+        if (INT8 && !float_path) {
+          const int H = butterfly8(hpart, lane);
+          const int M = butterfly8(mpart, lane);
+          bias_raw = __fadd_rn(__fmul_rn(static_cast<float>(H), 65536.f), static_cast<float>(M));
+        } else {
+          bias_raw = butterfly8(fpart, lane);
+        }
+        const int r = rbase + j8;
+        if (r < n) {
+          const int64_t v = v0 + r;
+          // int8: scale_v * 2^-shift * sum; the power of two is applied last so that a
+          // tiny embedding row underflows gracefully instead of through 2^-shift.
+          float bias = bias_raw;
+          if (INT8) {
+            bias = __fmul_rn(bias_raw, p.scales[v]);
+            if (!float_path) bias = ldexpf(bias, -shift);
+          }
+          best = umax64(best, score_entry<PROB, LOGITS>(p, b, i, v, bias, seed));
+        }
+      }
+      // CTA argmax for row b, then one atomic into this position's slot.
+      best = warp_max64(best);
+      if (lane == 0) red[warp] = best;
+      __syncthreads();
+      if (warp == 0) {
+        uint64_t x = lane < kWalkWarps ? red[lane] : 0ull;
+        x = warp_max64(x);
+        if (lane == 0 && x != 0ull) atomicMax(reinterpret_cast<unsigned long long*>(p.sync.slots + static_cast<size_t>(i) * p.bs + b),
+                                              static_cast<unsigned long long>(x));
+      }
+      filled = true;
+      __syncthreads();
+    }
+
+    if (!grid_step_barrier(p.sync, i, skip0 && i == 0, flag)) return;
+    for (int t = threadIdx.x; t < p.bs; t += blockDim.x) {
+      int tok = -1;
+      if (prev_s[t] >= 0) tok = unpack_idx(ld_relaxed_u64(p.sync.slots + static_cast<size_t>(i) * p.bs + t));
+      prev_s[t] = tok;
+      if (cta == 0) p.tokens[static_cast<size_t>(t) * p.K + i] = tok;
+    }
+    reset_behind(p.sync, i, p.bs);
+  }
+  finish_walk(p.sync, p.K, p.bs, flag);
+}
+
+#define DSPARK_INST(I, P, L) template __global__ void walk_cc_kernel<I, P, L>(const WalkParams);
+DSPARK_INST(true, false, false)
+DSPARK_INST(true, false, true)
+DSPARK_INST(true, true, false)
+DSPARK_INST(true, true, true)
+DSPARK_INST(false, false, false)
+DSPARK_INST(false, false, true)
+DSPARK_INST(false, true, false)
+DSPARK_INST(false, true, true)
+#undef DSPARK_INST
+
+// Host-side handle of the kernel variant for (W2 format, mode, draft_logits).
+const void* walk_cc_kernel_ptr(bool int8, bool prob, bool logits) {
+  if (int8) {
+    if (prob) return logits ? (const void*)walk_cc_kernel<true, true, true> : (const void*)walk_cc_kernel<true, true, false>;
+    return logits ? (const void*)walk_cc_kernel<true, false, true> : (const void*)walk_cc_kernel<true, false, false>;
+  }
+  if (prob) return logits ? (const void*)walk_cc_kernel<false, true, true> : (const void*)walk_cc_kernel<false, true, false>;
+  return logits ? (const void*)walk_cc_kernel<false, false, true> : (const void*)walk_cc_kernel<false, false, false>;
+}
+
+}  // namespace dspark

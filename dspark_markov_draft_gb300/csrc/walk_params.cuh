@@ -1,0 +1,42 @@
+// Kernel parameter blocks and launch plans of the walk kernels.
+#pragma once
+
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace dspark {
+
+struct WalkParams {
+  const uint16_t* base;      // [bs, K, V] bf16
+  const uint16_t* w1;        // [V, 256] bf16
+  const uint16_t* w2;        // [V, 256] bf16 (bf16 path)
+  const int8_t* w2q;         // [V, 256] int8 (int8 path)
+  const float* scales;       // [V]
+  const int32_t* prev;       // [bs]
+  const uint64_t* seeds;     // [bs]
+  int32_t* tokens;           // [bs, K]
+  uint16_t* logits;          // [bs, K, V] bf16 or null
+  const int32_t* cand;       // top-k candidates [bs, K, top_k] (top-k walk)
+  int64_t V;
+  int32_t bs, K, top_k;
+  float temperature;
+  int32_t temp_is_one;
+  int32_t resident_rows;     // W2 rows per CTA kept in shared memory (multiple of 32)
+  StepSync sync;
+};
+
+// Threads per CTA of the persistent walk kernels: 16 warps.
+constexpr int kWalkThreads = 512;
+constexpr int kWalkWarps = kWalkThreads / 32;
+
+// Shared memory outside the resident W2 rows, per CTA.
+__host__ __device__ inline size_t walk_cc_fixed_smem(int bs) {
+  return static_cast<size_t>(bs) * kRank * 2  // W1[prev] rows, bf16
+         + 64 * 4                              // e-shift per row (int8 path)
+         + 64 * 4                              // prev tokens
+         + kWalkWarps * 8 + 64                 // reduction scratch, flags
+         + 256;                                // alignment slack
+}
+
+}  // namespace dspark

@@ -1,0 +1,185 @@
+/*
+ * dspark.h -- C ABI of the GB300 DSpark Markov draft walk (libdspark.so).
+ *
+ * The method (vLLM PR #62958, "Overview"; vLLM PR #49969, "Purpose"): a draft block
+ * of K tokens is produced left to right. At draft position i of request row b the
+ * walk forms
+ *
+ *     logits[b, i, :] = base_logits[b, i, :] + W2 . W1[prev_b]
+ *
+ * where W1 and W2 are V x rank (rank 256) and prev_b is the token chosen at the
+ * previous position (at i = 0, the last accepted token), and then picks the next
+ * token by argmax (greedy) or by Gumbel-max sampling at a temperature.
+ *
+ * Conventions shared by every call:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller; tensors are
+ *     contiguous and row-major. bf16 tensors are passed as their 16-bit patterns.
+ *   - Every call is asynchronous on the stream it is given and allocates nothing.
+ *   - The return value is a dspark_status code for problems found on the host
+ *     (arguments, capacity, launch). Problems found on the device while the kernel
+ *     runs (an out-of-range token, a wait that timed out, a non-finite W2 entry) are
+ *     written to the optional device word `status_dev` (set only when non-zero;
+ *     the caller zeroes it and reads it after synchronising).
+ *   - Token ids are int32 (V < 2^31). Seeds are uint64, one per request row.
+ *   - Ties and NaN follow torch.argmax: the first NaN wins, otherwise the first
+ *     maximum (vLLM PR #64476, "New tests"); -0 and +0 are equal.
+ */
+#ifndef DSPARK_H_
+#define DSPARK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* dspark_stream_t;
+
+typedef enum dspark_status {
+  DSPARK_OK = 0,
+  DSPARK_ERR_INVALID_ARG = 1,     /* null required pointer, size out of range, bad mode/T */
+  DSPARK_ERR_UNSUPPORTED = 2,     /* a valid combination this library does not run */
+  DSPARK_ERR_CUDA = 3,            /* a CUDA runtime call failed; see dspark_last_cuda_error */
+  DSPARK_ERR_COOP_TOO_LARGE = 4,  /* the cooperative grid cannot be co-resident */
+  DSPARK_ERR_TIMEOUT = 5,         /* device: a bounded wait gave up (workspace is now dirty) */
+  DSPARK_ERR_BAD_TOKEN = 6,       /* device: a prev token outside [0, V); its row reads -1 */
+  DSPARK_ERR_NONFINITE_W2 = 7,    /* device: quantize found a non-finite W2 entry */
+  DSPARK_ERR_WORKSPACE = 8        /* workspace missing or smaller than dspark_walk_workspace_size */
+} dspark_status;
+
+typedef enum dspark_mode { DSPARK_GREEDY = 0, DSPARK_PROBABILISTIC = 1 } dspark_mode;
+
+/* Limits of this implementation. */
+#define DSPARK_RANK 256
+#define DSPARK_MAX_BS 64
+#define DSPARK_MAX_K 32
+#define DSPARK_MAX_V 2147483647LL
+
+/* Test and tuning knobs in dspark_walk_args.flags (0 = production behaviour). */
+#define DSPARK_FLAG_SKIP_ARRIVAL_CTA0 0x1u /* CTA 0 skips its step-0 arrival: the barrier
+                                              times out and the call reports TIMEOUT */
+#define DSPARK_FLAG_FORCE_CUDA_CORES 0x2u  /* never use the tensor-core contraction */
+#define DSPARK_FLAG_FORCE_TENSOR_CORES 0x4u /* use the tensor-core contraction for any bs */
+
+/*
+ * Arguments of one walk. Layouts:
+ *   base_logits  bf16  [bs, K, V]     per-position base logits
+ *   w1           bf16  [V, rank]      Markov embedding table
+ *   w2           bf16  [V, rank]      Markov projection (NULL when w2q is given)
+ *   w2q          int8  [V, rank]      quantized projection (from dspark_quantize_w2)
+ *   w2_scales    fp32  [V]            per-row scales of w2q
+ *   prev_tokens  int32 [bs]           last accepted token of each row
+ *   seeds        uint64 [bs]          per-request seeds (probabilistic mode only)
+ *   draft_tokens int32 [bs, K]        out: chosen tokens
+ *   draft_logits bf16  [bs, K, V]     optional out: bf16(logits) that each step chose
+ *                                     from (top-k: -inf off the candidates)
+ *   workspace    bytes                scratch, >= dspark_walk_workspace_size(...),
+ *                                     zeroed by the caller once after allocation; the
+ *                                     kernels leave it zeroed again on success. After a
+ *                                     TIMEOUT the caller must zero it again.
+ */
+typedef struct dspark_walk_args {
+  const uint16_t* base_logits;
+  const uint16_t* w1;
+  const uint16_t* w2;
+  const int8_t* w2q;
+  const float* w2_scales;
+  const int32_t* prev_tokens;
+  const uint64_t* seeds;
+  int64_t V;
+  int32_t rank;        /* must be DSPARK_RANK */
+  int32_t bs;          /* 1 .. DSPARK_MAX_BS */
+  int32_t K;           /* 1 .. DSPARK_MAX_K */
+  int32_t mode;        /* dspark_mode */
+  float temperature;   /* > 0 and finite in probabilistic mode; 1.0 skips the divide */
+  int32_t top_k;       /* 0: full vocabulary; 1..V: top-k walk (bf16 w2 only) */
+  int32_t* draft_tokens;
+  uint16_t* draft_logits;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* status_dev; /* optional device int32 */
+  uint32_t flags;      /* DSPARK_FLAG_* */
+  int32_t resident_rows_cap; /* tuning: cap on smem-resident W2 rows per CTA; -1 = automatic */
+  uint32_t timeout_us; /* limit of every device-side wait; 0 = 1,000,000 us */
+} dspark_walk_args;
+
+/*
+ * Per-row symmetric int8 quantization of W2 (vLLM PR #62958, "Overview": int8 W2 with
+ * one fp32 scale per row). For each row v:
+ *     scale[v] = max_k |w2[v,k]| / 127          (fp32 division)
+ *     w2q[v,k] = clamp(rint(w2[v,k] / scale[v]), -127, 127)   (fp32 division, ties to even)
+ * An all-zero row gets scale 0 and codes 0. A non-finite entry sets
+ * DSPARK_ERR_NONFINITE_W2 in *status_dev (outputs of that row unspecified).
+ *   w2         bf16 [V, rank] in;  w2q int8 [V, rank] out;  scales fp32 [V] out.
+ * Returns DSPARK_ERR_INVALID_ARG for null pointers, V <= 0 or rank != DSPARK_RANK.
+ */
+int32_t dspark_quantize_w2(const uint16_t* w2, int64_t V, int32_t rank, int8_t* w2q,
+                           float* scales, int32_t* status_dev, dspark_stream_t stream);
+
+/*
+ * The full-vocabulary walk (top_k == 0) as one persistent cooperative kernel; with
+ * top_k > 0 it forwards to dspark_walk_topk. Greedy mode takes the argmax of the fp32
+ * logits. Probabilistic mode takes the argmax of bf16(logit) / T + g, where
+ * g = -log(-log(u)) and u comes from Philox4x32-10 with key (seed lo, seed hi) and
+ * counter (v >> 2, i, b, 0), word v & 3, u = (2 * (word >> 9) + 1) * 2^-24
+ * (vLLM PR #62958, "Details": Philox keyed by the request seed and draft position;
+ * the sampled bf16 logits are what draft_logits holds).
+ * Exactly one of w2 / (w2q, w2_scales) must be given.
+ */
+int32_t dspark_walk(const dspark_walk_args* args, dspark_stream_t stream);
+
+/*
+ * The top-k walk (vLLM PR #49969, "Purpose"): for every (b, i) the top_k largest base
+ * logits are chosen once (NaN counts as largest; ties at the boundary go to the
+ * smaller index), the bias is computed for those candidates only (bf16 W2 rows
+ * gathered), and the step's argmax or sample runs over the dense row that is -inf
+ * off the candidates. Gumbel noise is keyed by the vocabulary id, so top_k == V
+ * reproduces dspark_walk. Requires bf16 w2; int8 returns DSPARK_ERR_UNSUPPORTED.
+ */
+int32_t dspark_walk_topk(const dspark_walk_args* args, dspark_stream_t stream);
+
+/*
+ * End-to-end variant for callers whose per-call inputs live in host memory: copies
+ * base_host [bs,K,V] bf16, prev_host [bs] and seeds_host [bs] (may be NULL in greedy
+ * mode) into the device buffers named by `args`, runs the walk, and copies
+ * draft_tokens (and draft_logits when both it and logits_host are given) back into
+ * tokens_host / logits_host. All copies and the kernels are queued on `stream`; host
+ * buffers should be pinned for the copies to be asynchronous. The caller synchronises.
+ */
+int32_t dspark_walk_from_host(const dspark_walk_args* args, const uint16_t* base_host,
+                              const int32_t* prev_host, const uint64_t* seeds_host,
+                              int32_t* tokens_host, uint16_t* logits_host,
+                              dspark_stream_t stream);
+
+/* Bytes of scratch workspace a walk of this shape needs (argmax slots, barrier
+ * counters, status words, top-k candidate lists). */
+size_t dspark_walk_workspace_size(int64_t V, int32_t bs, int32_t K, int32_t top_k);
+
+/*
+ * Launch plan the walk would use on `device`: cooperative grid size (CTAs) and the
+ * number of W2 rows kept resident in shared memory over the whole grid. Queries the
+ * device once and caches it (the only host-synchronous work of the library).
+ */
+int32_t dspark_query_capacity(int32_t device, int64_t V, int32_t w2_is_int8, int32_t bs,
+                              int32_t* grid_ctas, int64_t* resident_rows);
+
+/*
+ * The Philox words and Gumbel values the walk draws, for checking: words uint32 and
+ * gumbel fp32 [bs, K, V] (either may be NULL). Same generator code as the walk.
+ */
+int32_t dspark_gumbel_noise(const uint64_t* seeds, int32_t bs, int32_t K, int64_t V,
+                            uint32_t* words, float* gumbel, dspark_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* dspark_status_string(int32_t status);
+
+/* The last CUDA error string seen by this thread's calls into the library. */
+const char* dspark_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H_ */

@@ -1,0 +1,82 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds for sm_103a,
+loads, exports every entry point the public header declares, and rejects bad
+arguments before touching the device."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from dspark_markov_draft_gb300 import build, capi
+    build.build()
+    return capi.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "dspark.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dspark_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("dspark_quantize_w2", "dspark_walk", "dspark_walk_topk",
+                     "dspark_walk_workspace_size", "dspark_query_capacity",
+                     "dspark_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    from dspark_markov_draft_gb300 import capi
+    for code in capi.STATUS:
+        s = L.dspark_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert L.dspark_status_string(999).decode() == "unknown status"
+
+
+def test_workspace_size_grows_with_shape(L):
+    from dspark_markov_draft_gb300 import capi
+    a = capi.workspace_size(151936, 1, 7)
+    b = capi.workspace_size(151936, 64, 7)
+    c = capi.workspace_size(151936, 64, 7, 4096)
+    assert 0 < a < b < c
+    assert c - b >= 64 * 7 * 4096 * 4
+    assert capi.workspace_size(10, 0, 1) == 0
+
+
+def test_invalid_arguments_rejected_on_host(L):
+    from dspark_markov_draft_gb300 import capi
+    assert L.dspark_walk(None, None) == 1
+    a = capi.WalkArgs()
+    assert L.dspark_walk(C.byref(a), None) == 1          # null pointers
+    # plausible non-null (never dereferenced) pointers with a bad rank / size / mode
+    fake = 1 << 20
+    def args(**kw):
+        d = dict(base_logits=fake, w1=fake, w2=fake, prev_tokens=fake, draft_tokens=fake,
+                 workspace=fake, workspace_bytes=1 << 20, V=1000, rank=256, bs=1, K=2,
+                 mode=0, temperature=1.0, top_k=0, resident_rows_cap=-1)
+        d.update(kw)
+        x = capi.WalkArgs()
+        for k, v in d.items():
+            setattr(x, k, v)
+        return x
+    for bad in (dict(rank=128), dict(bs=0), dict(bs=65), dict(K=0), dict(K=33), dict(V=0),
+                dict(mode=2), dict(mode=1, seeds=fake, temperature=0.0),
+                dict(mode=1, seeds=None), dict(w2q=fake), dict(top_k=1001)):
+        assert L.dspark_walk(C.byref(args(**bad)), None) == 1, bad
+    assert L.dspark_walk(C.byref(args(workspace_bytes=16)), None) == 8
+    assert L.dspark_walk(C.byref(args(workspace=None)), None) == 8
+    assert L.dspark_walk_topk(C.byref(args(w2=None, w2q=fake, w2_scales=fake, top_k=5)), None) == 2
+    assert L.dspark_quantize_w2(None, 10, 256, None, None, None, None) == 1
+    assert L.dspark_quantize_w2(fake, 10, 255, fake, fake, None, None) == 1
+    assert L.dspark_gumbel_noise(None, 1, 1, 10, None, None, None) == 1
