@@ -47,6 +47,18 @@ VARIANTS = [
 ]
 
 
+# Further workloads that can be selected with --workload (parity cases, not bench lines).
+EXTRA = [
+    dict(name="v129280_k5_bs1_bf16_greedy", V=129280, K=5, bs=1, int8=False, mode=0, T=1.0, top_k=0, peak=None, logits=False),
+    dict(name="v151936_k16_bs1_bf16_prob_logits", V=151936, K=16, bs=1, int8=False, mode=1, T=0.7, top_k=0, peak=8.0, logits=True),
+    dict(name="v151936_k16_bs64_bf16_prob_logits", V=151936, K=16, bs=64, int8=False, mode=1, T=0.7, top_k=0, peak=8.0, logits=True),
+    dict(name="v248320_k16_bs1_int8_greedy", V=248320, K=16, bs=1, int8=True, mode=0, T=1.0, top_k=0, peak=None, logits=False),
+    dict(name="v248320_k16_bs64_int8_greedy", V=248320, K=16, bs=64, int8=True, mode=0, T=1.0, top_k=0, peak=None, logits=False),
+    dict(name="v151936_k7_bs64_topk512_prob", V=151936, K=7, bs=64, int8=False, mode=1, T=1.0, top_k=512, peak=None, logits=False),
+    dict(name="v151936_k7_bs64_topk4096_prob", V=151936, K=7, bs=64, int8=False, mode=1, T=1.0, top_k=4096, peak=None, logits=False),
+]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -260,6 +272,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default=MAIN["name"],
+                    help="run this workload as the main line (one of the built-in names)")
     a = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -280,7 +295,8 @@ def main():
 
     peaks = load_peaks()
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 129 MB L2
-    cfg = MAIN
+    by_name = {c["name"]: c for c in [MAIN] + VARIANTS + EXTRA}
+    cfg = by_name[a.workload]
     # untimed warm-up of the whole path, then the timed walks
     if dist:
         dist.barrier()
@@ -300,7 +316,7 @@ def main():
     toks = cfg["bs"] * cfg["K"]
     value = world * toks / (ms * 1e-3)
 
-    e2e_ms, h2d, d2h = time_e2e(cfg, t, args, max(3, a.steps // 2), dev)
+    e2e_ms, h2d, d2h = (float("nan"), 0, 0) if a.no_e2e else time_e2e(cfg, t, args, max(3, a.steps // 2), dev)
     hb = hbm_bytes(cfg)
     achieved = hb / (ms * 1e-3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -331,7 +347,9 @@ def main():
             "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int8 x int (dp4a) -> fp32", "data": "synthetic",
             "config": {"workload": cfg["name"], "V": cfg["V"], "rank": R, "K": cfg["K"],
-                       "bs": cfg["bs"], "w2": "int8", "mode": "greedy",
+                       "bs": cfg["bs"], "w2": "int8" if cfg["int8"] else "bf16",
+                       "mode": "greedy" if cfg["mode"] == 0 else f"probabilistic T={cfg['T']}",
+                       "top_k": cfg["top_k"], "draft_logits": cfg["logits"],
                        "l2": "flushed before every walk (256 MB write)",
                        "parallelism": f"replicas x{world}"},
             "us_per_walk": 1000 * ms,

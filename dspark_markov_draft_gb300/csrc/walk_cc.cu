@@ -72,6 +72,13 @@ __device__ __forceinline__ uint4 ld_row_chunk(const unsigned char* row_global, i
   return __ldg(reinterpret_cast<const uint4*>(row_global) + chunk);
 }
 
+// x * 2^s for |s| <= 252 as two exact multiplies by normal powers of two.
+__device__ __forceinline__ float pow2_lo(int s) { return __int_as_float((s / 2 + 127) << 23); }
+__device__ __forceinline__ float pow2_hi(int s) { return __int_as_float((s - s / 2 + 127) << 23); }
+__device__ __forceinline__ float mul_pow2(float x, int s) {
+  return __fmul_rn(__fmul_rn(x, pow2_lo(s)), pow2_hi(s));
+}
+
 // Limbs of the 16 integers of one chunk: hi (signed byte), mid and lo (unsigned).
 struct Limbs {
   int hi[4];
@@ -85,7 +92,7 @@ __device__ __forceinline__ void make_limbs(const uint16_t* e16, int shift, Limbs
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const float x = bf16_to_f32(e16[4 * w + t]);
-      const int xi = __float2int_rn(ldexpf(x, shift));
+      const int xi = __float2int_rn(mul_pow2(x, shift));
       h |= (static_cast<uint32_t>(xi >> 16) & 0xFFu) << (8 * t);
       m |= (static_cast<uint32_t>(xi >> 8) & 0xFFu) << (8 * t);
       l |= (static_cast<uint32_t>(xi) & 0xFFu) << (8 * t);
@@ -133,9 +140,9 @@ __device__ __forceinline__ float dot_bf16_chunk(const uint4& q, const float* e, 
 // Score of one vocabulary entry and its argmax word.
 template <bool PROB, bool LOGITS>
 __device__ __forceinline__ uint64_t score_entry(const WalkParams& p, int b, int i, int64_t v,
-                                                float bias, uint64_t seed) {
+                                                float base_v, float bias, uint64_t seed) {
   const size_t o = (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v;
-  const float l = __fadd_rn(bf16_to_f32(p.base[o]), bias);
+  const float l = __fadd_rn(base_v, bias);
   if (LOGITS) p.logits[o] = f32_to_bf16_bits(l);
   float s = l;
   if (PROB) {
@@ -240,12 +247,22 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkPara
         }
       }
 
+      const float inv_lo = pow2_lo(-shift), inv_hi = pow2_hi(-shift);
       uint64_t best = 0ull;
       // Warp-blocks of 32 rows: warp w takes blocks w, w + 16, ...
       for (int r0 = 32 * warp; r0 < n; r0 += 32 * kWalkWarps) {
         const bool from_smem = (i > 0 || !fill) && (r0 + 32 <= res);
         const bool store_smem = fill && (r0 + 32 <= res);
         const int rbase = r0 + 8 * grp;
+        // The lane's own epilogue row: fetch its base logit and scale before the
+        // contraction so the loads overlap it.
+        const int r_out = rbase + j8;
+        float base_v = 0.f, scale_v = 0.f;
+        if (r_out < n) {
+          const int64_t v = v0 + r_out;
+          base_v = bf16_to_f32(__ldg(p.base + (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v));
+          if (INT8) scale_v = __ldg(p.scales + v);
+        }
         float fpart[8];
         int hpart[8], mpart[8];
 #pragma unroll
@@ -292,17 +309,16 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkPara
         } else {
           bias_raw = butterfly8(fpart, lane);
         }
-        const int r = rbase + j8;
-        if (r < n) {
-          const int64_t v = v0 + r;
+        if (r_out < n) {
+          const int64_t v = v0 + r_out;
           // int8: scale_v * 2^-shift * sum; the power of two is applied last so that a
           // tiny embedding row underflows gracefully instead of through 2^-shift.
           float bias = bias_raw;
           if (INT8) {
-            bias = __fmul_rn(bias_raw, p.scales[v]);
-            if (!float_path) bias = ldexpf(bias, -shift);
+            bias = __fmul_rn(bias_raw, scale_v);
+            if (!float_path) bias = __fmul_rn(__fmul_rn(bias, inv_lo), inv_hi);
           }
-          best = umax64(best, score_entry<PROB, LOGITS>(p, b, i, v, bias, seed));
+          best = umax64(best, score_entry<PROB, LOGITS>(p, b, i, v, base_v, bias, seed));
         }
       }
       // CTA argmax for row b, then one atomic into this position's slot.
