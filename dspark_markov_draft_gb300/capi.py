@@ -63,6 +63,7 @@ def lib():
         L.dspark_quantize_w2.argtypes = [vp, i64, i32, vp, vp, vp, vp]
         L.dspark_walk.argtypes = [C.POINTER(WalkArgs), vp]
         L.dspark_walk_topk.argtypes = [C.POINTER(WalkArgs), vp]
+        L.dspark_walk_noalloc.argtypes = [C.POINTER(WalkArgs), vp]
         L.dspark_walk_from_host.argtypes = [C.POINTER(WalkArgs), vp, vp, vp, vp, vp, vp]
         L.dspark_walk_workspace_size.argtypes = [i64, i32, i32, i32]
         L.dspark_walk_workspace_size.restype = C.c_size_t
@@ -73,7 +74,7 @@ def lib():
         L.dspark_status_string.restype = C.c_char_p
         L.dspark_last_cuda_error.argtypes = []
         L.dspark_last_cuda_error.restype = C.c_char_p
-        for f in ("dspark_quantize_w2", "dspark_walk", "dspark_walk_topk",
+        for f in ("dspark_quantize_w2", "dspark_walk", "dspark_walk_topk", "dspark_walk_noalloc",
                   "dspark_walk_from_host", "dspark_query_capacity", "dspark_gumbel_noise"):
             getattr(L, f).restype = C.c_int32
         _lib = L
@@ -176,6 +177,11 @@ def walk_args_call(args: WalkArgs, stream=None, topk: bool = False) -> int:
     """Call dspark_walk / dspark_walk_topk on prepared arguments; returns the status."""
     f = lib().dspark_walk_topk if topk else lib().dspark_walk
     return int(f(C.byref(args), _stream(stream)))
+
+
+def walk_noalloc(args: WalkArgs, stream=None) -> int:
+    """Call dspark_walk_noalloc (scratch from the library's static array); returns the status."""
+    return int(lib().dspark_walk_noalloc(C.byref(args), _stream(stream)))
 
 
 def walk_from_host(args: WalkArgs, base_host, prev_host, seeds_host, tokens_host,

@@ -172,6 +172,26 @@ int32_t dspark_query_capacity(int32_t device, int64_t V, int32_t w2_is_int8, int
 int32_t dspark_gumbel_noise(const uint64_t* seeds, int32_t bs, int32_t K, int64_t V,
                             uint32_t* words, float* gumbel, dspark_stream_t stream);
 
+/*
+ * dspark_walk without a caller-provided workspace, for callers that cannot allocate
+ * device memory (e.g. a plugin whose enqueue hook may not call cudaMalloc, or a server
+ * whose device memory is all pre-reserved by a caching allocator; cudaMalloc on the
+ * decode path would fail or synchronise). The pages have no counterpart of this call.
+ *   - Takes the same arguments as dspark_walk; `workspace` and `workspace_bytes` are
+ *     ignored. Full-vocabulary walk only: top_k > 0 returns DSPARK_ERR_UNSUPPORTED.
+ *   - Scratch comes from one static device array of 24,576 bytes inside the library,
+ *     held by every GPU that loads the library until the process exits. A shape whose
+ *     scratch would not fit returns DSPARK_ERR_WORKSPACE (every shape dspark_walk
+ *     accepts fits).
+ *   - The first call on a device looks up the array's device address with that device
+ *     current; make that first call before any stream capture.
+ *   - Each call clears the part of the array it uses with cudaMemsetAsync on `stream`,
+ *     then launches the walk; it calls no allocating routine. All calls share the
+ *     array, so calls whose kernels overlap on the GPU (different streams, no ordering)
+ *     race and give wrong results: serialise them.
+ */
+int32_t dspark_walk_noalloc(const dspark_walk_args* args, dspark_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* dspark_status_string(int32_t status);
 
