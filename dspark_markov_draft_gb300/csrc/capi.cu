@@ -67,6 +67,7 @@ int32_t current_caps(DeviceCaps* caps) {
 struct Plan {
   int grid;
   int resident_rows;  // per CTA
+  int slice_cap;      // rows of the largest vocabulary slice, rounded up to 32
   size_t smem;
 };
 
@@ -75,8 +76,9 @@ Plan plan_dense(const DeviceCaps& caps, int64_t V, bool int8, int bs, int cap_ro
   Plan pl{};
   pl.grid = caps.sms;
   const int row_bytes = int8 ? kRank : 2 * kRank;
-  const size_t fixed = walk_cc_fixed_smem(bs);
   const int64_t per_cta = (V + pl.grid - 1) / pl.grid;
+  pl.slice_cap = static_cast<int>((per_cta + 31) & ~31LL);
+  const size_t fixed = walk_cc_fixed_smem(bs, int8, pl.slice_cap);
   int64_t rows = caps.smem_optin > static_cast<int>(fixed)
                      ? (static_cast<int64_t>(caps.smem_optin) - static_cast<int64_t>(fixed)) / row_bytes
                      : 0;
@@ -128,7 +130,7 @@ StepSync make_sync(const dspark_walk_args* a, int grid) {
   return s;
 }
 
-WalkParams make_params(const dspark_walk_args* a, int grid, int resident_rows) {
+WalkParams make_params(const dspark_walk_args* a, int grid, int resident_rows, int slice_cap) {
   WalkParams p{};
   p.base = a->base_logits;
   p.w1 = a->w1;
@@ -147,6 +149,7 @@ WalkParams make_params(const dspark_walk_args* a, int grid, int resident_rows) {
   p.temperature = a->temperature;
   p.temp_is_one = a->temperature == 1.0f ? 1 : 0;
   p.resident_rows = resident_rows;
+  p.slice_cap = slice_cap;
   p.sync = make_sync(a, grid);
   return p;
 }
@@ -238,11 +241,11 @@ int32_t dspark_walk_topk(const dspark_walk_args* a, dspark_stream_t stream) {
   if (!caps.coop) return DSPARK_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int rows = a->bs * a->K;
-  WalkParams p = make_params(a, caps.sms, 0);
+  WalkParams p = make_params(a, caps.sms, 0, 0);
   cudaError_t e = launch_topk_select(a->base_logits, a->V, a->top_k, rows,
                                      const_cast<int32_t*>(p.cand), a->draft_logits, s);
   if (e != cudaSuccess) return cuda_fail(e, "topk_select_kernel launch");
-  const size_t smem = static_cast<size_t>(a->bs) * kRank * 4 + 64 * 4 + kWalkWarps * 8 + 64 + 256;
+  const size_t smem = static_cast<size_t>(a->bs) * kRank * 4 + 64 * 4 + 64 * 8 + kWalkWarps * 8 + 64 + 256;
   const bool prob = a->mode == DSPARK_PROBABILISTIC, lg = a->draft_logits != nullptr;
   const void* fn = topk_walk_kernel_ptr(prob, lg);
   return launch_coop(fn, caps.sms, smem, p, s);
@@ -257,7 +260,7 @@ int32_t dspark_walk(const dspark_walk_args* a, dspark_stream_t stream) {
   if (!caps.coop) return DSPARK_ERR_UNSUPPORTED;
   const bool int8 = a->w2q != nullptr;
   const Plan pl = plan_dense(caps, a->V, int8, a->bs, a->resident_rows_cap);
-  WalkParams p = make_params(a, pl.grid, pl.resident_rows);
+  WalkParams p = make_params(a, pl.grid, pl.resident_rows, pl.slice_cap);
   const bool lg = a->draft_logits != nullptr;
   const void* fn = walk_cc_kernel_ptr(int8, a->mode == DSPARK_PROBABILISTIC, lg);
   return launch_coop(fn, pl.grid, pl.smem, p, reinterpret_cast<cudaStream_t>(stream));

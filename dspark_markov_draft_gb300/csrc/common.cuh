@@ -1,6 +1,6 @@
 // Device helpers shared by the walk kernels: bf16 handling, Philox4x32-10 Gumbel
-// noise, the orderable argmax word, the device status word and the bounded
-// grid-wide step barrier.
+// noise, the orderable argmax word, the device status word, the workspace layout and
+// the bounded grid-wide step exchange.
 #pragma once
 
 #include <cstdint>
@@ -131,14 +131,18 @@ __host__ __device__ inline size_t ws_slots_off(int K) {
   return kWsHeader + kWsCounterStride * static_cast<size_t>(K);
 }
 __host__ __device__ inline size_t ws_cand_off(int K, int bs) {
-  size_t end = ws_slots_off(K) + 8ull * K * bs;
+  const size_t end = ws_slots_off(K) + 8ull * K * bs;
   return (end + 255) & ~static_cast<size_t>(255);
 }
 __host__ __device__ inline size_t ws_total(int K, int bs, int top_k) {
   return ws_cand_off(K, bs) + 4ull * bs * K * static_cast<size_t>(top_k);
 }
 
-// ---------------------------------------------------------------- step barrier
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// ---------------------------------------------------------------- step exchange
 
 struct StepSync {
   WsHeader* hdr;
@@ -154,49 +158,60 @@ struct StepSync {
   }
 };
 
-// Arrive at step i's barrier and wait for the whole grid. Every thread of the CTA
-// calls it; the argmax atomics of the CTA must have been issued before. Returns
-// false when the wait gave up (timeout or another CTA's abort); the caller then
-// returns from the kernel. The wait is bounded by timeout_ns of wall-clock time.
-__device__ __forceinline__ bool grid_step_barrier(const StepSync& s, int i, bool skip_arrival,
-                                                  int* sh_flag) {
+// Give up a wait: flag the abort for the other CTAs and report a timeout.
+__device__ __forceinline__ void give_up(const StepSync& s) {
+  atomicExch(&s.hdr->abort, 1u);
+  report(s.status_dev, DSPARK_ERR_TIMEOUT);
+}
+
+// Exchange of the per-row argmax words of step i. best_s[b] (shared memory, b < bs)
+// holds this CTA's word on entry and the grid-wide maximum on return.
+// Each row's word goes into slot[i][b] with one 64-bit atomicMax; thread 0 then
+// arrives at the step counter with a release add (ordering the CTA's atomics before
+// it), spins with acquire loads until the whole grid has arrived, and the winners are
+// read back. Every thread of the CTA calls it. The spin is bounded by timeout_ns of
+// wall-clock time and watches the workspace abort flag; on either, the wait gives up
+// and false is returned (the same value in every thread), and the caller returns from
+// the kernel.
+__device__ __forceinline__ bool exchange_best(const StepSync& s, int i, int bs,
+                                              bool skip_arrival, uint64_t* best_s,
+                                              int* sh_flag) {
+  __syncthreads();
+  if (threadIdx.x < bs && best_s[threadIdx.x] != 0ull)
+    atomicMax(reinterpret_cast<unsigned long long*>(s.slots + static_cast<size_t>(i) * bs + threadIdx.x),
+              static_cast<unsigned long long>(best_s[threadIdx.x]));
   __syncthreads();
   if (threadIdx.x == 0) {
-    int ok = 1;
+    bool failed = false;
     uint32_t* ctr = s.counter(i);
     __threadfence();
-    if (!skip_arrival) atomicAdd(ctr, 1u);
+    if (!skip_arrival) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
     uint64_t t0 = 0;
     uint32_t it = 0;
     while (ld_acquire_u32(ctr) < s.grid) {
-      if ((++it & 63u) == 0u) {
-        if (t0 == 0) t0 = globaltimer_ns();
-        if (*reinterpret_cast<volatile uint32_t*>(&s.hdr->abort) != 0u) { ok = 0; break; }
-        if (globaltimer_ns() - t0 > s.timeout_ns) {
-          atomicExch(&s.hdr->abort, 1u);
-          report(s.status_dev, DSPARK_ERR_TIMEOUT);
-          ok = 0;
-          break;
-        }
-      }
+      if ((++it & 63u) != 0u) continue;
+      if (t0 == 0) t0 = globaltimer_ns();
+      if (*reinterpret_cast<volatile uint32_t*>(&s.hdr->abort) != 0u) { failed = true; break; }
+      if (globaltimer_ns() - t0 > s.timeout_ns) { give_up(s); failed = true; break; }
     }
-    __threadfence();
-    *sh_flag = ok;
+    *sh_flag = failed ? 0 : 1;
   }
   __syncthreads();
-  return *sh_flag != 0;
+  if (*sh_flag == 0) return false;
+  if (threadIdx.x < bs) best_s[threadIdx.x] = ld_relaxed_u64(s.slots + static_cast<size_t>(i) * bs + threadIdx.x);
+  __syncthreads();
+  return true;
 }
 
-// Reset-behind: once every CTA has passed step i+1's barrier nobody reads step i's
-// counter or slots again, so CTA 0 zeroes them for the next call. The last CTA to
-// finish zeroes the final step's state and the exit counter.
+// Reset-behind: once every CTA has passed step i's barrier nobody reads step i-1's
+// counter or slots again, so CTA 0 zeroes them for the next call.
 __device__ __forceinline__ void reset_behind(const StepSync& s, int i, int bs) {
-  if (blockIdx.x == 0 && i >= 1) {
-    for (int t = threadIdx.x; t < bs; t += blockDim.x) s.slots[static_cast<size_t>(i - 1) * bs + t] = 0ull;
-    if (threadIdx.x == 0) *s.counter(i - 1) = 0u;
-  }
+  if (blockIdx.x != 0 || i < 1) return;
+  for (int t = threadIdx.x; t < bs; t += blockDim.x) s.slots[static_cast<size_t>(i - 1) * bs + t] = 0ull;
+  if (threadIdx.x == 0) *s.counter(i - 1) = 0u;
 }
 
+// The last CTA to finish zeroes the final step's counter and slots and the exit counter.
 __device__ __forceinline__ void finish_walk(const StepSync& s, int K, int bs, int* sh_flag) {
   __syncthreads();
   if (threadIdx.x == 0) {

@@ -148,7 +148,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
   const int j8 = lane & 7, grp = lane >> 3;
   float* e_s = reinterpret_cast<float*>(smem);                 // [bs][256] fp32
   int* prev_s = reinterpret_cast<int*>(e_s + static_cast<size_t>(p.bs) * kRank);
-  uint64_t* red = reinterpret_cast<uint64_t*>(prev_s + 64);
+  uint64_t* best_s = reinterpret_cast<uint64_t*>(prev_s + 64);
+  uint64_t* red = best_s + 64;
   int* flag = reinterpret_cast<int*>(red + kWalkWarps);
 
   const int64_t items = static_cast<int64_t>(p.bs) * p.top_k;
@@ -167,6 +168,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
 
   for (int i = 0; i < p.K; ++i) {
     __syncthreads();
+    for (int t = threadIdx.x; t < p.bs; t += blockDim.x) best_s[t] = 0ull;
     for (int b = warp; b < p.bs; b += kWalkWarps) {
       const int tok = prev_s[b];
       if (tok < 0) continue;
@@ -257,18 +259,18 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
       if (warp == 0) {
         uint64_t xw = lane < kWalkWarps ? red[lane] : 0ull;
         xw = warp_max64(xw);
-        if (lane == 0 && xw != 0ull)
-          atomicMax(reinterpret_cast<unsigned long long*>(p.sync.slots + static_cast<size_t>(i) * p.bs + b),
-                    static_cast<unsigned long long>(xw));
+        if (lane == 0) best_s[b] = umax64(best_s[b], xw);
+        if (xw != 0ull && lane < 4 && i + 1 < p.K)
+          prefetch_l2(p.w1 + static_cast<size_t>(unpack_idx(xw)) * kRank + 64 * lane);
       }
       __syncthreads();
     }
 
-    if (!grid_step_barrier(p.sync, i, skip0 && i == 0, flag)) return;
+    if (!exchange_best(p.sync, i, p.bs, skip0 && i == 0, best_s, flag)) return;
     for (int t = threadIdx.x; t < p.bs; t += blockDim.x) {
       int tok = -1;
       if (prev_s[t] >= 0) {
-        const uint64_t w = ld_relaxed_u64(p.sync.slots + static_cast<size_t>(i) * p.bs + t);
+        const uint64_t w = best_s[t];
         // Every candidate at -inf: the dense row is -inf everywhere and its argmax is 0.
         tok = (static_cast<uint32_t>(w >> 32) == order_key(__int_as_float(0xFF800000))) ? 0 : unpack_idx(w);
       }

@@ -25,6 +25,7 @@
 // word per request row, issues one 64-bit atomicMax into slot[i][b], and the grid
 // meets at a bounded barrier; then every CTA reads the winning token.
 #include <cstdint>
+#include <type_traits>
 
 #include "common.cuh"
 #include "walk_params.cuh"
@@ -68,6 +69,25 @@ __device__ __forceinline__ T butterfly8(T (&v)[8], int lane) {
   return keep + __shfl_xor_sync(kFull, send, 1);
 }
 
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most `pending` of this thread's most recent commit groups are in flight.
+__device__ __forceinline__ void cp_async_wait(int pending) {
+  switch (pending) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+  }
+}
+
 __device__ __forceinline__ uint4 ld_row_chunk(const unsigned char* row_global, int chunk) {
   return __ldg(reinterpret_cast<const uint4*>(row_global) + chunk);
 }
@@ -85,22 +105,16 @@ struct Limbs {
   uint32_t mid[4], lo[4];
 };
 
-__device__ __forceinline__ void make_limbs(const uint16_t* e16, int shift, Limbs& L) {
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    uint32_t h = 0, m = 0, l = 0;
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const float x = bf16_to_f32(e16[4 * w + t]);
-      const int xi = __float2int_rn(mul_pow2(x, shift));
-      h |= (static_cast<uint32_t>(xi >> 16) & 0xFFu) << (8 * t);
-      m |= (static_cast<uint32_t>(xi >> 8) & 0xFFu) << (8 * t);
-      l |= (static_cast<uint32_t>(xi) & 0xFFu) << (8 * t);
-    }
-    L.hi[w] = static_cast<int>(h);
-    L.mid[w] = m;
-    L.lo[w] = l;
-  }
+// Limb words of one embedding row: [3][64] uint32, word w of limb j packs the byte j
+// of the 24-bit integers round(e_k 2^shift) for k = 4w .. 4w+3.
+__device__ __forceinline__ void load_limbs(const uint32_t* limb_row, int chunk, Limbs& L) {
+  const uint4 h = reinterpret_cast<const uint4*>(limb_row)[chunk];
+  const uint4 m = reinterpret_cast<const uint4*>(limb_row + 64)[chunk];
+  const uint4 l = reinterpret_cast<const uint4*>(limb_row + 128)[chunk];
+  L.hi[0] = static_cast<int>(h.x); L.hi[1] = static_cast<int>(h.y);
+  L.hi[2] = static_cast<int>(h.z); L.hi[3] = static_cast<int>(h.w);
+  L.mid[0] = m.x; L.mid[1] = m.y; L.mid[2] = m.z; L.mid[3] = m.w;
+  L.lo[0] = l.x; L.lo[1] = l.y; L.lo[2] = l.z; L.lo[3] = l.w;
 }
 
 __device__ __forceinline__ void dot_int8_chunk(const uint4& q, const Limbs& L, int& h, int& m,
@@ -154,6 +168,18 @@ __device__ __forceinline__ uint64_t score_entry(const WalkParams& p, int b, int 
   return pack_best(order_key(s), static_cast<uint32_t>(v));
 }
 
+// Prefetch this CTA's base-logit slices of position i (all rows) towards L2.
+__device__ __forceinline__ void prefetch_base_slice(const WalkParams& p, int64_t v0, int n, int i) {
+  if (i >= p.K) return;
+  const int lines = (n * 2 + 127) / 128 + 1;
+  for (int t = threadIdx.x; t < lines * p.bs; t += blockDim.x) {
+    const int b = t / lines, l = t % lines;
+    const uint16_t* row = p.base + (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v0;
+    const int64_t off = min(static_cast<int64_t>(l) * 64, static_cast<int64_t>(n - 1));
+    prefetch_l2(row + off);
+  }
+}
+
 }  // namespace
 
 template <bool INT8, bool PROB, bool LOGITS>
@@ -170,11 +196,16 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkPara
   const int n = static_cast<int>(v1 - v0);
   const int res = min(p.resident_rows, n & ~31);
 
+  // Shared memory: resident W2 rows | scales of the slice (int8) | embedding rows |
+  // shifts | previous tokens | per-row CTA argmax words | reduction scratch | flag.
   unsigned char* w2s = smem;
-  uint16_t* e_s = reinterpret_cast<uint16_t*>(smem + static_cast<size_t>(p.resident_rows) * kRowBytes);
-  int* sh_shift = reinterpret_cast<int*>(e_s + static_cast<size_t>(p.bs) * kRank);
+  float* scale_s = reinterpret_cast<float*>(smem + static_cast<size_t>(p.resident_rows) * kRowBytes);
+  uint16_t* e_s = reinterpret_cast<uint16_t*>(scale_s + (INT8 ? p.slice_cap : 0));
+  uint32_t* limb_s = reinterpret_cast<uint32_t*>(e_s + static_cast<size_t>(p.bs) * kRank);
+  int* sh_shift = reinterpret_cast<int*>(limb_s + (INT8 ? static_cast<size_t>(p.bs) * 3 * 64 : 0));
   int* prev_s = sh_shift + 64;
-  uint64_t* red = reinterpret_cast<uint64_t*>(prev_s + 64);
+  uint64_t* best_s = reinterpret_cast<uint64_t*>(prev_s + 64);
+  uint64_t* red = best_s + 64;
   int* flag = reinterpret_cast<int*>(red + kWalkWarps);
 
   const unsigned char* w2g = INT8 ? reinterpret_cast<const unsigned char*>(p.w2q)
@@ -189,6 +220,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkPara
     prev_s[t] = ok ? tok : -1;
     if (!ok && cta == 0) report(p.sync.status_dev, DSPARK_ERR_BAD_TOKEN);
   }
+  if (INT8)
+    for (int r = threadIdx.x; r < n; r += blockDim.x) scale_s[r] = __ldg(p.scales + v0 + r);
+  // Base logits of the first two positions towards L2; later positions are fetched
+  // two steps ahead, so the epilogue's loads hit L2 instead of cold HBM.
+  prefetch_base_slice(p, v0, n, 0);
+  prefetch_base_slice(p, v0, n, 1);
   bool filled = false;
 
   for (int i = 0; i < p.K; ++i) {
@@ -211,16 +248,33 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkPara
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-      if (lane == 0) {
-        int shift = 0;
-        if (!isfinite(amax)) {
-          shift = 1 << 30;  // marks a non-finite embedding row: fp32 fallback
-        } else if (amax > 0.f) {
-          int ex;
-          frexpf(amax, &ex);  // amax = f * 2^ex, f in [0.5, 1)
-          shift = 23 - ex;    // amax * 2^shift in [2^22, 2^23)
+      int shift = 0;
+      if (!isfinite(amax)) {
+        shift = 1 << 30;  // marks a non-finite embedding row: fp32 fallback
+      } else if (amax > 0.f) {
+        int ex;
+        frexpf(amax, &ex);  // amax = f * 2^ex, f in [0.5, 1)
+        shift = 23 - ex;    // amax * 2^shift in [2^22, 2^23)
+      }
+      if (lane == 0) sh_shift[b] = shift;
+      if (INT8 && tok >= 0 && shift != (1 << 30)) {
+        // This lane's 8 values k = 8 lane .. 8 lane + 7 become two words per limb.
+        const uint4 w = reinterpret_cast<const uint4*>(e_s + static_cast<size_t>(b) * kRank)[lane];
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+        uint32_t hl[2] = {0u, 0u}, ml[2] = {0u, 0u}, ll[2] = {0u, 0u};
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const float x = (t & 1) ? bf16_hi(ww[t >> 1]) : bf16_lo(ww[t >> 1]);
+          const int xi = __float2int_rn(mul_pow2(x, shift));
+          const int wsel = t >> 2, sh8 = 8 * (t & 3);
+          hl[wsel] |= (static_cast<uint32_t>(xi >> 16) & 0xFFu) << sh8;
+          ml[wsel] |= (static_cast<uint32_t>(xi >> 8) & 0xFFu) << sh8;
+          ll[wsel] |= (static_cast<uint32_t>(xi) & 0xFFu) << sh8;
         }
-        sh_shift[b] = shift;
+        uint32_t* lr = limb_s + static_cast<size_t>(b) * 3 * 64;
+        reinterpret_cast<uint2*>(lr)[lane] = make_uint2(hl[0], hl[1]);
+        reinterpret_cast<uint2*>(lr + 64)[lane] = make_uint2(ml[0], ml[1]);
+        reinterpret_cast<uint2*>(lr + 128)[lane] = make_uint2(ll[0], ll[1]);
       }
     }
     __syncthreads();
@@ -233,112 +287,157 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkPara
       const bool float_path = INT8 && shift == (1 << 30);
       const bool fill = !filled;
 
-      Limbs LA, LB;
-      float ef[32];
-      if (INT8 && !float_path) {
-        make_limbs(eb + 16 * j8, shift, LA);
-        make_limbs(eb + 16 * (j8 + 8), shift, LB);
-      } else {
-        const int cw = INT8 ? 16 : 8;  // values per chunk
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int chunk = j8 + 8 * (c / cw);
-          ef[c] = bf16_to_f32(eb[chunk * cw + (c % cw)]);
-        }
-      }
-
       const float inv_lo = pow2_lo(-shift), inv_hi = pow2_hi(-shift);
-      uint64_t best = 0ull;
-      // Warp-blocks of 32 rows: warp w takes blocks w, w + 16, ...
-      for (int r0 = 32 * warp; r0 < n; r0 += 32 * kWalkWarps) {
-        const bool from_smem = (i > 0 || !fill) && (r0 + 32 <= res);
-        const bool store_smem = fill && (r0 + 32 <= res);
-        const int rbase = r0 + 8 * grp;
-        // The lane's own epilogue row: fetch its base logit and scale before the
-        // contraction so the loads overlap it.
-        const int r_out = rbase + j8;
-        float base_v = 0.f, scale_v = 0.f;
-        if (r_out < n) {
-          const int64_t v = v0 + r_out;
-          base_v = bf16_to_f32(__ldg(p.base + (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v));
-          if (INT8) scale_v = __ldg(p.scales + v);
+
+      // The row loop, instantiated once with the integer limbs (int8 W2, finite
+      // embedding) and once with fp32 embedding values (bf16 W2, or the fallback for a
+      // non-finite embedding row), so each instance keeps only its own registers.
+      auto row_loop = [&](auto use_limbs_tag) -> uint64_t {
+        constexpr bool LIMBS = decltype(use_limbs_tag)::value;
+        Limbs LA, LB;
+        float ef[LIMBS ? 1 : 32];
+        if constexpr (LIMBS) {
+          const uint32_t* lr = limb_s + static_cast<size_t>(b) * 3 * 64;
+          load_limbs(lr, j8, LA);
+          load_limbs(lr, j8 + 8, LB);
+        } else {
+          constexpr int cw = INT8 ? 16 : 8;  // values per chunk
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int chunk = j8 + 8 * (c / cw);
+            ef[c] = bf16_to_f32(eb[chunk * cw + (c % cw)]);
+          }
         }
-        float fpart[8];
-        int hpart[8], mpart[8];
+        uint64_t best = 0ull;
+        // Warp w owns the 32-row blocks w, w + 16, ... of the slice. Blocks that are
+        // re-read from L2 every step (beyond the resident rows) come first so their
+        // latency overlaps the other warps' shared-memory blocks.
+        const int nblk = n > 32 * warp ? (n - 32 * warp + 32 * kWalkWarps - 1) / (32 * kWalkWarps) : 0;
+        int nres_blk = 0;  // the warp's resident blocks are its first nres_blk blocks
+        while (nres_blk < nblk && 32 * warp + 32 * kWalkWarps * nres_blk + 32 <= res) ++nres_blk;
+        // Position 0 brings the resident blocks in with asynchronous copies (one commit
+        // group per block, each lane copying exactly the chunks it reads later).
+        const bool fill_now = fill && i == 0;
+        if (fill_now) {
+          for (int t = 0; t < nres_blk; ++t) {
+            const int rb = 32 * warp + 32 * kWalkWarps * t + 8 * grp;
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr) {
-          const int r = rbase + rr;
-          constexpr int kChunks = INT8 ? 2 : 4;
-          uint4 q[kChunks];
+            for (int rr = 0; rr < 8; ++rr)
 #pragma unroll
-          for (int c = 0; c < kChunks; ++c) {
-            if (r < n) {
-              if (from_smem)
-                q[c] = reinterpret_cast<const uint4*>(w2s + static_cast<size_t>(r) * kRowBytes)[j8 + 8 * c];
-              else
-                q[c] = ld_row_chunk(w2g + static_cast<size_t>(r) * kRowBytes, j8 + 8 * c);
-              if (store_smem)
-                reinterpret_cast<uint4*>(w2s + static_cast<size_t>(r) * kRowBytes)[j8 + 8 * c] = q[c];
+              for (int c = 0; c < kRowBytes / 128; ++c) {
+                const size_t off = static_cast<size_t>(rb + rr) * kRowBytes + 16 * (j8 + 8 * c);
+                cp_async16(w2s + off, w2g + off);
+              }
+            cp_async_commit();
+          }
+        }
+        auto block_r0 = [&](int k) {  // k-th block in processing order
+          const int t = k < nblk - nres_blk ? nres_blk + k : k - (nblk - nres_blk);
+          return 32 * warp + 32 * kWalkWarps * t;
+        };
+        auto load_base = [&](int r) {
+          return r < n ? bf16_to_f32(__ldg(p.base + (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v0 + r))
+                       : 0.f;
+        };
+        float base_next = nblk > 0 ? load_base(block_r0(0) + 8 * grp + j8) : 0.f;
+        for (int k = 0; k < nblk; ++k) {
+          const int r0 = block_r0(k);
+          const bool resident = r0 + 32 <= res;
+          const bool from_smem = resident && (i > 0 || !fill || fill_now);
+          const bool store_smem = false;
+          if (fill_now && resident) cp_async_wait(nblk - 1 - k);
+          const int rbase = r0 + 8 * grp;
+          // The lane's own epilogue row: its base logit was loaded one block ahead.
+          const int r_out = rbase + j8;
+          const float base_v = base_next;
+          if (k + 1 < nblk) base_next = load_base(block_r0(k + 1) + 8 * grp + j8);
+          const float scale_v = (INT8 && r_out < n) ? scale_s[r_out] : 0.f;
+          float fpart[8];
+          int hpart[8], mpart[8];
+#pragma unroll
+          for (int rr = 0; rr < 8; ++rr) {
+            const int r = rbase + rr;
+            constexpr int kChunks = INT8 ? 2 : 4;
+            uint4 q[kChunks];
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) {
+              if (r < n) {
+                if (from_smem)
+                  q[c] = reinterpret_cast<const uint4*>(w2s + static_cast<size_t>(r) * kRowBytes)[j8 + 8 * c];
+                else
+                  q[c] = ld_row_chunk(w2g + static_cast<size_t>(r) * kRowBytes, j8 + 8 * c);
+                if (store_smem)
+                  reinterpret_cast<uint4*>(w2s + static_cast<size_t>(r) * kRowBytes)[j8 + 8 * c] = q[c];
+              } else {
+                q[c] = make_uint4(0u, 0u, 0u, 0u);
+              }
+            }
+            if constexpr (LIMBS) {
+              int h = 0, m = 0, l = 0;
+              dot_int8_chunk(q[0], LA, h, m, l);
+              dot_int8_chunk(q[1], LB, h, m, l);
+              hpart[rr] = h;
+              mpart[rr] = m * 256 + l;
+            } else if constexpr (INT8) {
+              float a = 0.f;
+              a = dot_int8_chunk_f32(q[0], ef, a);
+              a = dot_int8_chunk_f32(q[1], ef + 16, a);
+              fpart[rr] = a;
             } else {
-              q[c] = make_uint4(0u, 0u, 0u, 0u);
+              float a = 0.f;
+#pragma unroll
+              for (int c = 0; c < kChunks; ++c) a = dot_bf16_chunk(q[c], ef + 8 * c, a);
+              fpart[rr] = a;
             }
           }
-          if (INT8 && !float_path) {
-            int h = 0, m = 0, l = 0;
-            dot_int8_chunk(q[0], LA, h, m, l);
-            dot_int8_chunk(q[1], LB, h, m, l);
-            hpart[rr] = h;
-            mpart[rr] = m * 256 + l;
-          } else if (INT8) {
-            float a = 0.f;
-            a = dot_int8_chunk_f32(q[0], ef, a);
-            a = dot_int8_chunk_f32(q[1], ef + 16, a);
-            fpart[rr] = a;
+          float bias_raw;
+          if constexpr (LIMBS) {
+            const int H = butterfly8(hpart, lane);
+            const int M = butterfly8(mpart, lane);
+            bias_raw = __fadd_rn(__fmul_rn(static_cast<float>(H), 65536.f), static_cast<float>(M));
           } else {
-            float a = 0.f;
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c) a = dot_bf16_chunk(q[c], ef + 8 * c, a);
-            fpart[rr] = a;
+            bias_raw = butterfly8(fpart, lane);
+          }
+          if (r_out < n) {
+            const int64_t v = v0 + r_out;
+            // int8: scale_v * 2^-shift * sum; the power of two is applied last so that a
+            // tiny embedding row underflows gracefully instead of through 2^-shift.
+            float bias = bias_raw;
+            if constexpr (INT8) {
+              bias = __fmul_rn(bias_raw, scale_v);
+              if constexpr (LIMBS) bias = __fmul_rn(__fmul_rn(bias, inv_lo), inv_hi);
+            }
+            best = umax64(best, score_entry<PROB, LOGITS>(p, b, i, v, base_v, bias, seed));
           }
         }
-        float bias_raw;
-        if (INT8 && !float_path) {
-          const int H = butterfly8(hpart, lane);
-          const int M = butterfly8(mpart, lane);
-          bias_raw = __fadd_rn(__fmul_rn(static_cast<float>(H), 65536.f), static_cast<float>(M));
-        } else {
-          bias_raw = butterfly8(fpart, lane);
-        }
-        if (r_out < n) {
-          const int64_t v = v0 + r_out;
-          // int8: scale_v * 2^-shift * sum; the power of two is applied last so that a
-          // tiny embedding row underflows gracefully instead of through 2^-shift.
-          float bias = bias_raw;
-          if (INT8) {
-            bias = __fmul_rn(bias_raw, scale_v);
-            if (!float_path) bias = __fmul_rn(__fmul_rn(bias, inv_lo), inv_hi);
-          }
-          best = umax64(best, score_entry<PROB, LOGITS>(p, b, i, v, base_v, bias, seed));
-        }
-      }
-      // CTA argmax for row b, then one atomic into this position's slot.
+        return best;
+      };
+      uint64_t best;
+      if (INT8 && !float_path) best = row_loop(std::integral_constant<bool, INT8>{});
+      else best = row_loop(std::false_type{});
+
+      // CTA argmax for row b. Its W1 row goes towards L2 now: the grid-wide winner is
+      // one of the CTAs' local winners, so the next position's embedding load hits L2.
       best = warp_max64(best);
       if (lane == 0) red[warp] = best;
       __syncthreads();
       if (warp == 0) {
         uint64_t x = lane < kWalkWarps ? red[lane] : 0ull;
         x = warp_max64(x);
-        if (lane == 0 && x != 0ull) atomicMax(reinterpret_cast<unsigned long long*>(p.sync.slots + static_cast<size_t>(i) * p.bs + b),
-                                              static_cast<unsigned long long>(x));
+        if (lane == 0) best_s[b] = x;
+        if (x != 0ull && lane < 4 && i + 1 < p.K)
+          prefetch_l2(p.w1 + static_cast<size_t>(unpack_idx(x)) * kRank + 64 * lane);
       }
       filled = true;
       __syncthreads();
     }
+    for (int t = threadIdx.x; t < p.bs; t += blockDim.x)
+      if (prev_s[t] < 0) best_s[t] = 0ull;
 
-    if (!grid_step_barrier(p.sync, i, skip0 && i == 0, flag)) return;
+    if (!exchange_best(p.sync, i, p.bs, skip0 && i == 0, best_s, flag)) return;
+    if (i + 2 < p.K) prefetch_base_slice(p, v0, n, i + 2);
     for (int t = threadIdx.x; t < p.bs; t += blockDim.x) {
-      int tok = -1;
-      if (prev_s[t] >= 0) tok = unpack_idx(ld_relaxed_u64(p.sync.slots + static_cast<size_t>(i) * p.bs + t));
+      const int tok = prev_s[t] >= 0 ? unpack_idx(best_s[t]) : -1;
       prev_s[t] = tok;
       if (cta == 0) p.tokens[static_cast<size_t>(t) * p.K + i] = tok;
     }

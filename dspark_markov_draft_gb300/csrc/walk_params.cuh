@@ -23,6 +23,7 @@ struct WalkParams {
   float temperature;
   int32_t temp_is_one;
   int32_t resident_rows;     // W2 rows per CTA kept in shared memory (multiple of 32)
+  int32_t slice_cap;         // upper bound of the rows of one CTA's vocabulary slice
   StepSync sync;
 };
 
@@ -31,12 +32,15 @@ constexpr int kWalkThreads = 512;
 constexpr int kWalkWarps = kWalkThreads / 32;
 
 // Shared memory outside the resident W2 rows, per CTA.
-__host__ __device__ inline size_t walk_cc_fixed_smem(int bs) {
-  return static_cast<size_t>(bs) * kRank * 2  // W1[prev] rows, bf16
-         + 64 * 4                              // e-shift per row (int8 path)
-         + 64 * 4                              // prev tokens
-         + kWalkWarps * 8 + 64                 // reduction scratch, flags
-         + 256;                                // alignment slack
+__host__ __device__ inline size_t walk_cc_fixed_smem(int bs, bool int8, int slice_cap) {
+  return (int8 ? static_cast<size_t>(slice_cap) * 4 : 0)  // scales of the slice
+         + static_cast<size_t>(bs) * kRank * 2            // W1[prev] rows, bf16
+         + (int8 ? static_cast<size_t>(bs) * 3 * 64 * 4 : 0)  // their limb words
+         + 64 * 4                                         // e-shift per row (int8 path)
+         + 64 * 4                                         // prev tokens
+         + 64 * 8                                         // per-row argmax words
+         + kWalkWarps * 8 + 64                            // reduction scratch, flags
+         + 256;                                           // alignment slack
 }
 
 }  // namespace dspark

@@ -196,10 +196,11 @@ def test_bad_token_reported():
     assert list(t[1]) == [-1] * K and np.all(t[[0, 2]] >= 0)
 
 
-def test_timeout_returns_status_and_context_survives():
+@pytest.mark.parametrize("bs", [1, 8])
+def test_timeout_returns_status_and_context_survives(bs):
     """CTA 0 skips its first arrival: every wait gives up after 20 ms and reports
     TIMEOUT; after re-zeroing the workspace the next walk is correct."""
-    V, K, bs = 4000, 3, 2
+    V, K = 4000, 3
     inp = synth.make(V, bs, K, seed=4)
     w1, w2, base, prev, seeds = to_dev(inp)
     ws = capi.alloc_workspace(V, bs, K)
@@ -216,8 +217,9 @@ def test_timeout_returns_status_and_context_survives():
     assert int(status.item()) == 0 and torch.equal(t1, t2)
 
 
-def test_workspace_left_zeroed_and_reusable():
-    V, K, bs = 7000, 6, 4
+@pytest.mark.parametrize("bs", [1, 4, 8])
+def test_workspace_left_zeroed_and_reusable(bs):
+    V, K = 7000, 6
     inp = synth.make(V, bs, K, seed=8)
     w1, w2, base, prev, seeds = to_dev(inp)
     ws = capi.alloc_workspace(V, bs, K)
