@@ -11,6 +11,7 @@
 namespace dspark {
 
 const void* walk_cc_kernel_ptr(bool int8, bool prob, bool logits);
+const void* walk_tc_kernel_ptr(bool int8, bool prob, bool logits, int nq);
 const void* topk_walk_kernel_ptr(bool prob, bool logits);
 cudaError_t launch_topk_select(const uint16_t* base, int64_t V, int k, int rows, int32_t* cand,
                                uint16_t* logits, cudaStream_t stream);
@@ -85,6 +86,40 @@ Plan plan_dense(const DeviceCaps& caps, int64_t V, bool int8, int bs, int cap_ro
   rows = rows & ~31LL;
   const int64_t need = (per_cta + 31) & ~31LL;
   if (rows > need) rows = need;
+  if (cap_rows >= 0 && rows > cap_rows) rows = cap_rows & ~31;
+  pl.resident_rows = static_cast<int>(rows);
+  pl.smem = fixed + static_cast<size_t>(rows) * row_bytes;
+  return pl;
+}
+
+// Smallest batch that takes the tensor-core contraction by default.
+constexpr int kTcMinBs = 2;
+
+struct TcPlan {
+  int grid;
+  int resident_rows;  // per CTA
+  int slice_cap;
+  int nq;             // padded request rows / 4
+  size_t smem;
+};
+
+// Tensor-core walk: B operand (N x 512 bytes), the slice's scales, bookkeeping, and as
+// many resident W2 rows as the remaining shared memory holds.
+TcPlan plan_tc(const DeviceCaps& caps, int64_t V, bool int8, int bs, int cap_rows) {
+  TcPlan pl{};
+  pl.grid = caps.sms;
+  const int N = bs <= 16 ? 16 : bs <= 32 ? 32 : 64;
+  pl.nq = N / 4;
+  const int64_t per_cta = (V + pl.grid - 1) / pl.grid + 32;
+  pl.slice_cap = static_cast<int>((per_cta + 31) & ~31LL);
+  const int row_bytes = int8 ? kRank : 2 * kRank;
+  const size_t fixed = 1024 + static_cast<size_t>(N) * 512 + (int8 ? static_cast<size_t>(pl.slice_cap) * 4 : 0) +
+                       walk_tc_misc_smem();
+  int64_t rows = caps.smem_optin > static_cast<int>(fixed)
+                     ? (static_cast<int64_t>(caps.smem_optin) - static_cast<int64_t>(fixed)) / row_bytes
+                     : 0;
+  rows &= ~31LL;
+  if (rows > pl.slice_cap) rows = pl.slice_cap;
   if (cap_rows >= 0 && rows > cap_rows) rows = cap_rows & ~31;
   pl.resident_rows = static_cast<int>(rows);
   pl.smem = fixed + static_cast<size_t>(rows) * row_bytes;
@@ -259,10 +294,19 @@ int32_t dspark_walk(const dspark_walk_args* a, dspark_stream_t stream) {
   if ((st = current_caps(&caps)) != DSPARK_OK) return st;
   if (!caps.coop) return DSPARK_ERR_UNSUPPORTED;
   const bool int8 = a->w2q != nullptr;
+  const bool lg = a->draft_logits != nullptr;
+  const bool prob = a->mode == DSPARK_PROBABILISTIC;
+  const bool use_tc = !(a->flags & DSPARK_FLAG_FORCE_CUDA_CORES) &&
+                      (a->bs >= kTcMinBs || (a->flags & DSPARK_FLAG_FORCE_TENSOR_CORES));
+  if (use_tc) {
+    const TcPlan pl = plan_tc(caps, a->V, int8, a->bs, a->resident_rows_cap);
+    WalkParams p = make_params(a, pl.grid, pl.resident_rows, pl.slice_cap);
+    return launch_coop(walk_tc_kernel_ptr(int8, prob, lg, pl.nq), pl.grid, pl.smem, p,
+                       reinterpret_cast<cudaStream_t>(stream));
+  }
   const Plan pl = plan_dense(caps, a->V, int8, a->bs, a->resident_rows_cap);
   WalkParams p = make_params(a, pl.grid, pl.resident_rows, pl.slice_cap);
-  const bool lg = a->draft_logits != nullptr;
-  const void* fn = walk_cc_kernel_ptr(int8, a->mode == DSPARK_PROBABILISTIC, lg);
+  const void* fn = walk_cc_kernel_ptr(int8, prob, lg);
   return launch_coop(fn, pl.grid, pl.smem, p, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -168,18 +168,6 @@ __device__ __forceinline__ uint64_t score_entry(const WalkParams& p, int b, int 
   return pack_best(order_key(s), static_cast<uint32_t>(v));
 }
 
-// Prefetch this CTA's base-logit slices of position i (all rows) towards L2.
-__device__ __forceinline__ void prefetch_base_slice(const WalkParams& p, int64_t v0, int n, int i) {
-  if (i >= p.K) return;
-  const int lines = (n * 2 + 127) / 128 + 1;
-  for (int t = threadIdx.x; t < lines * p.bs; t += blockDim.x) {
-    const int b = t / lines, l = t % lines;
-    const uint16_t* row = p.base + (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v0;
-    const int64_t off = min(static_cast<int64_t>(l) * 64, static_cast<int64_t>(n - 1));
-    prefetch_l2(row + off);
-  }
-}
-
 }  // namespace
 
 template <bool INT8, bool PROB, bool LOGITS>

@@ -43,4 +43,33 @@ __host__ __device__ inline size_t walk_cc_fixed_smem(int bs, bool int8, int slic
          + 256;                                           // alignment slack
 }
 
+// Prefetch this CTA's base-logit slices of position i (all rows) towards L2.
+__device__ __forceinline__ void prefetch_base_slice(const WalkParams& p, int64_t v0, int n, int i) {
+  if (i >= p.K || n <= 0) return;
+  const int lines = (n * 2 + 127) / 128 + 1;
+  for (int t = threadIdx.x; t < lines * p.bs; t += blockDim.x) {
+    const int b = t / lines, l = t % lines;
+    const uint16_t* row = p.base + (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v0;
+    const int64_t off = min(static_cast<int64_t>(l) * 64, static_cast<int64_t>(n - 1));
+    prefetch_l2(row + off);
+  }
+}
+
+// Vocabulary slice of CTA c: starts are multiples of 32 (so a group of 4 consecutive
+// entries never straddles two CTAs), the last slice ends at V.
+__host__ __device__ inline int64_t slice_start(int c, int G, int64_t V) {
+  if (c <= 0) return 0;
+  if (c >= G) return V;
+  return (static_cast<int64_t>(c) * V / G) & ~static_cast<int64_t>(31);
+}
+
+// Tensor-core walk: shared memory besides the B operand and the resident rows.
+__host__ __device__ inline size_t walk_tc_misc_smem() {
+  return 64 * 4      // e-shift per row
+         + 64 * 4    // prev tokens
+         + 64 * 8    // per-row argmax words
+         + 4 * 64 * 8  // per-quadrant argmax words
+         + 64;       // mbarriers, TMEM base, flag
+}
+
 }  // namespace dspark

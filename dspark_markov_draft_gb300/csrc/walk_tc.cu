@@ -1,0 +1,560 @@
+// Full-vocabulary Markov draft walk with the bias contraction on the 5th-generation
+// tensor cores (tcgen05), for batches where W2 . E[256 x bs] is a real dense GEMM.
+// Same method and per-position exchange as the CUDA-core walk (vLLM PR #62958,
+// "Overview": one cooperative kernel for the whole walk, W2 on chip where it fits,
+// one packed atomic per step for the cross-CTA argmax).
+//
+// Per CTA (one per SM, 16 warps) and per draft position:
+//   * B operand: the bs embedding rows W1[prev_b] (N = 16, 32 or 64 rows, zero
+//     padded), 16-bit, K-major, 128-byte swizzled in shared memory. With int8 W2 each
+//     row is scaled by a power of two 2^s_b so that max|e| lies in [2^14, 2^15) and
+//     converted to fp16 (exact for every bf16 value within 2^-28 of the row maximum;
+//     inf and NaN stay inf and NaN); with bf16 W2 the rows are used as they are.
+//   * A operand: 128 W2 rows per tile, written by all warps straight into tensor
+//     memory (tcgen05.st): int8 codes become exact fp16 integers through a byte
+//     permute with 0x64 exponent bytes and one packed subtract; bf16 rows are copied.
+//     Thread (quadrant q, lane l) owns tile row 32q + l, warp group kq = warp / 4
+//     owns K range [64 kq, 64 kq + 64). Rows of the slice that fit stay resident in
+//     shared memory (XOR-swizzled 16-byte chunks, conflict-free for this access),
+//     brought in at position 0 with cp.async; the rest are re-read from L2.
+//   * D[128 x N] = A . B^T accumulates in fp32 in tensor memory (16 MMAs of K = 16);
+//     A and D are double-buffered so the MMAs of one tile overlap the epilogue of the
+//     previous tile and the production of the next.
+//   * Epilogue: each warp reads its quadrant's rows for its N/4 columns, transposes
+//     4 x 4 blocks across lanes so that a thread owns 4 consecutive vocabulary entries
+//     of one request row (one Philox call, one 8-byte base load, one 8-byte logits
+//     store per 4 entries), forms l = base + scale_v * 2^-s_b * D and the score, and
+//     keeps a running (orderable key, first index) maximum per request row.
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "walk_params.cuh"
+
+namespace dspark {
+
+namespace {
+
+constexpr int kTile = 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColA0 = 0, kColA1 = 128, kColD0 = 256, kColD1 = 384;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// sm_100 shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1) << 16;            // leading offset (unused here)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;    // stride between 8-row groups
+  d |= static_cast<uint64_t>(1) << 46;            // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;            // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B both fp16 (fmt 0) or
+// both bf16 (fmt 1), both K-major, M = 128, N.
+__host__ __device__ constexpr uint32_t f16_idesc(uint32_t fmt, int N) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(kTile >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(smem_u32(mbar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t* mbar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
+  return done != 0;
+}
+
+// Bounded wait for an mbarrier phase; false after timeout_ns of wall-clock time.
+__device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, uint64_t timeout_ns) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try(mbar, parity)) return true;
+    if ((it & 15u) == 15u) {
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > timeout_ns) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};"
+      ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+        "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+        "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]),
+        "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+        "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+template <int NQ>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&out)[NQ]);
+template <>
+__device__ __forceinline__ void tmem_ld<4>(uint32_t taddr, float (&o)[4]) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(taddr) : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 4; ++j) o[j] = __uint_as_float(r[j]);
+}
+template <>
+__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, float (&o)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7]) : "r"(taddr) : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 8; ++j) o[j] = __uint_as_float(r[j]);
+}
+template <>
+__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float (&o)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]) : "r"(taddr) : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(r[j]);
+}
+
+// 4 x 4 transpose inside each group of 4 lanes: on entry lane j holds row j
+// (x[c] = a[j][c]); on return it holds column j (x[r] = a[r][j]).
+__device__ __forceinline__ void transpose4(float (&x)[4], int lane) {
+  const bool odd = lane & 1, hi = lane & 2;
+  const float s0 = odd ? x[0] : x[1];
+  const float s1 = odd ? x[2] : x[3];
+  const float r0 = __shfl_xor_sync(kFull, s0, 1);
+  const float r1 = __shfl_xor_sync(kFull, s1, 1);
+  if (odd) { x[0] = r0; x[2] = r1; } else { x[1] = r0; x[3] = r1; }
+  const float t0 = hi ? x[0] : x[2];
+  const float t1 = hi ? x[1] : x[3];
+  const float q0 = __shfl_xor_sync(kFull, t0, 2);
+  const float q1 = __shfl_xor_sync(kFull, t1, 2);
+  if (hi) { x[0] = q0; x[1] = q1; } else { x[2] = q0; x[3] = q1; }
+}
+
+// Four int8 codes (one 32-bit word) as two fp16x2 words holding the exact integers.
+__device__ __forceinline__ void int8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = w ^ 0x80808080u;  // biased bytes q + 128 in [1, 255]
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(x), "r"(0x64646464u));  // 1024 + byte
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(x), "r"(0x64646464u));
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));  // 1152
+  const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+  const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+  lo = *reinterpret_cast<const uint32_t*>(&ha);
+  hi = *reinterpret_cast<const uint32_t*>(&hb);
+}
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_pending(int pending) {
+  switch (pending) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+  }
+}
+
+}  // namespace
+
+// NQ = N / 4 columns per warp (N = 16, 32 or 64 padded request rows).
+template <bool INT8, bool PROB, bool LOGITS, int NQ>
+__global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkParams p) {
+  constexpr int N = 4 * NQ;
+  constexpr int kRowBytes = INT8 ? kRank : 2 * kRank;
+  constexpr int kChunks = kRowBytes / 16;            // 16-byte chunks per W2 row
+  constexpr int kThrChunks = kChunks / 4;            // chunks per thread per row (4 or 8)
+  constexpr uint32_t kIdesc = f16_idesc(INT8 ? 0u : 1u, N);
+
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* b_s = smem;                                      // N x 512 bytes
+  unsigned char* w2s = b_s + N * 512;                             // resident rows
+  float* scale_s = reinterpret_cast<float*>(w2s + static_cast<size_t>(p.resident_rows) * kRowBytes);
+  int* sh_shift = reinterpret_cast<int*>(scale_s + (INT8 ? p.slice_cap : 0));
+  int* prev_s = sh_shift + 64;
+  uint64_t* best_s = reinterpret_cast<uint64_t*>(prev_s + 64);
+  uint64_t* red_s = best_s + 64;                                  // [4][64]
+  uint64_t* mbar = red_s + 4 * 64;                                // [2]
+  uint32_t* tbase_s = reinterpret_cast<uint32_t*>(mbar + 2);
+  int* flag = reinterpret_cast<int*>(tbase_s + 1);
+
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int q = warp & 3, kq = warp >> 2;
+  const int64_t v0 = slice_start(cta, G, p.V), v1 = slice_start(cta + 1, G, p.V);
+  const int n = static_cast<int>(v1 - v0);
+  const int res = min(p.resident_rows, n);
+  const int T = (n + kTile - 1) / kTile;
+  const unsigned char* w2g = (INT8 ? reinterpret_cast<const unsigned char*>(p.w2q)
+                                   : reinterpret_cast<const unsigned char*>(p.w2)) +
+                             static_cast<size_t>(v0) * kRowBytes;
+  const bool skip0 = (p.sync.flags & DSPARK_FLAG_SKIP_ARRIVAL_CTA0) && cta == 0;
+
+  // ---- set-up: zero B, scales, previous tokens, barriers, tensor memory
+  for (int t = tid; t < N * 512 / 16; t += blockDim.x) reinterpret_cast<uint4*>(b_s)[t] = make_uint4(0, 0, 0, 0);
+  if (INT8)
+    for (int r = tid; r < n; r += blockDim.x) scale_s[r] = __ldg(p.scales + v0 + r);
+  for (int t = tid; t < p.bs; t += blockDim.x) {
+    const int32_t tok = p.prev[t];
+    const bool ok = tok >= 0 && static_cast<int64_t>(tok) < p.V;
+    prev_s[t] = ok ? tok : -1;
+    if (!ok && cta == 0) report(p.sync.status_dev, DSPARK_ERR_BAD_TOKEN);
+  }
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[0])));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[1])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(tbase_s)), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  prefetch_base_slice(p, v0, n, 0);
+  prefetch_base_slice(p, v0, n, 1);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tbase_s;
+  const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+  uint32_t phase[2] = {0u, 0u};
+  bool ok = true;
+
+  // Produce A for tile t into tensor-memory columns a_col (this thread's row and K range).
+  auto produce = [&](int t, uint32_t a_col, bool fill_now) {
+    const int rr = t * kTile + 32 * q + lane;
+    uint4 c[kThrChunks];
+    if (rr < n) {
+      const bool resident = rr < res;
+#pragma unroll
+      for (int j = 0; j < kThrChunks; ++j) {
+        const int ch = kThrChunks * kq + j;
+        if (resident) {
+          const int pos = ch ^ (rr & (kChunks - 1));
+          c[j] = *reinterpret_cast<const uint4*>(w2s + static_cast<size_t>(rr) * kRowBytes + 16 * pos);
+        } else {
+          c[j] = __ldg(reinterpret_cast<const uint4*>(w2g + static_cast<size_t>(rr) * kRowBytes) + ch);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kThrChunks; ++j) c[j] = make_uint4(0, 0, 0, 0);
+    }
+    (void)fill_now;
+    uint32_t v[32];
+    if constexpr (INT8) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        int8x4_to_f16x4(c[j].x, v[8 * j + 0], v[8 * j + 1]);
+        int8x4_to_f16x4(c[j].y, v[8 * j + 2], v[8 * j + 3]);
+        int8x4_to_f16x4(c[j].z, v[8 * j + 4], v[8 * j + 5]);
+        int8x4_to_f16x4(c[j].w, v[8 * j + 6], v[8 * j + 7]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        v[4 * j + 0] = c[j].x;
+        v[4 * j + 1] = c[j].y;
+        v[4 * j + 2] = c[j].z;
+        v[4 * j + 3] = c[j].w;
+      }
+    }
+    tmem_st32(tmem + lane_off + a_col + 32 * kq, v);
+  };
+
+  auto issue_mma = [&](int t) {
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t a_col = (t & 1) ? kColA1 : kColA0;
+      const uint32_t d_col = (t & 1) ? kColD1 : kColD0;
+      const uint32_t b_base = smem_u32(b_s);
+#pragma unroll
+      for (int kk = 0; kk < kRank / 16; ++kk) {
+        const uint64_t bd = sw128_desc(b_base + (kk / 4) * N * 128 + (kk % 4) * 32);
+        mma_f16(tmem + d_col, tmem + a_col + 8 * kk, bd, kIdesc, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(&mbar[t & 1]);
+    }
+  };
+
+  for (int i = 0; i < p.K && ok; ++i) {
+    // ---- B operand: the embedding rows of this position's previous tokens
+    for (int b = warp; b < p.bs; b += kWalkWarps) {
+      const int tok = prev_s[b];
+      uint4 w = make_uint4(0, 0, 0, 0);
+      if (tok >= 0) w = __ldg(reinterpret_cast<const uint4*>(p.w1 + static_cast<size_t>(tok) * kRank) + lane);
+      int shift = 0;
+      if constexpr (INT8) {
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+        float amax = 0.f;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float lo = bf16_lo(ww[t]), hi = bf16_hi(ww[t]);
+          if (isfinite(lo)) amax = fmaxf(amax, fabsf(lo));
+          if (isfinite(hi)) amax = fmaxf(amax, fabsf(hi));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+        if (amax > 0.f) {
+          int ex;
+          frexpf(amax, &ex);  // amax = f 2^ex, f in [0.5, 1)
+          shift = 15 - ex;    // amax 2^shift in [2^14, 2^15)
+        }
+        const float s_lo = __int_as_float((shift / 2 + 127) << 23);
+        const float s_hi = __int_as_float((shift - shift / 2 + 127) << 23);
+        uint32_t h[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float a = __fmul_rn(__fmul_rn(bf16_lo(ww[t]), s_lo), s_hi);
+          const float c = __fmul_rn(__fmul_rn(bf16_hi(ww[t]), s_lo), s_hi);
+          const __half2 hh = __floats2half2_rn(a, c);
+          h[t] = *reinterpret_cast<const uint32_t*>(&hh);
+        }
+        w = make_uint4(h[0], h[1], h[2], h[3]);
+      }
+      if (lane == 0) sh_shift[b] = shift;
+      const int kb = lane >> 3, ch = lane & 7;
+      *reinterpret_cast<uint4*>(b_s + kb * N * 128 + b * 128 + ((ch ^ (b & 7)) * 16)) = w;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+
+    // ---- position 0: bring the resident rows in (one commit group per tile)
+    const bool fill_now = (i == 0);
+    int n_res_tiles = 0;
+    if (fill_now) {
+      for (int t = 0; t < T; ++t) {
+        const int rr = t * kTile + 32 * q + lane;
+        if (t * kTile >= res) break;
+        if (rr < res) {
+#pragma unroll
+          for (int j = 0; j < kThrChunks; ++j) {
+            const int ch = kThrChunks * kq + j;
+            const int pos = ch ^ (rr & (kChunks - 1));
+            cp_async16(w2s + static_cast<size_t>(rr) * kRowBytes + 16 * pos,
+                       w2g + static_cast<size_t>(rr) * kRowBytes + 16 * ch);
+          }
+        }
+        cp_async_commit();
+        ++n_res_tiles;
+      }
+    }
+
+    __syncthreads();  // B written and visible to the tensor core; shifts published
+    // Per-column constants (read only after the barrier: other warps wrote the shifts).
+    float inv_lo[NQ / 4], inv_hi[NQ / 4];
+    uint64_t seed[NQ / 4];
+    bool live[NQ / 4];
+    uint64_t best[NQ / 4];
+#pragma unroll
+    for (int g = 0; g < NQ / 4; ++g) {
+      const int b = kq * NQ + 4 * g + (lane & 3);
+      live[g] = b < p.bs && prev_s[min(b, 63)] >= 0;
+      const int sft = (INT8 && b < p.bs) ? sh_shift[b] : 0;
+      inv_lo[g] = __int_as_float(((-sft) / 2 + 127) << 23);
+      inv_hi[g] = __int_as_float(((-sft) - (-sft) / 2 + 127) << 23);
+      seed[g] = (PROB && b < p.bs) ? p.seeds[b] : 0ull;
+      best[g] = 0ull;
+    }
+
+    if (T > 0) {
+      if (fill_now && n_res_tiles > 0) cp_async_wait_pending(n_res_tiles - 1);
+      produce(0, kColA0, fill_now);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncthreads();
+      issue_mma(0);
+    }
+
+    for (int t = 0; t < T; ++t) {
+      if (t + 1 < T) {
+        if (fill_now && t + 1 < n_res_tiles) cp_async_wait_pending(n_res_tiles - 2 - t);
+        produce(t + 1, ((t + 1) & 1) ? kColA1 : kColA0, fill_now);
+      }
+      const bool waited = mbar_wait(&mbar[t & 1], phase[t & 1], p.sync.timeout_ns);
+      if (__syncthreads_or(!waited)) {
+        // Report, then give the MMA one more bounded chance to finish before the
+        // tensor memory it writes is released.
+        if (tid == 0) give_up(p.sync);
+        mbar_wait(&mbar[t & 1], phase[t & 1], p.sync.timeout_ns);
+        ok = false;
+        break;
+      }
+      phase[t & 1] ^= 1u;
+      tc_fence_after();
+
+      // ---- epilogue of tile t
+      float d[NQ];
+      tmem_ld<NQ>(tmem + lane_off + ((t & 1) ? kColD1 : kColD0) + kq * NQ, d);
+      const int rr0 = t * kTile + 32 * q + 4 * (lane >> 2);  // first of this thread's 4 rows
+      float sc[4] = {1.f, 1.f, 1.f, 1.f};
+      if constexpr (INT8) {
+        if (rr0 + 3 < n) {
+          const float4 s4 = *reinterpret_cast<const float4*>(scale_s + rr0);
+          sc[0] = s4.x; sc[1] = s4.y; sc[2] = s4.z; sc[3] = s4.w;
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) sc[k] = rr0 + k < n ? scale_s[rr0 + k] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < NQ / 4; ++g) {
+        float x[4] = {d[4 * g + 0], d[4 * g + 1], d[4 * g + 2], d[4 * g + 3]};
+        transpose4(x, lane);
+        if (!live[g] || rr0 >= n) continue;
+        const int b = kq * NQ + 4 * g + (lane & 3);
+        const size_t o = (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v0 + rr0;
+        const bool full4 = rr0 + 3 < n && (reinterpret_cast<uintptr_t>(p.base + o) & 7u) == 0 &&
+                           (!LOGITS || (reinterpret_cast<uintptr_t>(p.logits + o) & 7u) == 0);
+        float bv[4];
+        if (full4) {
+          const uint2 u = __ldg(reinterpret_cast<const uint2*>(p.base + o));
+          bv[0] = bf16_lo(u.x); bv[1] = bf16_hi(u.x); bv[2] = bf16_lo(u.y); bv[3] = bf16_hi(u.y);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) bv[k] = rr0 + k < n ? bf16_to_f32(p.base[o + k]) : 0.f;
+        }
+        float l[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float bias = x[k];
+          if constexpr (INT8) bias = __fmul_rn(__fmul_rn(__fmul_rn(bias, sc[k]), inv_lo[g]), inv_hi[g]);
+          l[k] = __fadd_rn(bv[k], bias);
+        }
+        if constexpr (LOGITS) {
+          uint16_t h[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) h[k] = f32_to_bf16_bits(l[k]);
+          if (full4) {
+            *reinterpret_cast<uint2*>(p.logits + o) =
+                make_uint2(static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 16),
+                           static_cast<uint32_t>(h[2]) | (static_cast<uint32_t>(h[3]) << 16));
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (rr0 + k < n) p.logits[o + k] = h[k];
+          }
+        }
+        float s[4] = {l[0], l[1], l[2], l[3]};
+        if constexpr (PROB) {
+          const uint4 w = philox_block(seed[g], b, i, static_cast<uint32_t>((v0 + rr0) >> 2));
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float lb = bf16_to_f32(f32_to_bf16_bits(l[k]));
+            const float xs = p.temp_is_one ? lb : __fdiv_rn(lb, p.temperature);
+            s[k] = __fadd_rn(xs, gumbel_from_word(ws[k]));
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (rr0 + k < n)
+            best[g] = umax64(best[g], pack_best(order_key(s[k]), static_cast<uint32_t>(v0 + rr0 + k)));
+      }
+      if (t + 1 < T) asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncthreads();
+      if (t + 1 < T) issue_mma(t + 1);
+    }
+    if (!ok) break;
+
+    // ---- CTA argmax per request row: lanes sharing (lane & 3) hold the same column
+#pragma unroll
+    for (int g = 0; g < NQ / 4; ++g) {
+      uint64_t x = best[g];
+      x = umax64(x, __shfl_xor_sync(kFull, x, 4));
+      x = umax64(x, __shfl_xor_sync(kFull, x, 8));
+      x = umax64(x, __shfl_xor_sync(kFull, x, 16));
+      if (lane < 4) red_s[q * 64 + kq * NQ + 4 * g + lane] = x;
+    }
+    __syncthreads();
+    if (tid < p.bs) {
+      uint64_t x = umax64(umax64(red_s[tid], red_s[64 + tid]), umax64(red_s[128 + tid], red_s[192 + tid]));
+      if (prev_s[tid] < 0) x = 0ull;
+      best_s[tid] = x;
+      if (x != 0ull && i + 1 < p.K) {
+        const uint16_t* row = p.w1 + static_cast<size_t>(unpack_idx(x)) * kRank;
+#pragma unroll
+        for (int l4 = 0; l4 < 4; ++l4) prefetch_l2(row + 64 * l4);
+      }
+    }
+    if (!exchange_best(p.sync, i, p.bs, skip0 && i == 0, best_s, flag)) { ok = false; break; }
+    for (int t = tid; t < p.bs; t += blockDim.x) {
+      const int tok = prev_s[t] >= 0 ? unpack_idx(best_s[t]) : -1;
+      prev_s[t] = tok;
+      if (cta == 0) p.tokens[static_cast<size_t>(t) * p.K + i] = tok;
+    }
+    reset_behind(p.sync, i, p.bs);
+    if (i + 2 < p.K) prefetch_base_slice(p, v0, n, i + 2);
+    __syncthreads();
+  }
+
+  // ---- release tensor memory (every MMA has completed or the wait gave up); no
+  // asynchronous copy may still be writing shared memory when the CTA exits.
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  if (ok) finish_walk(p.sync, p.K, p.bs, flag);
+}
+
+const void* walk_tc_kernel_ptr(bool int8, bool prob, bool logits, int nq) {
+#define DSPARK_TC(I, P, L)                                                  \
+  if (int8 == I && prob == P && logits == L) {                              \
+    if (nq == 4) return (const void*)walk_tc_kernel<I, P, L, 4>;            \
+    if (nq == 8) return (const void*)walk_tc_kernel<I, P, L, 8>;            \
+    return (const void*)walk_tc_kernel<I, P, L, 16>;                        \
+  }
+  DSPARK_TC(true, false, false)
+  DSPARK_TC(true, false, true)
+  DSPARK_TC(true, true, false)
+  DSPARK_TC(true, true, true)
+  DSPARK_TC(false, false, false)
+  DSPARK_TC(false, false, true)
+  DSPARK_TC(false, true, false)
+  DSPARK_TC(false, true, true)
+#undef DSPARK_TC
+  return nullptr;
+}
+
+}  // namespace dspark

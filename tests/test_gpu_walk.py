@@ -102,6 +102,33 @@ def test_walk_small_parity(oracle, int8, mode, T, bs, logits, cap):
     check_walk(oracle, inp, tokens, mode=mode, T=T, q=q_ref, sc=sc_ref, gpu_logits=lg)
 
 
+PATH_FLAGS = {"cuda_cores": capi.FLAG_FORCE_CUDA_CORES, "tensor_cores": capi.FLAG_FORCE_TENSOR_CORES}
+
+
+@pytest.mark.parametrize("path", ["cuda_cores", "tensor_cores"])
+@pytest.mark.parametrize("bs", [1, 5, 20, 40, 64])
+@pytest.mark.parametrize("int8,mode,T,logits", [(True, capi.GREEDY, 1.0, True),
+                                                (False, capi.PROBABILISTIC, 0.7, True),
+                                                (True, capi.PROBABILISTIC, 1.0, False)])
+def test_both_contraction_paths_match_oracle(oracle, path, bs, int8, mode, T, logits):
+    """Each contraction path (CUDA cores, tcgen05 tensor cores with N = 16/32/64) on
+    its own, for several batch sizes, against the oracle."""
+    V, K = 5003, 3
+    inp = synth.make(V, bs, K, seed=50 + bs, peak=8.0)
+    w1, w2, base, prev, seeds = to_dev(inp)
+    q_ref = sc_ref = None
+    wk = dict(w2=w2)
+    if int8:
+        q, sc = capi.quantize_w2(w2)
+        _, q_ref, sc_ref = oracle.quantize_w2(bits(inp.w2))
+        wk = dict(w2q=q, scales=sc)
+    rows = list(range(bs)) if bs <= 8 else [0, bs // 2, bs - 1]
+    tokens, lg = capi.walk(base, w1, prev, seeds=seeds, mode=mode, temperature=T,
+                           want_logits=logits, flags=PATH_FLAGS[path], **wk)
+    torch.cuda.synchronize()
+    check_walk(oracle, inp, tokens, mode=mode, T=T, q=q_ref, sc=sc_ref, gpu_logits=lg, rows=rows)
+
+
 @pytest.mark.parametrize("int8", [True, False])
 def test_resident_split_does_not_change_results(int8):
     V, K, bs = 20011, 4, 2
@@ -111,14 +138,16 @@ def test_resident_split_does_not_change_results(int8):
     if int8:
         q, sc = capi.quantize_w2(w2)
         wk = dict(w2q=q, scales=sc)
-    outs = []
-    for cap in (0, 32, 64, -1):
-        t, lg = capi.walk(base, w1, prev, seeds=seeds, mode=capi.PROBABILISTIC, temperature=0.9,
-                          want_logits=True, resident_rows_cap=cap, **wk)
-        outs.append((t.cpu(), lg.cpu()))
-    for t, lg in outs[1:]:
-        assert torch.equal(t, outs[0][0])
-        assert torch.equal(lg.view(torch.int16), outs[0][1].view(torch.int16))
+    for flags in (capi.FLAG_FORCE_CUDA_CORES, capi.FLAG_FORCE_TENSOR_CORES):
+        outs = []
+        for cap in (0, 32, 64, -1):
+            t, lg = capi.walk(base, w1, prev, seeds=seeds, mode=capi.PROBABILISTIC,
+                              temperature=0.9, want_logits=True, resident_rows_cap=cap,
+                              flags=flags, **wk)
+            outs.append((t.cpu(), lg.cpu()))
+        for t, lg in outs[1:]:
+            assert torch.equal(t, outs[0][0])
+            assert torch.equal(lg.view(torch.int16), outs[0][1].view(torch.int16))
 
 
 def test_integer_inputs_bit_exact_logits(oracle):
