@@ -54,12 +54,34 @@ __device__ __forceinline__ uint32_t uint4_get(const uint4& w, int j) {
   return j == 0 ? w.x : j == 1 ? w.y : j == 2 ? w.z : w.w;
 }
 
+// -ln(u) for u in (0, 1) with a small RELATIVE error everywhere, including u -> 1
+// where the largest Gumbel values come from:
+//   * u <= 0.75: -log2(u) ln 2 from the hardware base-2 logarithm; |log2 u| >= 0.41
+//     there, so its ~2^-22 error is below 6e-7 relative;
+//   * u > 0.75: t = 1 - u is exact, and -ln(1 - t) = 2 atanh(s) with s = t / (2 - t)
+//     in (0, 1/7], summed as the series 2 s (1 + s^2/3 + s^4/5 + s^6/7) (the first
+//     omitted term is below 3e-15 relative).
+__device__ __forceinline__ float neg_log_unit(float u) {
+  float l2, r;
+  asm("lg2.approx.f32 %0, %1;" : "=f"(l2) : "f"(u));
+  const float a = -l2 * 0.693147180559945f;
+  const float t = 1.f - u;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(2.f - t));
+  const float sv = t * r;
+  const float s2 = sv * sv;
+  const float poly = fmaf(s2, fmaf(s2, fmaf(s2, 0.142857142857143f, 0.2f), 0.333333333333333f), 1.f);
+  const float b = 2.f * sv * poly;
+  return u > 0.75f ? b : a;
+}
+
 // u = (2 * (w >> 9) + 1) * 2^-24 lies strictly inside (0, 1) and is exact in fp32;
-// g = -log(-log(u)) with the full-precision logf (its accuracy near u -> 1 matters,
-// since that is where the largest noise values come from).
+// g = -ln(-ln(u)): the inner logarithm as above, the outer one (argument in
+// [6e-8, 16.7]) from the hardware base-2 logarithm, absolute error below 5e-6.
 __device__ __forceinline__ float gumbel_from_word(uint32_t w) {
   const float u = static_cast<float>(2u * (w >> 9) + 1u) * 5.9604644775390625e-08f;
-  return -logf(-logf(u));
+  float l2;
+  asm("lg2.approx.f32 %0, %1;" : "=f"(l2) : "f"(neg_log_unit(u)));
+  return -l2 * 0.693147180559945f;
 }
 
 // ---------------------------------------------------------------- argmax words

@@ -69,7 +69,8 @@ __host__ __device__ inline size_t walk_tc_misc_smem() {
          + 64 * 4    // prev tokens
          + 64 * 8    // per-row argmax words
          + 4 * 64 * 8  // per-quadrant argmax words
-         + 64;       // mbarriers, TMEM base, flag
+         + 64 * 8      // per-row 2^-s factors
+         + 12 * 8 + 16;  // mbarriers, TMEM base, flag
 }
 
 }  // namespace dspark

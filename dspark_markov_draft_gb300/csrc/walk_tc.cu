@@ -10,21 +10,22 @@
 //     row is scaled by a power of two 2^s_b so that max|e| lies in [2^14, 2^15) and
 //     converted to fp16 (exact for every bf16 value within 2^-28 of the row maximum;
 //     inf and NaN stay inf and NaN); with bf16 W2 the rows are used as they are.
-//   * A operand: 128 W2 rows per tile, written by all warps straight into tensor
-//     memory (tcgen05.st): int8 codes become exact fp16 integers through a byte
-//     permute with 0x64 exponent bytes and one packed subtract; bf16 rows are copied.
-//     Thread (quadrant q, lane l) owns tile row 32q + l, warp group kq = warp / 4
-//     owns K range [64 kq, 64 kq + 64). Rows of the slice that fit stay resident in
-//     shared memory (XOR-swizzled 16-byte chunks, conflict-free for this access),
-//     brought in at position 0 with cp.async; the rest are re-read from L2.
-//   * D[128 x N] = A . B^T accumulates in fp32 in tensor memory (16 MMAs of K = 16);
-//     A and D are double-buffered so the MMAs of one tile overlap the epilogue of the
-//     previous tile and the production of the next.
-//   * Epilogue: each warp reads its quadrant's rows for its N/4 columns, transposes
-//     4 x 4 blocks across lanes so that a thread owns 4 consecutive vocabulary entries
-//     of one request row (one Philox call, one 8-byte base load, one 8-byte logits
-//     store per 4 entries), forms l = base + scale_v * 2^-s_b * D and the score, and
-//     keeps a running (orderable key, first index) maximum per request row.
+//   * A operand: 128 W2 rows per tile, written into tensor memory (tcgen05.st) by 8
+//     producer warps: int8 codes become exact fp16 integers through a byte permute
+//     with 0x64 exponent bytes and one packed subtract; bf16 rows are copied. Rows of
+//     the slice that fit stay resident in shared memory (XOR-swizzled 16-byte chunks,
+//     conflict-free for this access), brought in at position 0 with cp.async; the
+//     rest are re-read from L2.
+//   * D[128 x N] = A . B^T accumulates in fp32 in tensor memory. One thread issues an
+//     MMA only about every 70 cycles whatever N is, so the K range is split in two
+//     halves issued by two threads into two accumulators, which the epilogue adds.
+//   * Epilogue (8 warps): each warp reads its quadrant's rows for its N/2 columns,
+//     transposes 4 x 4 blocks across lanes so that a thread owns 4 consecutive
+//     vocabulary entries of one request row (one Philox call, one 8-byte base load,
+//     one 8-byte logits store per 4 entries), forms l = base + scale_v 2^-s_b D and
+//     the score, and keeps a running (orderable key, first index) maximum per row.
+//   * Producers, MMA issuers and the epilogue hand tiles over through mbarriers, with
+//     two A and two D buffers, so the three overlap across tiles.
 #include <cstdint>
 #include <cuda_fp16.h>
 
@@ -37,7 +38,7 @@ namespace {
 
 constexpr int kTile = 128;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColA0 = 0, kColA1 = 128, kColD0 = 256, kColD1 = 384;
+constexpr uint32_t kColA0 = 0, kColA1 = 128;  // A buffers; D buffers follow at column 256
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -112,17 +113,22 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       : "memory");
 }
 
+// The same store from 8 raw 16-byte chunks (bf16 rows need no conversion).
+__device__ __forceinline__ void tmem_st32_u4(uint32_t taddr, const uint4 (&c)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};"
+      ::"r"(taddr), "r"(c[0].x), "r"(c[0].y), "r"(c[0].z), "r"(c[0].w), "r"(c[1].x), "r"(c[1].y),
+        "r"(c[1].z), "r"(c[1].w), "r"(c[2].x), "r"(c[2].y), "r"(c[2].z), "r"(c[2].w), "r"(c[3].x),
+        "r"(c[3].y), "r"(c[3].z), "r"(c[3].w), "r"(c[4].x), "r"(c[4].y), "r"(c[4].z), "r"(c[4].w),
+        "r"(c[5].x), "r"(c[5].y), "r"(c[5].z), "r"(c[5].w), "r"(c[6].x), "r"(c[6].y), "r"(c[6].z),
+        "r"(c[6].w), "r"(c[7].x), "r"(c[7].y), "r"(c[7].z), "r"(c[7].w)
+      : "memory");
+}
+
 template <int NQ>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&out)[NQ]);
-template <>
-__device__ __forceinline__ void tmem_ld<4>(uint32_t taddr, float (&o)[4]) {
-  uint32_t r[4];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(taddr) : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int j = 0; j < 4; ++j) o[j] = __uint_as_float(r[j]);
-}
 template <>
 __device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, float (&o)[8]) {
   uint32_t r[8];
@@ -133,20 +139,6 @@ __device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, float (&o)[8]) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) o[j] = __uint_as_float(r[j]);
 }
-template <>
-__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float (&o)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]) : "r"(taddr) : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(r[j]);
-}
-
 // 4 x 4 transpose inside each group of 4 lanes: on entry lane j holds row j
 // (x[c] = a[j][c]); on return it holds column j (x[r] = a[r][j]).
 __device__ __forceinline__ void transpose4(float (&x)[4], int lane) {
@@ -195,14 +187,27 @@ __device__ __forceinline__ void cp_async_wait_pending(int pending) {
 
 }  // namespace
 
-// NQ = N / 4 columns per warp (N = 16, 32 or 64 padded request rows).
-template <bool INT8, bool PROB, bool LOGITS, int NQ>
+// N = 16, 32 or 64 padded request rows. Warp roles inside the tile pipeline:
+//   warps 0-7   producers: quadrant w & 3 (tensor-memory lanes), K half w >> 2; each
+//               thread converts half of one W2 row of the tile into tensor memory.
+//               Lane 0 of warp 0 / warp 4 also issues the 8 MMAs of its K half, into
+//               its own accumulator, as soon as the 4 producer warps of that half are
+//               done (two issuing threads double the MMA issue rate).
+//   warps 8-15  epilogue: quadrant w & 3, column half (w - 8) >> 2; each sums the two
+//               K-half accumulators and scores the entries.
+// Roles hand tiles over through mbarriers (A full/empty per buffer and K half, D
+// full/empty per buffer), with two A and two D buffers in tensor memory.
+template <bool INT8, bool PROB, bool LOGITS, int N>
 __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkParams p) {
-  constexpr int N = 4 * NQ;
+  constexpr int NC = N / 2;                          // columns per epilogue warp
+  constexpr int CH = 8;                              // columns per tensor-memory load
+  constexpr int NG = NC / 4;                         // 4-column groups per epilogue thread
   constexpr int kRowBytes = INT8 ? kRank : 2 * kRank;
   constexpr int kChunks = kRowBytes / 16;            // 16-byte chunks per W2 row
-  constexpr int kThrChunks = kChunks / 4;            // chunks per thread per row (4 or 8)
+  constexpr int kHalfChunks = kChunks / 2;           // per producer thread and tile
+  constexpr int kPassChunks = INT8 ? 4 : 8;          // chunks per 32-column store
   constexpr uint32_t kIdesc = f16_idesc(INT8 ? 0u : 1u, N);
+  constexpr uint32_t kColD = 256;                    // D[buf][half] at kColD + (2 buf + half) N
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -214,13 +219,17 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
   int* prev_s = sh_shift + 64;
   uint64_t* best_s = reinterpret_cast<uint64_t*>(prev_s + 64);
   uint64_t* red_s = best_s + 64;                                  // [4][64]
-  uint64_t* mbar = red_s + 4 * 64;                                // [2]
-  uint32_t* tbase_s = reinterpret_cast<uint32_t*>(mbar + 2);
+  float2* inv_s = reinterpret_cast<float2*>(red_s + 4 * 64);       // [64] 2^-s as two factors
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(inv_s + 64);       // [12]
+  uint64_t* a_full = mbar;        // [buf * 2 + half], 4 arrivals
+  uint64_t* a_empty = mbar + 4;   // [buf * 2 + half], 1 commit
+  uint64_t* d_full = mbar + 8;    // [buf], 2 commits
+  uint64_t* d_empty = mbar + 10;  // [buf], 8 arrivals
+  uint32_t* tbase_s = reinterpret_cast<uint32_t*>(mbar + 12);
   int* flag = reinterpret_cast<int*>(tbase_s + 1);
 
   const int G = gridDim.x, cta = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int q = warp & 3, kq = warp >> 2;
   const int64_t v0 = slice_start(cta, G, p.V), v1 = slice_start(cta + 1, G, p.V);
   const int n = static_cast<int>(v1 - v0);
   const int res = min(p.resident_rows, n);
@@ -229,6 +238,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
                                    : reinterpret_cast<const unsigned char*>(p.w2)) +
                              static_cast<size_t>(v0) * kRowBytes;
   const bool skip0 = (p.sync.flags & DSPARK_FLAG_SKIP_ARRIVAL_CTA0) && cta == 0;
+  const bool producer = warp < 8;
+  const int q = warp & 3;                                          // tensor-memory lane quadrant
+  const int half = (warp >> 2) & 1;                                // producers: K half; epilogue: column half
 
   // ---- set-up: zero B, scales, previous tokens, barriers, tensor memory
   for (int t = tid; t < N * 512 / 16; t += blockDim.x) reinterpret_cast<uint4*>(b_s)[t] = make_uint4(0, 0, 0, 0);
@@ -236,13 +248,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
     for (int r = tid; r < n; r += blockDim.x) scale_s[r] = __ldg(p.scales + v0 + r);
   for (int t = tid; t < p.bs; t += blockDim.x) {
     const int32_t tok = p.prev[t];
-    const bool ok = tok >= 0 && static_cast<int64_t>(tok) < p.V;
-    prev_s[t] = ok ? tok : -1;
-    if (!ok && cta == 0) report(p.sync.status_dev, DSPARK_ERR_BAD_TOKEN);
+    const bool okt = tok >= 0 && static_cast<int64_t>(tok) < p.V;
+    prev_s[t] = okt ? tok : -1;
+    if (!okt && cta == 0) report(p.sync.status_dev, DSPARK_ERR_BAD_TOKEN);
   }
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[0])));
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&mbar[1])));
+    const uint32_t counts[12] = {4, 4, 4, 4, 1, 1, 1, 1, 2, 2, 8, 8};
+    for (int b = 0; b < 12; ++b)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&mbar[b])), "r"(counts[b]));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -257,72 +270,26 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
   tc_fence_after();
   const uint32_t tmem = *tbase_s;
   const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
-  uint32_t phase[2] = {0u, 0u};
   bool ok = true;
-
-  // Produce A for tile t into tensor-memory columns a_col (this thread's row and K range).
-  auto produce = [&](int t, uint32_t a_col, bool fill_now) {
-    const int rr = t * kTile + 32 * q + lane;
-    uint4 c[kThrChunks];
-    if (rr < n) {
-      const bool resident = rr < res;
-#pragma unroll
-      for (int j = 0; j < kThrChunks; ++j) {
-        const int ch = kThrChunks * kq + j;
-        if (resident) {
-          const int pos = ch ^ (rr & (kChunks - 1));
-          c[j] = *reinterpret_cast<const uint4*>(w2s + static_cast<size_t>(rr) * kRowBytes + 16 * pos);
-        } else {
-          c[j] = __ldg(reinterpret_cast<const uint4*>(w2g + static_cast<size_t>(rr) * kRowBytes) + ch);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < kThrChunks; ++j) c[j] = make_uint4(0, 0, 0, 0);
-    }
-    (void)fill_now;
-    uint32_t v[32];
-    if constexpr (INT8) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        int8x4_to_f16x4(c[j].x, v[8 * j + 0], v[8 * j + 1]);
-        int8x4_to_f16x4(c[j].y, v[8 * j + 2], v[8 * j + 3]);
-        int8x4_to_f16x4(c[j].z, v[8 * j + 4], v[8 * j + 5]);
-        int8x4_to_f16x4(c[j].w, v[8 * j + 6], v[8 * j + 7]);
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        v[4 * j + 0] = c[j].x;
-        v[4 * j + 1] = c[j].y;
-        v[4 * j + 2] = c[j].z;
-        v[4 * j + 3] = c[j].w;
-      }
-    }
-    tmem_st32(tmem + lane_off + a_col + 32 * kq, v);
-  };
-
-  auto issue_mma = [&](int t) {
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t a_col = (t & 1) ? kColA1 : kColA0;
-      const uint32_t d_col = (t & 1) ? kColD1 : kColD0;
-      const uint32_t b_base = smem_u32(b_s);
-#pragma unroll
-      for (int kk = 0; kk < kRank / 16; ++kk) {
-        const uint64_t bd = sw128_desc(b_base + (kk / 4) * N * 128 + (kk % 4) * 32);
-        mma_f16(tmem + d_col, tmem + a_col + 8 * kk, bd, kIdesc, kk > 0 ? 1u : 0u);
-      }
-      mma_commit(&mbar[t & 1]);
-    }
-  };
+  int g_base = 0;        // tiles processed by all earlier positions (buffer / phase bookkeeping)
+  int last_issued = -1;  // issuers: last tile whose MMAs were committed
 
   for (int i = 0; i < p.K && ok; ++i) {
     // ---- B operand: the embedding rows of this position's previous tokens
-    for (int b = warp; b < p.bs; b += kWalkWarps) {
-      const int tok = prev_s[b];
-      uint4 w = make_uint4(0, 0, 0, 0);
-      if (tok >= 0) w = __ldg(reinterpret_cast<const uint4*>(p.w1 + static_cast<size_t>(tok) * kRank) + lane);
+    // (at most 4 rows per warp: issue every load before converting any row)
+    uint4 wrow[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int b = warp + kWalkWarps * r;
+      const int tok = b < p.bs ? prev_s[b] : -1;
+      wrow[r] = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(p.w1 + static_cast<size_t>(tok) * kRank) + lane)
+                         : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int b = warp + kWalkWarps * r;
+      if (b >= p.bs) break;
+      uint4 w = wrow[r];
       int shift = 0;
       if constexpr (INT8) {
         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
@@ -352,161 +319,255 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
         }
         w = make_uint4(h[0], h[1], h[2], h[3]);
       }
-      if (lane == 0) sh_shift[b] = shift;
+      if (lane == 0) {
+        sh_shift[b] = shift;
+        inv_s[b] = make_float2(__int_as_float(((-shift) / 2 + 127) << 23),
+                               __int_as_float(((-shift) - (-shift) / 2 + 127) << 23));
+      }
       const int kb = lane >> 3, ch = lane & 7;
       *reinterpret_cast<uint4*>(b_s + kb * N * 128 + b * 128 + ((ch ^ (b & 7)) * 16)) = w;
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();  // B written and visible to the tensor core; shifts published
 
-    // ---- position 0: bring the resident rows in (one commit group per tile)
-    const bool fill_now = (i == 0);
-    int n_res_tiles = 0;
-    if (fill_now) {
-      for (int t = 0; t < T; ++t) {
-        const int rr = t * kTile + 32 * q + lane;
-        if (t * kTile >= res) break;
-        if (rr < res) {
+    bool failed = false;
+    if (producer) {
+      // ---------------------------------------------------------------- producers
+      const bool fill_now = (i == 0);
+      int n_res_tiles = 0;
+      if (fill_now) {  // position 0: resident rows arrive through cp.async, a group per tile
+        for (int t = 0; t < T && t * kTile < res; ++t) {
+          const int rr = t * kTile + 32 * q + lane;
+          if (rr < res) {
 #pragma unroll
-          for (int j = 0; j < kThrChunks; ++j) {
-            const int ch = kThrChunks * kq + j;
+            for (int j = 0; j < kHalfChunks; ++j) {
+              const int ch = kHalfChunks * half + j;
+              const int pos = ch ^ (rr & (kChunks - 1));
+              cp_async16(w2s + static_cast<size_t>(rr) * kRowBytes + 16 * pos,
+                         w2g + static_cast<size_t>(rr) * kRowBytes + 16 * ch);
+            }
+          }
+          cp_async_commit();
+          ++n_res_tiles;
+        }
+      }
+      // This thread's half row of tile t: kHalfChunks 16-byte chunks, loaded as passes
+      // of kPassChunks (one 32-column tensor-memory store each).
+      auto load_pass = [&](int t, int pass, uint4 (&c)[kPassChunks]) {
+        const int rr = t * kTile + 32 * q + lane;
+#pragma unroll
+        for (int j = 0; j < kPassChunks; ++j) {
+          const int ch = kHalfChunks * half + kPassChunks * pass + j;
+          if (rr >= n) {
+            c[j] = make_uint4(0, 0, 0, 0);
+          } else if (rr < res) {
             const int pos = ch ^ (rr & (kChunks - 1));
-            cp_async16(w2s + static_cast<size_t>(rr) * kRowBytes + 16 * pos,
-                       w2g + static_cast<size_t>(rr) * kRowBytes + 16 * ch);
+            c[j] = *reinterpret_cast<const uint4*>(w2s + static_cast<size_t>(rr) * kRowBytes + 16 * pos);
+          } else {
+            c[j] = __ldg(reinterpret_cast<const uint4*>(w2g + static_cast<size_t>(rr) * kRowBytes) + ch);
           }
         }
-        cp_async_commit();
-        ++n_res_tiles;
-      }
-    }
-
-    __syncthreads();  // B written and visible to the tensor core; shifts published
-    // Per-column constants (read only after the barrier: other warps wrote the shifts).
-    float inv_lo[NQ / 4], inv_hi[NQ / 4];
-    uint64_t seed[NQ / 4];
-    bool live[NQ / 4];
-    uint64_t best[NQ / 4];
+      };
+      auto store_pass = [&](const uint4 (&c)[kPassChunks], uint32_t col) {
+        if constexpr (INT8) {
+          uint32_t v[32];
 #pragma unroll
-    for (int g = 0; g < NQ / 4; ++g) {
-      const int b = kq * NQ + 4 * g + (lane & 3);
-      live[g] = b < p.bs && prev_s[min(b, 63)] >= 0;
-      const int sft = (INT8 && b < p.bs) ? sh_shift[b] : 0;
-      inv_lo[g] = __int_as_float(((-sft) / 2 + 127) << 23);
-      inv_hi[g] = __int_as_float(((-sft) - (-sft) / 2 + 127) << 23);
-      seed[g] = (PROB && b < p.bs) ? p.seeds[b] : 0ull;
-      best[g] = 0ull;
-    }
-
-    if (T > 0) {
-      if (fill_now && n_res_tiles > 0) cp_async_wait_pending(n_res_tiles - 1);
-      produce(0, kColA0, fill_now);
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      tc_fence_before();
-      __syncthreads();
-      issue_mma(0);
-    }
-
-    for (int t = 0; t < T; ++t) {
-      if (t + 1 < T) {
-        if (fill_now && t + 1 < n_res_tiles) cp_async_wait_pending(n_res_tiles - 2 - t);
-        produce(t + 1, ((t + 1) & 1) ? kColA1 : kColA0, fill_now);
-      }
-      const bool waited = mbar_wait(&mbar[t & 1], phase[t & 1], p.sync.timeout_ns);
-      if (__syncthreads_or(!waited)) {
-        // Report, then give the MMA one more bounded chance to finish before the
-        // tensor memory it writes is released.
-        if (tid == 0) give_up(p.sync);
-        mbar_wait(&mbar[t & 1], phase[t & 1], p.sync.timeout_ns);
-        ok = false;
-        break;
-      }
-      phase[t & 1] ^= 1u;
-      tc_fence_after();
-
-      // ---- epilogue of tile t
-      float d[NQ];
-      tmem_ld<NQ>(tmem + lane_off + ((t & 1) ? kColD1 : kColD0) + kq * NQ, d);
-      const int rr0 = t * kTile + 32 * q + 4 * (lane >> 2);  // first of this thread's 4 rows
-      float sc[4] = {1.f, 1.f, 1.f, 1.f};
-      if constexpr (INT8) {
-        if (rr0 + 3 < n) {
-          const float4 s4 = *reinterpret_cast<const float4*>(scale_s + rr0);
-          sc[0] = s4.x; sc[1] = s4.y; sc[2] = s4.z; sc[3] = s4.w;
+          for (int j = 0; j < 4; ++j) {
+            int8x4_to_f16x4(c[j].x, v[8 * j + 0], v[8 * j + 1]);
+            int8x4_to_f16x4(c[j].y, v[8 * j + 2], v[8 * j + 3]);
+            int8x4_to_f16x4(c[j].z, v[8 * j + 4], v[8 * j + 5]);
+            int8x4_to_f16x4(c[j].w, v[8 * j + 6], v[8 * j + 7]);
+          }
+          tmem_st32(tmem + lane_off + col, v);
         } else {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) sc[k] = rr0 + k < n ? scale_s[rr0 + k] : 0.f;
+          tmem_st32_u4(tmem + lane_off + col, c);
         }
+      };
+      // int8: both passes of the next tile are prefetched; bf16 (twice the bytes): the
+      // first pass is prefetched and the second loaded just before its store.
+      uint4 c0[kPassChunks], c1[kPassChunks];
+      if (T > 0) {
+        if (fill_now && n_res_tiles > 0) cp_async_wait_pending(n_res_tiles - 1);
+        load_pass(0, 0, c0);
+        if constexpr (INT8) load_pass(0, 1, c1);
       }
-#pragma unroll
-      for (int g = 0; g < NQ / 4; ++g) {
-        float x[4] = {d[4 * g + 0], d[4 * g + 1], d[4 * g + 2], d[4 * g + 3]};
-        transpose4(x, lane);
-        if (!live[g] || rr0 >= n) continue;
-        const int b = kq * NQ + 4 * g + (lane & 3);
-        const size_t o = (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v0 + rr0;
-        const bool full4 = rr0 + 3 < n && (reinterpret_cast<uintptr_t>(p.base + o) & 7u) == 0 &&
-                           (!LOGITS || (reinterpret_cast<uintptr_t>(p.logits + o) & 7u) == 0);
-        float bv[4];
-        if (full4) {
-          const uint2 u = __ldg(reinterpret_cast<const uint2*>(p.base + o));
-          bv[0] = bf16_lo(u.x); bv[1] = bf16_hi(u.x); bv[2] = bf16_lo(u.y); bv[3] = bf16_hi(u.y);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) bv[k] = rr0 + k < n ? bf16_to_f32(p.base[o + k]) : 0.f;
+      for (int t = 0; t < T; ++t) {
+        const int g = g_base + t, buf = g & 1, u = g >> 1;
+        if (u >= 1 && !mbar_wait(&a_empty[buf * 2 + half], (u - 1) & 1, p.sync.timeout_ns)) failed = true;
+        if (__shfl_sync(kFull, failed ? 1 : 0, 0)) { failed = true; break; }
+        tc_fence_after();
+        const uint32_t acol = (buf ? kColA1 : kColA0) + 64 * half;
+        store_pass(c0, acol);
+        if constexpr (!INT8) load_pass(t, 1, c1);
+        store_pass(c1, acol + 32);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&a_full[buf * 2 + half])) : "memory");
+        if (t + 1 < T) {  // next tile's data in flight while this warp issues or waits
+          if (fill_now && t + 1 < n_res_tiles) cp_async_wait_pending(n_res_tiles - 2 - t);
+          load_pass(t + 1, 0, c0);
+          if constexpr (INT8) load_pass(t + 1, 1, c1);
         }
-        float l[4];
+        if ((warp & 3) == 0 && lane == 0) {
+          // MMA issue for this K half: A complete (all 4 quadrants), D buffer free.
+          bool good = mbar_wait(&a_full[buf * 2 + half], u & 1, p.sync.timeout_ns);
+          if (good && u >= 1) good = mbar_wait(&d_empty[buf], (u - 1) & 1, p.sync.timeout_ns);
+          if (!good) {
+            failed = true;
+          } else {
+            tc_fence_after();
+            const uint32_t a_col = buf ? kColA1 : kColA0;
+            const uint32_t d_col = kColD + (2 * buf + half) * N;
+            const uint32_t b_base = smem_u32(b_s);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float bias = x[k];
-          if constexpr (INT8) bias = __fmul_rn(__fmul_rn(__fmul_rn(bias, sc[k]), inv_lo[g]), inv_hi[g]);
-          l[k] = __fadd_rn(bv[k], bias);
+            for (int k8 = 0; k8 < 8; ++k8) {
+              const int kk = 8 * half + k8;
+              const uint64_t bd = sw128_desc(b_base + (kk / 4) * N * 128 + (kk % 4) * 32);
+              mma_f16(tmem + d_col, tmem + a_col + 8 * kk, bd, kIdesc, k8 > 0 ? 1u : 0u);
+            }
+            mma_commit(&d_full[buf]);
+            mma_commit(&a_empty[buf * 2 + half]);
+            last_issued = g;
+          }
         }
-        if constexpr (LOGITS) {
-          uint16_t h[4];
+        if (__shfl_sync(kFull, failed ? 1 : 0, 0)) { failed = true; break; }
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    } else {
+      // ---------------------------------------------------------------- epilogue
+      // Column c of this thread's group j: b = half * NC + 4 j + (lane & 3).
+      uint32_t live_mask = 0;
+      uint64_t best[NG];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) h[k] = f32_to_bf16_bits(l[k]);
-          if (full4) {
-            *reinterpret_cast<uint2*>(p.logits + o) =
-                make_uint2(static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 16),
-                           static_cast<uint32_t>(h[2]) | (static_cast<uint32_t>(h[3]) << 16));
+      for (int j = 0; j < NG; ++j) {
+        const int b = half * NC + 4 * j + (lane & 3);
+        if (b < p.bs && prev_s[b] >= 0) live_mask |= 1u << j;
+        best[j] = 0ull;
+      }
+      auto fetch_base = [&](int t, uint2 (&bw)[NG]) {
+        const int rr0 = t * kTile + 32 * q + 4 * (lane >> 2);
+#pragma unroll
+        for (int j = 0; j < NG; ++j) {
+          bw[j] = make_uint2(0u, 0u);
+          if (!((live_mask >> j) & 1u) || rr0 >= n) continue;
+          const int b = half * NC + 4 * j + (lane & 3);
+          const uint16_t* src = p.base + (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v0 + rr0;
+          if (rr0 + 3 < n && (reinterpret_cast<uintptr_t>(src) & 7u) == 0) {
+            bw[j] = __ldg(reinterpret_cast<const uint2*>(src));
+          } else {
+            uint16_t h[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) h[k] = rr0 + k < n ? src[k] : 0;
+            bw[j] = make_uint2(static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 16),
+                               static_cast<uint32_t>(h[2]) | (static_cast<uint32_t>(h[3]) << 16));
+          }
+        }
+      };
+      uint2 bcur[NG], bnext[NG];
+      if (T > 0) fetch_base(0, bcur);
+      for (int t = 0; t < T; ++t) {
+        const int g = g_base + t, buf = g & 1, u = g >> 1;
+        if (t + 1 < T) fetch_base(t + 1, bnext);
+        if (!mbar_wait(&d_full[buf], u & 1, p.sync.timeout_ns)) failed = true;
+        if (__shfl_sync(kFull, failed ? 1 : 0, 0)) { failed = true; break; }
+        tc_fence_after();
+        const int rr0 = t * kTile + 32 * q + 4 * (lane >> 2);  // this thread's 4 rows
+        float sc[4] = {1.f, 1.f, 1.f, 1.f};
+        if constexpr (INT8) {
+          if (rr0 + 3 < n) {
+            const float4 s4 = *reinterpret_cast<const float4*>(scale_s + rr0);
+            sc[0] = s4.x; sc[1] = s4.y; sc[2] = s4.z; sc[3] = s4.w;
           } else {
 #pragma unroll
+            for (int k = 0; k < 4; ++k) sc[k] = rr0 + k < n ? scale_s[rr0 + k] : 0.f;
+          }
+        }
+#pragma unroll
+        for (int cc = 0; cc < NC / CH; ++cc) {
+          float d[CH], d2[CH];
+          const uint32_t dcol = kColD + 2 * buf * N + half * NC + cc * CH;
+          tmem_ld<CH>(tmem + lane_off + dcol, d);        // K half 0
+          tmem_ld<CH>(tmem + lane_off + dcol + N, d2);   // K half 1
+#pragma unroll
+          for (int k = 0; k < CH; ++k) d[k] = __fadd_rn(d[k], d2[k]);
+#pragma unroll
+          for (int gg = 0; gg < CH / 4; ++gg) {
+            const int j = cc * (CH / 4) + gg;
+            float x[4] = {d[4 * gg + 0], d[4 * gg + 1], d[4 * gg + 2], d[4 * gg + 3]};
+            transpose4(x, lane);
+            if (!((live_mask >> j) & 1u) || rr0 >= n) continue;
+            const int b = half * NC + 4 * j + (lane & 3);
+            const size_t o = (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v0 + rr0;
+            const float bv[4] = {bf16_lo(bcur[j].x), bf16_hi(bcur[j].x), bf16_lo(bcur[j].y), bf16_hi(bcur[j].y)};
+            float l[4];
+            const float2 inv = INT8 ? inv_s[b] : make_float2(1.f, 1.f);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float bias = x[k];
+              if constexpr (INT8) bias = __fmul_rn(__fmul_rn(__fmul_rn(bias, sc[k]), inv.x), inv.y);
+              l[k] = __fadd_rn(bv[k], bias);
+            }
+            if constexpr (LOGITS) {
+              uint16_t h[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) h[k] = f32_to_bf16_bits(l[k]);
+              if (rr0 + 3 < n && (reinterpret_cast<uintptr_t>(p.logits + o) & 7u) == 0) {
+                *reinterpret_cast<uint2*>(p.logits + o) =
+                    make_uint2(static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 16),
+                               static_cast<uint32_t>(h[2]) | (static_cast<uint32_t>(h[3]) << 16));
+              } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  if (rr0 + k < n) p.logits[o + k] = h[k];
+              }
+            }
+            float sco[4] = {l[0], l[1], l[2], l[3]};
+            if constexpr (PROB) {
+              const uint4 w = philox_block(p.seeds[b], b, i, static_cast<uint32_t>((v0 + rr0) >> 2));
+              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float lb = bf16_to_f32(f32_to_bf16_bits(l[k]));
+                const float xs = p.temp_is_one ? lb : __fdiv_rn(lb, p.temperature);
+                sco[k] = __fadd_rn(xs, gumbel_from_word(ws[k]));
+              }
+            }
+#pragma unroll
             for (int k = 0; k < 4; ++k)
-              if (rr0 + k < n) p.logits[o + k] = h[k];
+              if (rr0 + k < n)
+                best[j] = umax64(best[j], pack_best(order_key(sco[k]), static_cast<uint32_t>(v0 + rr0 + k)));
           }
         }
-        float s[4] = {l[0], l[1], l[2], l[3]};
-        if constexpr (PROB) {
-          const uint4 w = philox_block(seed[g], b, i, static_cast<uint32_t>((v0 + rr0) >> 2));
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&d_empty[buf])) : "memory");
+        if (t + 1 < T) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float lb = bf16_to_f32(f32_to_bf16_bits(l[k]));
-            const float xs = p.temp_is_one ? lb : __fdiv_rn(lb, p.temperature);
-            s[k] = __fadd_rn(xs, gumbel_from_word(ws[k]));
-          }
+          for (int j = 0; j < NG; ++j) bcur[j] = bnext[j];
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          if (rr0 + k < n)
-            best[g] = umax64(best[g], pack_best(order_key(s[k]), static_cast<uint32_t>(v0 + rr0 + k)));
       }
-      if (t + 1 < T) asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      tc_fence_before();
-      __syncthreads();
-      if (t + 1 < T) issue_mma(t + 1);
-    }
-    if (!ok) break;
-
-    // ---- CTA argmax per request row: lanes sharing (lane & 3) hold the same column
+      // CTA argmax per request row: lanes sharing (lane & 3) hold the same column.
 #pragma unroll
-    for (int g = 0; g < NQ / 4; ++g) {
-      uint64_t x = best[g];
-      x = umax64(x, __shfl_xor_sync(kFull, x, 4));
-      x = umax64(x, __shfl_xor_sync(kFull, x, 8));
-      x = umax64(x, __shfl_xor_sync(kFull, x, 16));
-      if (lane < 4) red_s[q * 64 + kq * NQ + 4 * g + lane] = x;
+      for (int j = 0; j < NG; ++j) {
+        uint64_t x = best[j];
+        x = umax64(x, __shfl_xor_sync(kFull, x, 4));
+        x = umax64(x, __shfl_xor_sync(kFull, x, 8));
+        x = umax64(x, __shfl_xor_sync(kFull, x, 16));
+        if (lane < 4) red_s[q * 64 + half * NC + 4 * j + lane] = x;
+      }
     }
-    __syncthreads();
+    g_base += T;
+    if (__syncthreads_or(failed)) {
+      // Report, then let the issued MMAs finish (bounded) before tensor memory goes.
+      if (tid == 0) give_up(p.sync);
+      if (producer && (warp & 3) == 0 && lane == 0 && last_issued >= 0)
+        mbar_wait(&a_empty[(last_issued & 1) * 2 + half], (last_issued >> 1) & 1, p.sync.timeout_ns);
+      ok = false;
+      break;
+    }
+
     if (tid < p.bs) {
       uint64_t x = umax64(umax64(red_s[tid], red_s[64 + tid]), umax64(red_s[128 + tid], red_s[192 + tid]));
       if (prev_s[tid] < 0) x = 0ull;
@@ -528,8 +589,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
     __syncthreads();
   }
 
-  // ---- release tensor memory (every MMA has completed or the wait gave up); no
-  // asynchronous copy may still be writing shared memory when the CTA exits.
+  // ---- release tensor memory (every MMA has completed or the bounded wait gave up)
   asm volatile("cp.async.wait_all;" ::: "memory");
   tc_fence_before();
   __syncthreads();
@@ -541,9 +601,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
 const void* walk_tc_kernel_ptr(bool int8, bool prob, bool logits, int nq) {
 #define DSPARK_TC(I, P, L)                                                  \
   if (int8 == I && prob == P && logits == L) {                              \
-    if (nq == 4) return (const void*)walk_tc_kernel<I, P, L, 4>;            \
-    if (nq == 8) return (const void*)walk_tc_kernel<I, P, L, 8>;            \
-    return (const void*)walk_tc_kernel<I, P, L, 16>;                        \
+    if (nq == 4) return (const void*)walk_tc_kernel<I, P, L, 16>;           \
+    if (nq == 8) return (const void*)walk_tc_kernel<I, P, L, 32>;           \
+    return (const void*)walk_tc_kernel<I, P, L, 64>;                        \
   }
   DSPARK_TC(true, false, false)
   DSPARK_TC(true, false, true)
