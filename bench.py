@@ -63,21 +63,105 @@ def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         d = json.load(open(path))
-        return dict(hbm_gbs=float(d["hbm_gbs"]), src="measured")
-    return dict(hbm_gbs=6800.0, src="fallback")
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    sm_mhz=float(d.get("sm_max_mhz", 2070.0)), src="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, sm_mhz=2070.0, src="fallback")
+
+
+# Per-SM issue rates used for the on-chip floors (nominal Blackwell figures): 128 bytes
+# of shared memory per clock, 64 dp4a lanes per clock (half the fp32 lanes), 128 fp32
+# FMA lanes per clock.
+SMEM_B_PER_CLK = 128
+DP4A_PER_CLK = 64
+FFMA_PER_CLK = 128
+
+
+def row_bytes(cfg) -> int:
+    return R * (1 if cfg["int8"] else 2)
 
 
 def hbm_bytes(cfg) -> float:
     """Algorithmic HBM bytes of one walk: W2 (+ scales) once, every base logit once, the
     K embedding rows per request, the tokens, and draft_logits when written."""
     V, K, bs = cfg["V"], cfg["K"], cfg["bs"]
-    w2 = V * R * (1 if cfg["int8"] else 2) + (4 * V if cfg["int8"] else 0)
+    w2 = V * row_bytes(cfg) + (4 * V if cfg["int8"] else 0)
     if cfg["top_k"]:
         w2 = bs * K * cfg["top_k"] * R * 2
     base = bs * K * V * 2
     emb = bs * K * R * 2
     out = bs * K * 4 + (bs * K * V * 2 if cfg["logits"] else 0)
     return float(w2 + base + emb + out)
+
+
+def uses_tensor_cores(cfg) -> bool:
+    return cfg["top_k"] == 0 and cfg["bs"] >= 2
+
+
+def floors(cfg, peaks, sms: int, resident_rows: int, l2_gbs: float):
+    """Lower bounds (µs) of one walk, per resource. Memory: HBM (W2 once, base logits,
+    outputs), shared memory (the resident W2 rows read at every position), L2 (the
+    streamed W2 rows at positions 1..K-1). Contraction: 2 V 256 bs K flops on the
+    tensor cores (bs >= 2), or the dp4a / fp32 FMA instructions of the CUDA-core
+    contraction (bs = 1). The roofline is the slowest of them."""
+    V, K, bs = cfg["V"], cfg["K"], cfg["bs"]
+    clk = peaks["sm_mhz"] * 1e6
+    out = {"hbm_us": hbm_bytes(cfg) / (peaks["hbm_gbs"] * 1e9) * 1e6}
+    if cfg["top_k"]:
+        return out
+    rb = row_bytes(cfg)
+    res_b = resident_rows * rb
+    out["smem_us"] = K * res_b / (SMEM_B_PER_CLK * sms * clk) * 1e6
+    out["l2_us"] = (K - 1) * (V - resident_rows) * rb / (l2_gbs * 1e9) * 1e6
+    if uses_tensor_cores(cfg):
+        out["tensor_us"] = 2.0 * V * R * bs * K / (peaks["bf16_tflops"] * 1e12) * 1e6
+    else:
+        ops, lanes = alu_ops(cfg)  # int8: 3 byte limbs of the embedding, one dp4a per 4 codes each
+        out["alu_us"] = ops / (lanes * sms * clk) * 1e6
+    return out
+
+
+def alu_ops(cfg) -> tuple[float, int]:
+    """(instructions per walk, lanes per clock per SM) of the CUDA-core contraction."""
+    n = float(cfg["V"]) * R * cfg["bs"] * cfg["K"]
+    return (3.0 * n / 4, DP4A_PER_CLK) if cfg["int8"] else (n, FFMA_PER_CLK)
+
+
+def roofline(cfg, peaks, fl, us, sms: int):
+    """The roofline object for the slowest floor: achieved = that resource's algorithmic
+    work per walk / measured walk time, against its peak."""
+    key = max(fl, key=fl.get)
+    if key == "tensor_us":
+        ach = 2.0 * cfg["V"] * R * cfg["bs"] * cfg["K"] / (us * 1e-6) / 1e12
+        r = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    elif key == "alu_us":
+        ops, lanes = alu_ops(cfg)
+        peak = lanes * sms * peaks["sm_mhz"] * 1e6 / 1e9
+        r = {"bound": "alu", "achieved": ops / (us * 1e-6) / 1e9, "peak": peak,
+             "unit": "G dp4a/s" if cfg["int8"] else "G FMA/s"}
+    elif key == "smem_us":
+        r = {"bound": "smem", "achieved": fl[key] / us, "peak": 1.0, "unit": "fraction"}
+    elif key == "l2_us":
+        r = {"bound": "l2", "achieved": fl[key] / us, "peak": 1.0, "unit": "fraction"}
+    else:
+        ach = hbm_bytes(cfg) / (us * 1e-6) / 1e9
+        r = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    return r
+
+
+def measure_l2_gbs(dev) -> float:
+    """Copy bandwidth of a 32 MB buffer that stays in L2 (read + write bytes)."""
+    a = torch.empty(32 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    b = torch.empty_like(a)
+    for _ in range(5):
+        b.copy_(a)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(50):
+        b.copy_(a)
+    e.record()
+    torch.cuda.synchronize()
+    return 2.0 * a.numel() * 50 / (s.elapsed_time(e) * 1e-3) / 1e9
 
 
 class ClockSampler:
@@ -213,55 +297,123 @@ def time_e2e(cfg, t, args, steps, dev):
     return ms, h2d, d2h
 
 
-def oracle_sample(cfg, rows: int, nthreads: int):
-    """Time the CPU oracle on `rows` request rows of the workload (all K positions)."""
-    from dspark_markov_draft_gb300 import synth
-    from oracle import oracle as O
-    O.build()
-    inp = synth.make(cfg["V"], rows, cfg["K"], seed=0, peak=cfg["peak"])
-    b = inp.bits
-    kw = {}
-    if cfg["int8"]:
-        st, q, sc = O.quantize_w2(b(inp.w2))
-        kw = dict(w2q=q, scales=sc)
-    else:
-        kw = dict(w2_bits=b(inp.w2))
-    t0 = time.perf_counter()
-    O.walk(b(inp.base), b(inp.w1), inp.prev.numpy(), cfg["K"],
-           seeds=inp.seeds.numpy().astype(np.uint64), mode=cfg["mode"], temperature=cfg["T"],
-           top_k=cfg["top_k"], nthreads=nthreads, **kw)
-    dt = time.perf_counter() - t0
-    return dt, rows * cfg["K"]
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class OracleRunner:
+    """The CPU oracle (fp64, OpenMP over rows and vocabulary) on `rows` request rows of
+    the workload, all K positions, inputs prepared once."""
+
+    def __init__(self, cfg, rows: int):
+        from dspark_markov_draft_gb300 import synth
+        from oracle import oracle as O
+        O.build()
+        self.O, self.cfg, self.rows = O, cfg, rows
+        inp = synth.make(cfg["V"], rows, cfg["K"], seed=0, peak=cfg["peak"])
+        b = inp.bits
+        if cfg["int8"]:
+            _, q, sc = O.quantize_w2(b(inp.w2))
+            self.kw = dict(w2q=q, scales=sc)
+        else:
+            self.kw = dict(w2_bits=b(inp.w2))
+        self.base, self.w1 = b(inp.base), b(inp.w1)
+        self.prev = inp.prev.numpy()
+        self.seeds = inp.seeds.numpy().astype(np.uint64)
+
+    def run(self, rows: int, nthreads: int) -> float:
+        """Seconds for a walk of the first `rows` rows."""
+        c = self.cfg
+        t0 = time.perf_counter()
+        r = self.O.walk(self.base[:rows], self.w1, self.prev[:rows], c["K"],
+                        seeds=self.seeds[:rows], mode=c["mode"], temperature=c["T"],
+                        top_k=c["top_k"], nthreads=nthreads, **self.kw)
+        dt = time.perf_counter() - t0
+        if r.status != 0:
+            raise RuntimeError(f"oracle walk status {r.status}")
+        return dt
+
+
+def cpu_baseline(cfg, target_s: float = 12.0):
+    """Oracle throughput on a bounded sample of the workload: enough request rows (all
+    K positions) for about `target_s` seconds of CPU work, capped at the whole batch."""
+    cores = host_cores()
+    runner = OracleRunner(cfg, cfg["bs"])
+    t1 = runner.run(1, cores)
+    rows = int(min(cfg["bs"], max(1, target_s / max(t1, 1e-6))))
+    reps = 1 if rows < cfg["bs"] else int(min(5, max(1, target_s / max(rows * t1, 1e-6))))
+    dt = sum(runner.run(rows, cores) for _ in range(reps))
+    toks = reps * rows * cfg["K"]
+    return {"value": toks / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{reps} x {rows} of {cfg['bs']} request rows, all {cfg['K']} positions, "
+                      f"{dt:.1f} s of oracle time"}
 
 
 def reference_arm(a, rank, world):
+    """The oracle timed on the host cores as the reference arm: each step walks a bounded
+    sample of the main workload's request rows (all K positions)."""
     if rank != 0:
         return 0
-    cores = os.cpu_count() or 1
+    cores = host_cores()
     cfg = MAIN
-    rows = 1
+    runner = OracleRunner(cfg, cfg["bs"])
+    t1 = runner.run(1, cores)
+    rows = int(min(cfg["bs"], max(1, 2.0 / max(t1, 1e-6))))  # about 2 s per step
     for _ in range(a.warmup):
-        oracle_sample(cfg, rows, cores)
-    ts = []
-    toks = 0
-    for _ in range(a.steps):
-        dt, n = oracle_sample(cfg, rows, cores)
-        ts.append(dt)
-        toks += n
-    value = toks / sum(ts)
+        runner.run(rows, cores)
+    ts = [runner.run(rows, cores) for _ in range(a.steps)]
+    value = a.steps * rows * cfg["K"] / sum(ts)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1000 * statistics.mean(ts),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": cfg["name"], "V": cfg["V"], "K": cfg["K"], "bs": cfg["bs"],
-                   "w2": "int8", "mode": "greedy", "sample_rows": rows},
+                   "w2": "int8", "mode": "greedy", "sample_rows_per_step": rows},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{rows} of {cfg['bs']} request rows, all {cfg['K']} positions, per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+KERNEL_SOURCES = {
+    "walk_tc_kernel": ["walk_tc.cu", "common.cuh", "walk_params.cuh"],
+    "walk_cc_kernel": ["walk_cc.cu", "common.cuh", "walk_params.cuh"],
+    "topk_walk_kernel": ["topk.cu", "common.cuh", "walk_params.cuh"],
+}
+
+
+def kernel_name(cfg) -> str:
+    if cfg["top_k"]:
+        return "topk_walk_kernel"
+    return "walk_tc_kernel" if uses_tensor_cores(cfg) else "walk_cc_kernel"
+
+
+def sources_digest(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "dspark_markov_draft_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(cfg):
+    """DRAM bytes per launch from the committed ncu capture of this workload's kernel,
+    or None when there is none or the kernel's sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(cfg["name"])
+    k = kernel_name(cfg)
+    if not rec or rec.get("kernel") != k or rec.get("sources_sha256_16") != sources_digest(k):
+        return None
+    return float(rec["dram_bytes_per_launch"])
 
 
 def main():
@@ -294,9 +446,19 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     peaks = load_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 129 MB L2
     by_name = {c["name"]: c for c in [MAIN] + VARIANTS + EXTRA}
     cfg = by_name[a.workload]
+
+    def floors_of(c):
+        res = 0
+        if not c["top_k"]:
+            _, res = capi.query_capacity(local, c["V"], c["int8"], c["bs"])
+        fl = floors(c, peaks, sms, res, l2_gbs)
+        return fl, res
+
+    l2_gbs = measure_l2_gbs(dev)
     # untimed warm-up of the whole path, then the timed walks
     if dist:
         dist.barrier()
@@ -317,47 +479,60 @@ def main():
     value = world * toks / (ms * 1e-3)
 
     e2e_ms, h2d, d2h = (float("nan"), 0, 0) if a.no_e2e else time_e2e(cfg, t, args, max(3, a.steps // 2), dev)
-    hb = hbm_bytes(cfg)
-    achieved = hb / (ms * 1e-3) / 1e9
-    roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "traffic": None,
-            "peak_source": peaks["src"], "algorithmic_bytes_per_launch": hb}
+    fl, res_rows = floors_of(cfg)
+    us = 1000 * ms
+    roof = roofline(cfg, peaks, fl, us, sms)
+    roof["traffic"] = recorded_traffic(cfg)
+    roof["peak_source"] = f"{peaks['src']} (MEASURED_PEAKS.json)" if peaks["src"] == "measured" else "fallback"
+    roof["kernel"] = kernel_name(cfg)
+    floor_us = max(fl.values())
+    floor_rec = {k: round(v, 3) for k, v in fl.items()}
+    floor_rec.update({"floor_us": round(floor_us, 3), "frac_of_floor": floor_us / us,
+                      "resident_w2_rows": res_rows, "l2_gbs_live": round(l2_gbs, 1),
+                      "hbm_bytes": hbm_bytes(cfg)})
 
     variants = []
     if not a.no_variants:
         for vc in VARIANTS:
-            vt, _, _ = time_walks(vc, max(5, a.steps // 2), 2, dev, flush)
-            vms = statistics.median(vt)
-            vhb = hbm_bytes(vc)
-            variants.append({"workload": vc["name"], "us_per_walk": 1000 * vms,
-                             "draft_tokens_per_s": vc["bs"] * vc["K"] / (vms * 1e-3),
-                             "hbm_gbs": vhb / (vms * 1e-3) / 1e9,
-                             "hbm_frac": vhb / (vms * 1e-3) / 1e9 / peaks["hbm_gbs"]})
+            vt, _, _ = time_walks(vc, max(5, a.steps // 2), 3, dev, flush)
+            vus = 1000 * statistics.mean(vt)
+            vfl, vres = floors_of(vc)
+            vfloor = max(vfl.values())
+            vr = roofline(vc, peaks, vfl, vus, sms)
+            variants.append({"workload": vc["name"], "us_per_walk": vus,
+                             "draft_tokens_per_s": vc["bs"] * vc["K"] / (vus * 1e-6),
+                             "kernel": kernel_name(vc), "floor_us": vfloor,
+                             "frac_of_floor": vfloor / vus,
+                             "bound": vr["bound"], "frac": vr["frac"],
+                             "floors_us": {k: round(v, 3) for k, v in vfl.items()}})
 
     cpu = None
     if rank == 0 and not a.no_cpu_baseline:
-        cores = os.cpu_count() or 1
-        dt, n = oracle_sample(cfg, 1, cores)
-        cpu = {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"1 of {cfg['bs']} request rows, all {cfg['K']} positions ({dt:.1f} s)"}
+        cpu = cpu_baseline(cfg)
 
     if rank == 0:
+        tc = uses_tensor_cores(cfg)
+        dtype = (("int8 W2 codes as fp16 x fp16 embedding, fp32 accumulate (tcgen05)" if cfg["int8"]
+                  else "bf16 x bf16, fp32 accumulate (tcgen05)") if tc else
+                 ("int8 x 24-bit integer embedding (dp4a), fp32 epilogue" if cfg["int8"]
+                  else "bf16 x bf16, fp32 FMA"))
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int8 x int (dp4a) -> fp32", "data": "synthetic",
+            "vs_baseline": None, "dtype": dtype, "data": "synthetic",
             "config": {"workload": cfg["name"], "V": cfg["V"], "rank": R, "K": cfg["K"],
                        "bs": cfg["bs"], "w2": "int8" if cfg["int8"] else "bf16",
                        "mode": "greedy" if cfg["mode"] == 0 else f"probabilistic T={cfg['T']}",
                        "top_k": cfg["top_k"], "draft_logits": cfg["logits"],
                        "l2": "flushed before every walk (256 MB write)",
                        "parallelism": f"replicas x{world}"},
-            "us_per_walk": 1000 * ms,
+            "us_per_walk": us,
             "roofline": roof,
+            "floors": floor_rec,
             "cpu_baseline": cpu,
             "e2e": {"value": world * toks / (e2e_ms * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": a.steps,
+            "gpu_launches": a.steps * (2 if cfg["top_k"] else 1),
             "clocks": clk.summary(),
             "wall_s_timed": wall,
             "variants": variants,

@@ -238,17 +238,29 @@ size_t dspark_walk_workspace_size(int64_t V, int32_t bs, int32_t K, int32_t top_
 
 int32_t dspark_query_capacity(int32_t device, int64_t V, int32_t w2_is_int8, int32_t bs,
                               int32_t* grid_ctas, int64_t* resident_rows) {
-  if (V <= 0 || bs < 1 || bs > DSPARK_MAX_BS) return DSPARK_ERR_INVALID_ARG;
+  if (V <= 0 || V > DSPARK_MAX_V || bs < 1 || bs > DSPARK_MAX_BS) return DSPARK_ERR_INVALID_ARG;
   DeviceCaps caps;
   int32_t st = get_caps(device, &caps);
   if (st != DSPARK_OK) return st;
-  const Plan pl = plan_dense(caps, V, w2_is_int8 != 0, bs, -1);
-  if (grid_ctas) *grid_ctas = pl.grid;
+  // The plan dspark_walk takes by default for this batch size.
+  const bool tc = bs >= kTcMinBs;
+  int grid, per_cta;
+  if (tc) {
+    const TcPlan pl = plan_tc(caps, V, w2_is_int8 != 0, bs, -1);
+    grid = pl.grid;
+    per_cta = pl.resident_rows;
+  } else {
+    const Plan pl = plan_dense(caps, V, w2_is_int8 != 0, bs, -1);
+    grid = pl.grid;
+    per_cta = pl.resident_rows;
+  }
+  if (grid_ctas) *grid_ctas = grid;
   if (resident_rows) {
     int64_t tot = 0;
-    for (int c = 0; c < pl.grid; ++c) {
-      const int64_t n = (static_cast<int64_t>(c + 1) * V / pl.grid) - (static_cast<int64_t>(c) * V / pl.grid);
-      tot += n < (pl.resident_rows) ? (n & ~31LL) : pl.resident_rows;
+    for (int c = 0; c < grid; ++c) {
+      const int64_t n = slice_start(c + 1, grid, V) - slice_start(c, grid, V);
+      const int64_t cap = tc ? n : (n & ~31LL);
+      tot += cap < per_cta ? cap : per_cta;
     }
     *resident_rows = tot;
   }

@@ -158,9 +158,12 @@ int32_t dspark_walk_from_host(const dspark_walk_args* args, const uint16_t* base
 size_t dspark_walk_workspace_size(int64_t V, int32_t bs, int32_t K, int32_t top_k);
 
 /*
- * Launch plan the walk would use on `device`: cooperative grid size (CTAs) and the
- * number of W2 rows kept resident in shared memory over the whole grid. Queries the
- * device once and caches it (the only host-synchronous work of the library).
+ * Launch plan dspark_walk takes by default on `device` for this batch size (CUDA-core
+ * contraction at bs = 1, tensor cores from bs = 2): cooperative grid size (CTAs) and
+ * the number of W2 rows kept resident in shared memory over the whole grid. Queries
+ * the device once and caches it (the only host-synchronous work of the library).
+ * Returns DSPARK_ERR_INVALID_ARG for V outside 1..DSPARK_MAX_V or bs outside
+ * 1..DSPARK_MAX_BS.
  */
 int32_t dspark_query_capacity(int32_t device, int64_t V, int32_t w2_is_int8, int32_t bs,
                               int32_t* grid_ctas, int64_t* resident_rows);
