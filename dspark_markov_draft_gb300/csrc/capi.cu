@@ -105,7 +105,7 @@ struct TcPlan {
 
 // Tensor-core walk: B operand (N x 512 bytes), the slice's scales, bookkeeping, and as
 // many resident W2 rows as the remaining shared memory holds.
-TcPlan plan_tc(const DeviceCaps& caps, int64_t V, bool int8, int bs, int cap_rows) {
+TcPlan plan_tc(const DeviceCaps& caps, int64_t V, bool int8, bool prob, int bs, int cap_rows) {
   TcPlan pl{};
   pl.grid = caps.sms;
   const int N = bs <= 16 ? 16 : bs <= 32 ? 32 : 64;
@@ -113,7 +113,8 @@ TcPlan plan_tc(const DeviceCaps& caps, int64_t V, bool int8, int bs, int cap_row
   const int64_t per_cta = (V + pl.grid - 1) / pl.grid + 32;
   pl.slice_cap = static_cast<int>((per_cta + 31) & ~31LL);
   const int row_bytes = int8 ? kRank : 2 * kRank;
-  const size_t fixed = 1024 + static_cast<size_t>(N) * 512 + (int8 ? static_cast<size_t>(pl.slice_cap) * 4 : 0) +
+  const size_t fixed = 1024 + static_cast<size_t>(N) * 512 + walk_tc_stage_bytes(N, prob) +
+                       (int8 ? static_cast<size_t>(pl.slice_cap) * 4 : 0) +
                        walk_tc_misc_smem();
   int64_t rows = caps.smem_optin > static_cast<int>(fixed)
                      ? (static_cast<int64_t>(caps.smem_optin) - static_cast<int64_t>(fixed)) / row_bytes
@@ -124,6 +125,12 @@ TcPlan plan_tc(const DeviceCaps& caps, int64_t V, bool int8, int bs, int cap_row
   pl.resident_rows = static_cast<int>(rows);
   pl.smem = fixed + static_cast<size_t>(rows) * row_bytes;
   return pl;
+}
+
+// The tensor-core walk handles vocabulary slices of up to kTcMaxTiles tiles.
+bool tc_fits(const DeviceCaps& caps, int64_t V) {
+  const int64_t per_cta = (V + caps.sms - 1) / caps.sms + 32;
+  return (per_cta + 127) / 128 <= kTcMaxTiles;
 }
 
 int32_t check_common(const dspark_walk_args* a) {
@@ -243,10 +250,10 @@ int32_t dspark_query_capacity(int32_t device, int64_t V, int32_t w2_is_int8, int
   int32_t st = get_caps(device, &caps);
   if (st != DSPARK_OK) return st;
   // The plan dspark_walk takes by default for this batch size.
-  const bool tc = bs >= kTcMinBs;
+  const bool tc = bs >= kTcMinBs && tc_fits(caps, V);
   int grid, per_cta;
   if (tc) {
-    const TcPlan pl = plan_tc(caps, V, w2_is_int8 != 0, bs, -1);
+    const TcPlan pl = plan_tc(caps, V, w2_is_int8 != 0, false, bs, -1);
     grid = pl.grid;
     per_cta = pl.resident_rows;
   } else {
@@ -309,9 +316,10 @@ int32_t dspark_walk(const dspark_walk_args* a, dspark_stream_t stream) {
   const bool lg = a->draft_logits != nullptr;
   const bool prob = a->mode == DSPARK_PROBABILISTIC;
   const bool use_tc = !(a->flags & DSPARK_FLAG_FORCE_CUDA_CORES) &&
-                      (a->bs >= kTcMinBs || (a->flags & DSPARK_FLAG_FORCE_TENSOR_CORES));
+                      (a->bs >= kTcMinBs || (a->flags & DSPARK_FLAG_FORCE_TENSOR_CORES)) &&
+                      tc_fits(caps, a->V);
   if (use_tc) {
-    const TcPlan pl = plan_tc(caps, a->V, int8, a->bs, a->resident_rows_cap);
+    const TcPlan pl = plan_tc(caps, a->V, int8, prob, a->bs, a->resident_rows_cap);
     WalkParams p = make_params(a, pl.grid, pl.resident_rows, pl.slice_cap);
     return launch_coop(walk_tc_kernel_ptr(int8, prob, lg, pl.nq), pl.grid, pl.smem, p,
                        reinterpret_cast<cudaStream_t>(stream));

@@ -63,14 +63,21 @@ __host__ __device__ inline int64_t slice_start(int c, int G, int64_t V) {
   return (static_cast<int64_t>(c) * V / G) & ~static_cast<int64_t>(31);
 }
 
+// Tensor-core walk, greedy epilogue: base logits staged per epilogue warp (8), two
+// tiles of 32 rows x N/2 request rows, bf16. The epilogue keeps tile numbers in 8-bit
+// fields, so a CTA's vocabulary slice holds at most kTcMaxTiles tiles of 128 rows.
+constexpr int kTcMaxTiles = 255;
+__host__ __device__ constexpr int walk_tc_stage_bytes(int N, bool prob) {
+  return prob ? 0 : 8 * 2 * (N / 2) * 32 * 2;
+}
+
 // Tensor-core walk: shared memory besides the B operand and the resident rows.
 __host__ __device__ inline size_t walk_tc_misc_smem() {
-  return 64 * 4      // e-shift per row
-         + 64 * 4    // prev tokens
-         + 64 * 8    // per-row argmax words
-         + 4 * 64 * 8  // per-quadrant argmax words
-         + 64 * 8      // per-row 2^-s factors
-         + 12 * 8 + 16;  // mbarriers, TMEM base, flag
+  return 64 * 4          // prev tokens
+         + 64 * 8        // per-row argmax words
+         + 4 * 64 * 8    // per-quadrant argmax words
+         + 2 * 8         // 2^-s as two factors
+         + 12 * 8 + 16;  // mbarriers, TMEM base, flag, batch |e| maximum
 }
 
 }  // namespace dspark

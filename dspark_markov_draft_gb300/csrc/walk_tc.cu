@@ -28,6 +28,7 @@
 //     two A and two D buffers, so the three overlap across tiles.
 #include <cstdint>
 #include <cuda_fp16.h>
+#include <type_traits>
 
 #include "common.cuh"
 #include "walk_params.cuh"
@@ -139,6 +140,42 @@ __device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, float (&o)[8]) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) o[j] = __uint_as_float(r[j]);
 }
+// Two loads of CH consecutive columns (the two K-half accumulators), one wait.
+template <int CH>
+__device__ __forceinline__ void tmem_ld2(uint32_t a0, uint32_t a1, float (&d0)[CH], float (&d1)[CH]);
+template <>
+__device__ __forceinline__ void tmem_ld2<8>(uint32_t a0, uint32_t a1, float (&d0)[8], float (&d1)[8]) {
+  uint32_t r[16];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7]) : "r"(a0) : "memory");
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                 "=r"(r[14]), "=r"(r[15]) : "r"(a1) : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 8; ++j) { d0[j] = __uint_as_float(r[j]); d1[j] = __uint_as_float(r[8 + j]); }
+}
+template <>
+__device__ __forceinline__ void tmem_ld2<16>(uint32_t a0, uint32_t a1, float (&d0)[16], float (&d1)[16]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]) : "r"(a0) : "memory");
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+        "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31]) : "r"(a1) : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 16; ++j) { d0[j] = __uint_as_float(r[j]); d1[j] = __uint_as_float(r[16 + j]); }
+}
+
 // 4 x 4 transpose inside each group of 4 lanes: on entry lane j holds row j
 // (x[c] = a[j][c]); on return it holds column j (x[r] = a[r][j]).
 __device__ __forceinline__ void transpose4(float (&x)[4], int lane) {
@@ -213,20 +250,21 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   unsigned char* b_s = smem;                                      // N x 512 bytes
-  unsigned char* w2s = b_s + N * 512;                             // resident rows
+  uint16_t* base_stage = reinterpret_cast<uint16_t*>(b_s + N * 512);  // greedy: [8 warps][2][N/2][32]
+  unsigned char* w2s = b_s + N * 512 + walk_tc_stage_bytes(N, PROB);  // resident rows
   float* scale_s = reinterpret_cast<float*>(w2s + static_cast<size_t>(p.resident_rows) * kRowBytes);
-  int* sh_shift = reinterpret_cast<int*>(scale_s + (INT8 ? p.slice_cap : 0));
-  int* prev_s = sh_shift + 64;
+  int* prev_s = reinterpret_cast<int*>(scale_s + (INT8 ? p.slice_cap : 0));   // [64]
   uint64_t* best_s = reinterpret_cast<uint64_t*>(prev_s + 64);
   uint64_t* red_s = best_s + 64;                                  // [4][64]
-  float2* inv_s = reinterpret_cast<float2*>(red_s + 4 * 64);       // [64] 2^-s as two factors
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(inv_s + 64);       // [12]
+  float2* inv_s = reinterpret_cast<float2*>(red_s + 4 * 64);       // 2^-s as two factors
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(inv_s + 2);        // [12]
   uint64_t* a_full = mbar;        // [buf * 2 + half], 4 arrivals
   uint64_t* a_empty = mbar + 4;   // [buf * 2 + half], 1 commit
   uint64_t* d_full = mbar + 8;    // [buf], 2 commits
   uint64_t* d_empty = mbar + 10;  // [buf], 8 arrivals
   uint32_t* tbase_s = reinterpret_cast<uint32_t*>(mbar + 12);
   int* flag = reinterpret_cast<int*>(tbase_s + 1);
+  int* sh_amax = flag + 1;        // largest finite |e| of the batch, as fp32 bits
 
   const int G = gridDim.x, cta = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -257,6 +295,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
     for (int b = 0; b < 12; ++b)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&mbar[b])), "r"(counts[b]));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    *sh_amax = 0;
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -285,30 +324,43 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
       wrow[r] = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(p.w1 + static_cast<size_t>(tok) * kRank) + lane)
                          : make_uint4(0, 0, 0, 0);
     }
+    // int8 W2: one power-of-two scale 2^s for the whole batch, with the largest finite
+    // |e| of all rows in [2^14, 2^15) after scaling.
+    int shift = 0;
+    if constexpr (INT8) {
+      float amax = 0.f;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int b = warp + kWalkWarps * r;
-      if (b >= p.bs) break;
-      uint4 w = wrow[r];
-      int shift = 0;
-      if constexpr (INT8) {
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-        float amax = 0.f;
+      for (int r = 0; r < 4; ++r) {
+        const int b = warp + kWalkWarps * r;
+        if (b >= p.bs) break;
+        const uint32_t ww[4] = {wrow[r].x, wrow[r].y, wrow[r].z, wrow[r].w};
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const float lo = bf16_lo(ww[t]), hi = bf16_hi(ww[t]);
           if (isfinite(lo)) amax = fmaxf(amax, fabsf(lo));
           if (isfinite(hi)) amax = fmaxf(amax, fabsf(hi));
         }
+      }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-        if (amax > 0.f) {
-          int ex;
-          frexpf(amax, &ex);  // amax = f 2^ex, f in [0.5, 1)
-          shift = 15 - ex;    // amax 2^shift in [2^14, 2^15)
-        }
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+      if (lane == 0 && amax > 0.f) atomicMax(sh_amax, __float_as_int(amax));
+      __syncthreads();
+      const float am = __int_as_float(*reinterpret_cast<volatile int*>(sh_amax));
+      if (am > 0.f) {
+        int ex;
+        frexpf(am, &ex);  // am = f 2^ex, f in [0.5, 1)
+        shift = 15 - ex;  // am 2^shift in [2^14, 2^15)
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int b = warp + kWalkWarps * r;
+      if (b >= p.bs) break;
+      uint4 w = wrow[r];
+      if constexpr (INT8) {
         const float s_lo = __int_as_float((shift / 2 + 127) << 23);
         const float s_hi = __int_as_float((shift - shift / 2 + 127) << 23);
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
         uint32_t h[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
@@ -319,16 +371,15 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
         }
         w = make_uint4(h[0], h[1], h[2], h[3]);
       }
-      if (lane == 0) {
-        sh_shift[b] = shift;
-        inv_s[b] = make_float2(__int_as_float(((-shift) / 2 + 127) << 23),
-                               __int_as_float(((-shift) - (-shift) / 2 + 127) << 23));
-      }
       const int kb = lane >> 3, ch = lane & 7;
       *reinterpret_cast<uint4*>(b_s + kb * N * 128 + b * 128 + ((ch ^ (b & 7)) * 16)) = w;
     }
+    if (tid == 0)
+      *inv_s = make_float2(__int_as_float(((-shift) / 2 + 127) << 23),
+                           __int_as_float(((-shift) - (-shift) / 2 + 127) << 23));
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();  // B written and visible to the tensor core; shifts published
+    __syncthreads();  // B written and visible to the tensor core; 2^-s published
+    if (tid == 0) *sh_amax = 0;  // every thread read it before the barrier
 
     bool failed = false;
     if (producer) {
@@ -435,8 +486,117 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
         if (__shfl_sync(kFull, failed ? 1 : 0, 0)) { failed = true; break; }
       }
       asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if constexpr (!PROB) {
+      // ------------------------------------------------------- epilogue, greedy
+      // Thread = tensor-memory lane = vocabulary row 32 q + lane of the tile; the
+      // warp's NC columns (request rows) are warp-uniform. Each thread keeps, per
+      // column, the running maximum of its rows over the tiles (max.NaN: a NaN sticks)
+      // and the tile where it was first reached: the tile is rewritten when the maximum
+      // changes (an unordered compare, so the first NaN counts) unless it already is
+      // NaN. Equal values (also -0 and +0) never rewrite it, so the first maximum stays.
+      // Tiles are 8-bit fields, four columns per register. The lanes and quadrants are
+      // combined once per position. The base logits of the warp's rows and columns are
+      // staged in shared memory one tile ahead with cp.async.
+      constexpr int CHG = NC < 16 ? NC : 16;
+      const int cb = half * NC;                                 // first column of the warp
+      const int ncol = max(0, min(NC, p.bs - cb));              // live columns (uniform)
+      const int ew = warp - 8;
+      uint16_t* stage_s = base_stage + static_cast<size_t>(ew) * 2 * NC * 32;  // [2][NC][32]
+      // request rows whose previous token was out of range are skipped
+      const uint32_t live = __ballot_sync(kFull, lane < ncol && prev_s[cb + min(lane, NC - 1)] >= 0);
+      const size_t bstride = static_cast<size_t>(p.K) * static_cast<size_t>(p.V);
+      const uint16_t* brow = p.base + static_cast<size_t>(i) * p.V + v0;  // + b K V + row
+      const bool vec_ok = (p.V & 7) == 0 && (reinterpret_cast<uintptr_t>(p.base) & 15u) == 0;
+      // Copy the warp's 32 rows x ncol columns of tile t into stage buffer sb: 16-byte
+      // pieces of 8 rows (slices start on multiples of 32 rows and, with V a multiple
+      // of 8, end on multiples of 8, so a piece is entirely inside or outside).
+      auto stage = [&](int t, int sb) {
+        const int r0 = t * kTile + 32 * q;
+        for (int e = lane; e < ncol * 4; e += 32) {
+          const int j = e >> 2, c8 = e & 3;
+          if (!((live >> j) & 1u)) continue;
+          const int rr = r0 + 8 * c8;
+          uint16_t* dst = stage_s + (sb * NC + j) * 32 + 8 * c8;
+          const uint16_t* src = brow + static_cast<size_t>(cb + j) * bstride + rr;
+          if (vec_ok) {
+            if (rr < n) cp_async16(dst, src);
+          } else {
+#pragma unroll
+            for (int e8 = 0; e8 < 8; ++e8) dst[e8] = rr + e8 < n ? src[e8] : 0;
+          }
+        }
+        cp_async_commit();
+      };
+      float bv[NC];
+      uint32_t bt[(NC + 3) / 4];
+#pragma unroll
+      for (int j = 0; j < NC; ++j) bv[j] = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < (NC + 3) / 4; ++w) bt[w] = 0u;
+      if (T > 0) stage(0, 0);
+      const float2 inv = inv_s[0];
+      // One tile; FULL: every row of the tile lies in the slice.
+      auto tile = [&](auto full_tag, int t, int buf) {
+        constexpr bool FULL = decltype(full_tag)::value;
+        const int rr = t * kTile + 32 * q + lane;
+        const bool valid = rr < n;
+        [[maybe_unused]] float c = 1.f;
+        if constexpr (INT8) c = __fmul_rn(__fmul_rn(valid ? scale_s[rr] : 0.f, inv.x), inv.y);
+        const uint32_t trep = static_cast<uint32_t>(t) * 0x01010101u;
+        const uint16_t* bsm = stage_s + (t & 1) * NC * 32 + lane;
+#pragma unroll
+        for (int cc = 0; cc < NC / CHG; ++cc) {
+          if (cc * CHG >= ncol) break;
+          float d0[CHG], d1[CHG];
+          const uint32_t dcol = kColD + 2 * buf * N + cb + cc * CHG;
+          tmem_ld2<CHG>(tmem + lane_off + dcol, tmem + lane_off + dcol + N, d0, d1);
+#pragma unroll
+          for (int k = 0; k < CHG; ++k) {
+            const int j = cc * CHG + k;
+            if (!((live >> j) & 1u)) continue;  // uniform; also every j >= ncol
+            const float bvl = __uint_as_float(static_cast<uint32_t>(bsm[j * 32]) << 16);
+            float l;
+            if constexpr (INT8) l = __fmaf_rn(__fadd_rn(d0[k], d1[k]), c, bvl);
+            else l = __fadd_rn(__fadd_rn(d0[k], d1[k]), bvl);
+            if constexpr (!FULL) l = valid ? l : -INFINITY;
+            if constexpr (LOGITS)
+              if (valid) p.logits[static_cast<size_t>(cb + j) * bstride + static_cast<size_t>(i) * p.V + v0 + rr] = f32_to_bf16_bits(l);
+            float nv;
+            asm("max.NaN.f32 %0, %1, %2;" : "=f"(nv) : "f"(bv[j]), "f"(l));
+            asm("{ .reg .pred r, u; setp.num.f32 r, %1, %1; setp.neu.and.f32 u, %2, %1, r; "
+                "@u lop3.b32 %0, %0, %3, %4, 0xB8; }"
+                : "+r"(bt[j >> 2]) : "f"(bv[j]), "f"(nv), "r"(0xFFu << (8 * (j & 3))), "r"(trep));
+            bv[j] = nv;
+          }
+        }
+      };
+      for (int t = 0; t < T; ++t) {
+        const int g = g_base + t, buf = g & 1, u = g >> 1;
+        if (t + 1 < T) stage(t + 1, (t + 1) & 1);
+        if (!mbar_wait(&d_full[buf], u & 1, p.sync.timeout_ns)) failed = true;
+        if (__shfl_sync(kFull, failed ? 1 : 0, 0)) { failed = true; break; }
+        tc_fence_after();
+        cp_async_wait_pending(t + 1 < T ? 1 : 0);
+        __syncwarp();
+        if ((t + 1) * kTile <= n) tile(std::true_type{}, t, buf);
+        else tile(std::false_type{}, t, buf);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&d_empty[buf])) : "memory");
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      // per column: (orderable key, first index) maximum over the warp's 32 rows
+      const uint32_t vlane = static_cast<uint32_t>(v0) + 32u * q + lane;
+#pragma unroll
+      for (int j = 0; j < NC; ++j) {
+        if (j >= ncol) break;
+        const uint32_t tj = (bt[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+        uint64_t x = pack_best(order_key(bv[j]), vlane + tj * kTile);
+        x = warp_max64(x);
+        if (lane == 0) red_s[q * 64 + cb + j] = x;
+      }
     } else {
-      // ---------------------------------------------------------------- epilogue
+      // ---------------------------------------------------- epilogue, probabilistic
       // Column c of this thread's group j: b = half * NC + 4 j + (lane & 3).
       uint32_t live_mask = 0;
       uint64_t best[NG];
@@ -502,7 +662,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
             const size_t o = (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v0 + rr0;
             const float bv[4] = {bf16_lo(bcur[j].x), bf16_hi(bcur[j].x), bf16_lo(bcur[j].y), bf16_hi(bcur[j].y)};
             float l[4];
-            const float2 inv = INT8 ? inv_s[b] : make_float2(1.f, 1.f);
+            const float2 inv = INT8 ? inv_s[0] : make_float2(1.f, 1.f);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               float bias = x[k];
