@@ -196,15 +196,15 @@ WalkParams make_params(const dspark_walk_args* a, int grid, int resident_rows, i
   return p;
 }
 
-int32_t launch_coop(const void* fn, int grid, size_t smem, WalkParams& p, cudaStream_t stream) {
+int32_t launch_coop(const void* fn, int grid, int threads, size_t smem, WalkParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kWalkThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
   if (per_sm < 1) return DSPARK_ERR_COOP_TOO_LARGE;
   void* args[] = {&p};
-  e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kWalkThreads), args, smem, stream);
+  e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(threads), args, smem, stream);
   if (e == cudaErrorCooperativeLaunchTooLarge) {
     cudaGetLastError();
     return DSPARK_ERR_COOP_TOO_LARGE;
@@ -302,7 +302,7 @@ int32_t dspark_walk_topk(const dspark_walk_args* a, dspark_stream_t stream) {
   const size_t smem = static_cast<size_t>(a->bs) * kRank * 4 + 64 * 4 + 64 * 8 + kWalkWarps * 8 + 64 + 256;
   const bool prob = a->mode == DSPARK_PROBABILISTIC, lg = a->draft_logits != nullptr;
   const void* fn = topk_walk_kernel_ptr(prob, lg);
-  return launch_coop(fn, caps.sms, smem, p, s);
+  return launch_coop(fn, caps.sms, kWalkThreads, smem, p, s);
 }
 
 int32_t dspark_walk(const dspark_walk_args* a, dspark_stream_t stream) {
@@ -321,13 +321,13 @@ int32_t dspark_walk(const dspark_walk_args* a, dspark_stream_t stream) {
   if (use_tc) {
     const TcPlan pl = plan_tc(caps, a->V, int8, prob, a->bs, a->resident_rows_cap);
     WalkParams p = make_params(a, pl.grid, pl.resident_rows, pl.slice_cap);
-    return launch_coop(walk_tc_kernel_ptr(int8, prob, lg, pl.nq), pl.grid, pl.smem, p,
+    return launch_coop(walk_tc_kernel_ptr(int8, prob, lg, pl.nq), pl.grid, kWalkThreads, pl.smem, p,
                        reinterpret_cast<cudaStream_t>(stream));
   }
   const Plan pl = plan_dense(caps, a->V, int8, a->bs, a->resident_rows_cap);
   WalkParams p = make_params(a, pl.grid, pl.resident_rows, pl.slice_cap);
   const void* fn = walk_cc_kernel_ptr(int8, prob, lg);
-  return launch_coop(fn, pl.grid, pl.smem, p, reinterpret_cast<cudaStream_t>(stream));
+  return launch_coop(fn, pl.grid, kWalkThreads, pl.smem, p, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int32_t dspark_walk_from_host(const dspark_walk_args* a, const uint16_t* base_host,

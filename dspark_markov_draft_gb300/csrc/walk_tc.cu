@@ -176,6 +176,28 @@ __device__ __forceinline__ void tmem_ld2<16>(uint32_t a0, uint32_t a1, float (&d
   for (int j = 0; j < 16; ++j) { d0[j] = __uint_as_float(r[j]); d1[j] = __uint_as_float(r[16 + j]); }
 }
 
+// Column maxima of NC packed words per lane over the 32 lanes of a warp: plain
+// butterfly rounds while the offset is at least NC, then reduce-scatter rounds that
+// halve the columns a lane holds; lane l returns the maximum of column l % NC.
+template <int NC>
+__device__ __forceinline__ uint64_t column_max_scatter(uint64_t (&x)[NC], int lane) {
+#pragma unroll
+  for (int o = 16; o >= NC; o >>= 1)
+#pragma unroll
+    for (int k = 0; k < NC; ++k) x[k] = umax64(x[k], __shfl_xor_sync(kFull, x[k], o));
+#pragma unroll
+  for (int w = NC / 2; w >= 1; w >>= 1) {
+    const bool up = (lane & w) != 0;
+#pragma unroll
+    for (int k = 0; k < w; ++k) {
+      const uint64_t keep = up ? x[k + w] : x[k];
+      const uint64_t send = up ? x[k] : x[k + w];
+      x[k] = umax64(keep, __shfl_xor_sync(kFull, send, w));
+    }
+  }
+  return x[0];
+}
+
 // 4 x 4 transpose inside each group of 4 lanes: on entry lane j holds row j
 // (x[c] = a[j][c]); on return it holds column j (x[r] = a[r][j]).
 __device__ __forceinline__ void transpose4(float (&x)[4], int lane) {
@@ -227,7 +249,7 @@ __device__ __forceinline__ void cp_async_wait_pending(int pending) {
 // N = 16, 32 or 64 padded request rows. Warp roles inside the tile pipeline:
 //   warps 0-7   producers: quadrant w & 3 (tensor-memory lanes), K half w >> 2; each
 //               thread converts half of one W2 row of the tile into tensor memory.
-//               Lane 0 of warp 0 / warp 4 also issues the 8 MMAs of its K half, into
+//               Lane 0 of warp 0 / warp 5 also issues the 8 MMAs of its K half, into
 //               its own accumulator, as soon as the 4 producer warps of that half are
 //               done (two issuing threads double the MMA issue rate).
 //   warps 8-15  epilogue: quadrant w & 3, column half (w - 8) >> 2; each sums the two
@@ -279,6 +301,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
   const bool producer = warp < 8;
   const int q = warp & 3;                                          // tensor-memory lane quadrant
   const int half = (warp >> 2) & 1;                                // producers: K half; epilogue: column half
+  // MMA issuers: producer warp 0 (K half 0) and 5 (K half 1), on different SM sub-partitions
+  const bool issuer = producer && q == half;
 
   // ---- set-up: zero B, scales, previous tokens, barriers, tensor memory
   for (int t = tid; t < N * 512 / 16; t += blockDim.x) reinterpret_cast<uint4*>(b_s)[t] = make_uint4(0, 0, 0, 0);
@@ -456,12 +480,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
         __syncwarp();
         if (lane == 0)
           asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&a_full[buf * 2 + half])) : "memory");
-        if (t + 1 < T) {  // next tile's data in flight while this warp issues or waits
-          if (fill_now && t + 1 < n_res_tiles) cp_async_wait_pending(n_res_tiles - 2 - t);
-          load_pass(t + 1, 0, c0);
-          if constexpr (INT8) load_pass(t + 1, 1, c1);
-        }
-        if ((warp & 3) == 0 && lane == 0) {
+        if (issuer && lane == 0) {
           // MMA issue for this K half: A complete (all 4 quadrants), D buffer free.
           bool good = mbar_wait(&a_full[buf * 2 + half], u & 1, p.sync.timeout_ns);
           if (good && u >= 1) good = mbar_wait(&d_empty[buf], (u - 1) & 1, p.sync.timeout_ns);
@@ -482,6 +501,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
             mma_commit(&a_empty[buf * 2 + half]);
             last_issued = g;
           }
+        }
+        if (t + 1 < T) {  // next tile's data in flight while this warp waits (issuers: after the MMAs)
+          if (fill_now && t + 1 < n_res_tiles) cp_async_wait_pending(n_res_tiles - 2 - t);
+          load_pass(t + 1, 0, c0);
+          if constexpr (INT8) load_pass(t + 1, 1, c1);
         }
         if (__shfl_sync(kFull, failed ? 1 : 0, 0)) { failed = true; break; }
       }
@@ -587,14 +611,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
       asm volatile("cp.async.wait_all;" ::: "memory");
       // per column: (orderable key, first index) maximum over the warp's 32 rows
       const uint32_t vlane = static_cast<uint32_t>(v0) + 32u * q + lane;
+      uint64_t x[NC];
 #pragma unroll
       for (int j = 0; j < NC; ++j) {
-        if (j >= ncol) break;
         const uint32_t tj = (bt[j >> 2] >> (8 * (j & 3))) & 0xFFu;
-        uint64_t x = pack_best(order_key(bv[j]), vlane + tj * kTile);
-        x = warp_max64(x);
-        if (lane == 0) red_s[q * 64 + cb + j] = x;
+        x[j] = j < ncol ? pack_best(order_key(bv[j]), vlane + tj * kTile) : 0ull;
       }
+      const uint64_t xm = column_max_scatter<NC>(x, lane);
+      if (lane < ncol) red_s[q * 64 + cb + lane] = xm;
     } else {
       // ---------------------------------------------------- epilogue, probabilistic
       // Column c of this thread's group j: b = half * NC + 4 j + (lane & 3).
@@ -722,7 +746,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
     if (__syncthreads_or(failed)) {
       // Report, then let the issued MMAs finish (bounded) before tensor memory goes.
       if (tid == 0) give_up(p.sync);
-      if (producer && (warp & 3) == 0 && lane == 0 && last_issued >= 0)
+      if (issuer && lane == 0 && last_issued >= 0)
         mbar_wait(&a_empty[(last_issued & 1) * 2 + half], (last_issued >> 1) & 1, p.sync.timeout_ns);
       ok = false;
       break;
