@@ -80,25 +80,25 @@ __device__ __forceinline__ void mma_commit(uint64_t* mbar) {
                ::"r"(smem_u32(mbar)) : "memory");
 }
 
+// Longest time (ns) one try_wait may suspend the thread before it returns false; the
+// thread wakes as soon as the phase completes, so waiting costs no issue slots.
+constexpr uint32_t kSuspendHintNs = 1000000;
+
 __device__ __forceinline__ bool mbar_try(uint64_t* mbar, uint32_t parity) {
   uint32_t done;
   asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-      : "=r"(done) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done) : "r"(smem_u32(mbar)), "r"(parity), "r"(kSuspendHintNs) : "memory");
   return done != 0;
 }
 
 // Bounded wait for an mbarrier phase; false after timeout_ns of wall-clock time.
 __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, uint64_t timeout_ns) {
-  uint64_t t0 = 0;
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try(mbar, parity)) return true;
-    if ((it & 15u) == 15u) {
-      const uint64_t now = globaltimer_ns();
-      if (t0 == 0) t0 = now;
-      else if (now - t0 > timeout_ns) return false;
-    }
-  }
+  if (mbar_try(mbar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try(mbar, parity))
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
+  return true;
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
