@@ -5,6 +5,9 @@
 #include <cstring>
 #include <mutex>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "walk_params.cuh"
 
@@ -196,6 +199,41 @@ WalkParams make_params(const dspark_walk_args* a, int grid, int resident_rows, i
   return p;
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      f = nullptr;
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// Tensor map over the base logits [bs][K][V] for the greedy tensor-core epilogue: box of
+// 32 vocabulary rows x 1 position x N/2 requests. False (and the kernel stages with
+// cp.async) when the layout cannot be described: V not a multiple of 8, or a base
+// pointer not 16-byte aligned.
+bool make_base_map(const dspark_walk_args* a, int N, CUtensorMap* m) {
+  if ((a->V & 7) != 0 || (reinterpret_cast<uintptr_t>(a->base_logits) & 15u) != 0) return false;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a->V), static_cast<cuuint64_t>(a->K),
+                              static_cast<cuuint64_t>(a->bs)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a->V) * 2,
+                                 static_cast<cuuint64_t>(a->V) * 2 * static_cast<cuuint64_t>(a->K)};
+  const cuuint32_t box[3] = {32, 1, static_cast<cuuint32_t>(N / 2)};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(a->base_logits),
+                         dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int32_t launch_coop(const void* fn, int grid, int threads, size_t smem, WalkParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
@@ -321,6 +359,7 @@ int32_t dspark_walk(const dspark_walk_args* a, dspark_stream_t stream) {
   if (use_tc) {
     const TcPlan pl = plan_tc(caps, a->V, int8, prob, a->bs, a->resident_rows_cap);
     WalkParams p = make_params(a, pl.grid, pl.resident_rows, pl.slice_cap);
+    if (!prob) p.base_tma = make_base_map(a, pl.nq * 4, &p.base_map) ? 1 : 0;
     return launch_coop(walk_tc_kernel_ptr(int8, prob, lg, pl.nq), pl.grid, kWalkThreads, pl.smem, p,
                        reinterpret_cast<cudaStream_t>(stream));
   }

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 
 #include "common.cuh"
 
@@ -24,7 +25,11 @@ struct WalkParams {
   int32_t temp_is_one;
   int32_t resident_rows;     // W2 rows per CTA kept in shared memory (multiple of 32)
   int32_t slice_cap;         // upper bound of the rows of one CTA's vocabulary slice
+  int32_t base_tma;          // base_map is valid (tensor-core walk, greedy)
   StepSync sync;
+  // Tensor map over base [bs][K][V] (bf16), box {32 rows, 1 position, N/2 requests}:
+  // one tile copy brings an epilogue warp's base logits of one 128-row tile.
+  CUtensorMap base_map;      // 128-byte aligned type
 };
 
 // Threads per CTA of the persistent walk kernels: 16 warps.
@@ -77,7 +82,7 @@ __host__ __device__ inline size_t walk_tc_misc_smem() {
          + 64 * 8        // per-row argmax words
          + 4 * 64 * 8    // per-quadrant argmax words
          + 2 * 8         // 2^-s as two factors
-         + 12 * 8 + 16;  // mbarriers, TMEM base, flag, batch |e| maximum
+         + 28 * 8 + 16;  // mbarriers, TMEM base, flag, batch |e| maximum
 }
 
 }  // namespace dspark

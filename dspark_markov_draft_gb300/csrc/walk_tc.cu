@@ -257,7 +257,7 @@ __device__ __forceinline__ void cp_async_wait_pending(int pending) {
 // Roles hand tiles over through mbarriers (A full/empty per buffer and K half, D
 // full/empty per buffer), with two A and two D buffers in tensor memory.
 template <bool INT8, bool PROB, bool LOGITS, int N>
-__global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkParams p) {
+__global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const __grid_constant__ WalkParams p) {
   constexpr int NC = N / 2;                          // columns per epilogue warp
   constexpr int CH = 8;                              // columns per tensor-memory load
   constexpr int NG = NC / 4;                         // 4-column groups per epilogue thread
@@ -269,8 +269,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
   constexpr uint32_t kColD = 256;                    // D[buf][half] at kColD + (2 buf + half) N
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned start, by an offset from smem_raw so that every derived pointer
+  // stays a shared-memory pointer (32-bit shared loads and stores)
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char* b_s = smem;                                      // N x 512 bytes
   uint16_t* base_stage = reinterpret_cast<uint16_t*>(b_s + N * 512);  // greedy: [8 warps][2][N/2][32]
   unsigned char* w2s = b_s + N * 512 + walk_tc_stage_bytes(N, PROB);  // resident rows
@@ -279,12 +280,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
   uint64_t* best_s = reinterpret_cast<uint64_t*>(prev_s + 64);
   uint64_t* red_s = best_s + 64;                                  // [4][64]
   float2* inv_s = reinterpret_cast<float2*>(red_s + 4 * 64);       // 2^-s as two factors
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(inv_s + 2);        // [12]
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(inv_s + 2);        // [28]
   uint64_t* a_full = mbar;        // [buf * 2 + half], 4 arrivals
   uint64_t* a_empty = mbar + 4;   // [buf * 2 + half], 1 commit
   uint64_t* d_full = mbar + 8;    // [buf], 2 commits
   uint64_t* d_empty = mbar + 10;  // [buf], 8 arrivals
-  uint32_t* tbase_s = reinterpret_cast<uint32_t*>(mbar + 12);
+  uint64_t* s_full = mbar + 12;   // [epilogue warp * 2 + stage buffer], 1 arrival + bytes
+  uint32_t* tbase_s = reinterpret_cast<uint32_t*>(mbar + 28);
   int* flag = reinterpret_cast<int*>(tbase_s + 1);
   int* sh_amax = flag + 1;        // largest finite |e| of the batch, as fp32 bits
 
@@ -316,8 +318,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
   }
   if (tid == 0) {
     const uint32_t counts[12] = {4, 4, 4, 4, 1, 1, 1, 1, 2, 2, 8, 8};
-    for (int b = 0; b < 12; ++b)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&mbar[b])), "r"(counts[b]));
+    for (int b = 0; b < 28; ++b)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&mbar[b])), "r"(b < 12 ? counts[b] : 1u));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *sh_amax = 0;
   }
@@ -336,6 +338,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
   bool ok = true;
   int g_base = 0;        // tiles processed by all earlier positions (buffer / phase bookkeeping)
   int last_issued = -1;  // issuers: last tile whose MMAs were committed
+  uint32_t stage_ph = 0;  // greedy epilogue: bit b = parity of stage buffer b's next completion
 
   for (int i = 0; i < p.K && ok; ++i) {
     // ---- B operand: the embedding rows of this position's previous tokens
@@ -430,17 +433,18 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
       // of kPassChunks (one 32-column tensor-memory store each).
       auto load_pass = [&](int t, int pass, uint4 (&c)[kPassChunks]) {
         const int rr = t * kTile + 32 * q + lane;
+        const int ch0 = kHalfChunks * half + kPassChunks * pass;
+        if (rr < res) {  // resident row: shared memory, XOR-swizzled chunks
+          const uint4* row = reinterpret_cast<const uint4*>(w2s + rr * kRowBytes);
 #pragma unroll
-        for (int j = 0; j < kPassChunks; ++j) {
-          const int ch = kHalfChunks * half + kPassChunks * pass + j;
-          if (rr >= n) {
-            c[j] = make_uint4(0, 0, 0, 0);
-          } else if (rr < res) {
-            const int pos = ch ^ (rr & (kChunks - 1));
-            c[j] = *reinterpret_cast<const uint4*>(w2s + static_cast<size_t>(rr) * kRowBytes + 16 * pos);
-          } else {
-            c[j] = __ldg(reinterpret_cast<const uint4*>(w2g + static_cast<size_t>(rr) * kRowBytes) + ch);
-          }
+          for (int j = 0; j < kPassChunks; ++j) c[j] = row[(ch0 + j) ^ (rr & (kChunks - 1))];
+        } else if (rr < n) {  // streamed row: L2
+          const uint4* row = reinterpret_cast<const uint4*>(w2g + static_cast<size_t>(rr) * kRowBytes) + ch0;
+#pragma unroll
+          for (int j = 0; j < kPassChunks; ++j) c[j] = __ldg(row + j);
+        } else {
+#pragma unroll
+          for (int j = 0; j < kPassChunks; ++j) c[j] = make_uint4(0, 0, 0, 0);
         }
       };
       auto store_pass = [&](const uint4 (&c)[kPassChunks], uint32_t col) {
@@ -520,8 +524,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
       // NaN. Equal values (also -0 and +0) never rewrite it, so the first maximum stays.
       // Tiles are 8-bit fields, four columns per register. The lanes and quadrants are
       // combined once per position. The base logits of the warp's rows and columns are
-      // staged in shared memory one tile ahead with cp.async.
-      constexpr int CHG = NC < 16 ? NC : 16;
+      // staged in shared memory one tile ahead.
+      constexpr int CHG = NC < 8 ? NC : 8;
       const int cb = half * NC;                                 // first column of the warp
       const int ncol = max(0, min(NC, p.bs - cb));              // live columns (uniform)
       const int ew = warp - 8;
@@ -530,26 +534,63 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
       const uint32_t live = __ballot_sync(kFull, lane < ncol && prev_s[cb + min(lane, NC - 1)] >= 0);
       const size_t bstride = static_cast<size_t>(p.K) * static_cast<size_t>(p.V);
       const uint16_t* brow = p.base + static_cast<size_t>(i) * p.V + v0;  // + b K V + row
+      // Base logits of tile t into stage buffer t & 1: one tensor-map tile copy (box of
+      // 32 rows x 1 position x NC requests, completion counted in bytes on s_full) when
+      // the host could describe base, else 16-byte cp.async pieces of 8 rows (slices
+      // start on multiples of 32 rows and, with V a multiple of 8, end on multiples of
+      // 8, so a piece is entirely inside or outside), else plain loads.
+      const bool tma = p.base_tma != 0;
       const bool vec_ok = (p.V & 7) == 0 && (reinterpret_cast<uintptr_t>(p.base) & 15u) == 0;
-      // Copy the warp's 32 rows x ncol columns of tile t into stage buffer sb: 16-byte
-      // pieces of 8 rows (slices start on multiples of 32 rows and, with V a multiple
-      // of 8, end on multiples of 8, so a piece is entirely inside or outside).
-      auto stage = [&](int t, int sb) {
+      uint64_t* sfull = s_full + 2 * (warp - 8);
+      int staged = -1;       // last tile whose copy was issued
+      int landed = -1;       // last tile whose copy was waited for
+      auto stage = [&](int t) {
+        const int sb = t & 1;
         const int r0 = t * kTile + 32 * q;
-        for (int e = lane; e < ncol * 4; e += 32) {
-          const int j = e >> 2, c8 = e & 3;
-          if (!((live >> j) & 1u)) continue;
-          const int rr = r0 + 8 * c8;
-          uint16_t* dst = stage_s + (sb * NC + j) * 32 + 8 * c8;
-          const uint16_t* src = brow + static_cast<size_t>(cb + j) * bstride + rr;
-          if (vec_ok) {
-            if (rr < n) cp_async16(dst, src);
-          } else {
-#pragma unroll
-            for (int e8 = 0; e8 < 8; ++e8) dst[e8] = rr + e8 < n ? src[e8] : 0;
+        uint16_t* buf_s = stage_s + sb * NC * 32;
+        if (tma) {
+          if (lane == 0) {
+            constexpr uint32_t kBytes = NC * 32 * 2;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                         ::"r"(smem_u32(&sfull[sb])), "r"(kBytes) : "memory");
+            asm volatile(
+                "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                " [%0], [%1, {%2, %3, %4}], [%5];"
+                ::"r"(smem_u32(buf_s)), "l"(reinterpret_cast<uint64_t>(&p.base_map)),
+                  "r"(static_cast<int>(v0) + r0), "r"(i), "r"(cb), "r"(smem_u32(&sfull[sb]))
+                : "memory");
           }
+        } else {
+          for (int e = lane; e < ncol * 4; e += 32) {
+            const int j = e >> 2, c8 = e & 3;
+            if (!((live >> j) & 1u)) continue;
+            const int rr = r0 + 8 * c8;
+            uint16_t* dst = buf_s + j * 32 + 8 * c8;
+            const uint16_t* src = brow + static_cast<size_t>(cb + j) * bstride + rr;
+            if (vec_ok) {
+              if (rr < n) cp_async16(dst, src);
+            } else {
+#pragma unroll
+              for (int e8 = 0; e8 < 8; ++e8) dst[e8] = rr + e8 < n ? src[e8] : 0;
+            }
+          }
+          cp_async_commit();
         }
-        cp_async_commit();
+        staged = t;
+      };
+      // Wait until tile t's copy has landed (bounded); true on success.
+      auto land = [&](int t) -> bool {
+        bool good = true;
+        if (tma) {
+          const int sb = t & 1;
+          good = mbar_wait(&sfull[sb], (stage_ph >> sb) & 1u, p.sync.timeout_ns);
+          stage_ph ^= 1u << sb;
+        } else {
+          cp_async_wait_pending(staged > t ? 1 : 0);
+        }
+        landed = t;
+        return good;
       };
       float bv[NC];
       uint32_t bt[(NC + 3) / 4];
@@ -557,7 +598,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
       for (int j = 0; j < NC; ++j) bv[j] = -INFINITY;
 #pragma unroll
       for (int w = 0; w < (NC + 3) / 4; ++w) bt[w] = 0u;
-      if (T > 0) stage(0, 0);
+      if (T > 0) stage(0);
       const float2 inv = inv_s[0];
       // One tile; FULL: every row of the tile lies in the slice.
       auto tile = [&](auto full_tag, int t, int buf) {
@@ -576,15 +617,15 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
           tmem_ld2<CHG>(tmem + lane_off + dcol, tmem + lane_off + dcol + N, d0, d1);
 #pragma unroll
           for (int k = 0; k < CHG; ++k) {
-            const int j = cc * CHG + k;
-            if (!((live >> j) & 1u)) continue;  // uniform; also every j >= ncol
+            const int j = cc * CHG + k;  // columns past bs or of dead rows are computed and discarded
             const float bvl = __uint_as_float(static_cast<uint32_t>(bsm[j * 32]) << 16);
             float l;
             if constexpr (INT8) l = __fmaf_rn(__fadd_rn(d0[k], d1[k]), c, bvl);
             else l = __fadd_rn(__fadd_rn(d0[k], d1[k]), bvl);
             if constexpr (!FULL) l = valid ? l : -INFINITY;
             if constexpr (LOGITS)
-              if (valid) p.logits[static_cast<size_t>(cb + j) * bstride + static_cast<size_t>(i) * p.V + v0 + rr] = f32_to_bf16_bits(l);
+              if (valid && j < ncol)
+                p.logits[static_cast<size_t>(cb + j) * bstride + static_cast<size_t>(i) * p.V + v0 + rr] = f32_to_bf16_bits(l);
             float nv;
             asm("max.NaN.f32 %0, %1, %2;" : "=f"(nv) : "f"(bv[j]), "f"(l));
             asm("{ .reg .pred r, u; setp.num.f32 r, %1, %1; setp.neu.and.f32 u, %2, %1, r; "
@@ -596,11 +637,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
       };
       for (int t = 0; t < T; ++t) {
         const int g = g_base + t, buf = g & 1, u = g >> 1;
-        if (t + 1 < T) stage(t + 1, (t + 1) & 1);
+        if (t + 1 < T) stage(t + 1);
         if (!mbar_wait(&d_full[buf], u & 1, p.sync.timeout_ns)) failed = true;
+        if (!failed && !land(t)) failed = true;
         if (__shfl_sync(kFull, failed ? 1 : 0, 0)) { failed = true; break; }
         tc_fence_after();
-        cp_async_wait_pending(t + 1 < T ? 1 : 0);
         __syncwarp();
         if ((t + 1) * kTile <= n) tile(std::true_type{}, t, buf);
         else tile(std::false_type{}, t, buf);
@@ -608,17 +649,24 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const WalkPara
         __syncwarp();
         if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&d_empty[buf])) : "memory");
       }
+      // copies still in flight after a failure land before the CTA can leave
+      for (int t = landed + 1; t <= staged; ++t) land(t);
       asm volatile("cp.async.wait_all;" ::: "memory");
       // per column: (orderable key, first index) maximum over the warp's 32 rows
       const uint32_t vlane = static_cast<uint32_t>(v0) + 32u * q + lane;
-      uint64_t x[NC];
+      constexpr int RG = NC < 16 ? NC : 16;  // columns per reduction group (register budget)
 #pragma unroll
-      for (int j = 0; j < NC; ++j) {
-        const uint32_t tj = (bt[j >> 2] >> (8 * (j & 3))) & 0xFFu;
-        x[j] = j < ncol ? pack_best(order_key(bv[j]), vlane + tj * kTile) : 0ull;
+      for (int g0 = 0; g0 < NC; g0 += RG) {
+        uint64_t x[RG];
+#pragma unroll
+        for (int k = 0; k < RG; ++k) {
+          const int j = g0 + k;
+          const uint32_t tj = (bt[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+          x[k] = j < ncol ? pack_best(order_key(bv[j]), vlane + tj * kTile) : 0ull;
+        }
+        const uint64_t xm = column_max_scatter<RG>(x, lane);
+        if (lane < RG && g0 + lane < ncol) red_s[q * 64 + cb + g0 + lane] = xm;
       }
-      const uint64_t xm = column_max_scatter<NC>(x, lane);
-      if (lane < ncol) red_s[q * 64 + cb + lane] = xm;
     } else {
       // ---------------------------------------------------- epilogue, probabilistic
       // Column c of this thread's group j: b = half * NC + 4 j + (lane & 3).
