@@ -360,7 +360,7 @@ int32_t dspark_walk(const dspark_walk_args* a, dspark_stream_t stream) {
     const TcPlan pl = plan_tc(caps, a->V, int8, prob, a->bs, a->resident_rows_cap);
     WalkParams p = make_params(a, pl.grid, pl.resident_rows, pl.slice_cap);
     if (!prob) p.base_tma = make_base_map(a, pl.nq * 4, &p.base_map) ? 1 : 0;
-    return launch_coop(walk_tc_kernel_ptr(int8, prob, lg, pl.nq), pl.grid, kWalkThreads, pl.smem, p,
+    return launch_coop(walk_tc_kernel_ptr(int8, prob, lg, pl.nq), pl.grid, walk_tc_threads(pl.nq * 4), pl.smem, p,
                        reinterpret_cast<cudaStream_t>(stream));
   }
   const Plan pl = plan_dense(caps, a->V, int8, a->bs, a->resident_rows_cap);

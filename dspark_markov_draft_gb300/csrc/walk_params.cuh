@@ -68,6 +68,12 @@ __host__ __device__ inline int64_t slice_start(int c, int G, int64_t V) {
   return (static_cast<int64_t>(c) * V / G) & ~static_cast<int64_t>(31);
 }
 
+// Tensor-core walk: threads per CTA for N padded request rows. N = 16 adds two warps
+// that only issue MMAs (18 warps, 96 registers per thread); N = 32 and 64 keep 16
+// warps, the issuing done by two producer warps, so that the epilogue keeps 128
+// registers per thread.
+__host__ __device__ constexpr int walk_tc_threads(int N) { return N <= 16 ? 576 : 512; }
+
 // Tensor-core walk, greedy epilogue: base logits staged per epilogue warp (8), two
 // tiles of 32 rows x N/2 request rows, bf16. The epilogue keeps tile numbers in 8-bit
 // fields, so a CTA's vocabulary slice holds at most kTcMaxTiles tiles of 128 rows.

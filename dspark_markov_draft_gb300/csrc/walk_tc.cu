@@ -249,15 +249,19 @@ __device__ __forceinline__ void cp_async_wait_pending(int pending) {
 // N = 16, 32 or 64 padded request rows. Warp roles inside the tile pipeline:
 //   warps 0-7   producers: quadrant w & 3 (tensor-memory lanes), K half w >> 2; each
 //               thread converts half of one W2 row of the tile into tensor memory.
-//               Lane 0 of warp 0 / warp 5 also issues the 8 MMAs of its K half, into
-//               its own accumulator, as soon as the 4 producer warps of that half are
-//               done (two issuing threads double the MMA issue rate).
 //   warps 8-15  epilogue: quadrant w & 3, column half (w - 8) >> 2; each sums the two
 //               K-half accumulators and scores the entries.
+//   MMA issue   one thread per K half issues that half's 8 MMAs of a tile into its own
+//               accumulator once the half's 4 producer warps are done (two issuing
+//               threads double the issue rate): lane 0 of warps 16 and 17, which do
+//               nothing else, for N = 16; lane 0 of producer warps 0 and 5 for N = 32
+//               and 64, where the epilogue needs every register of a 512-thread CTA.
 // Roles hand tiles over through mbarriers (A full/empty per buffer and K half, D
 // full/empty per buffer), with two A and two D buffers in tensor memory.
 template <bool INT8, bool PROB, bool LOGITS, int N>
-__global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const __grid_constant__ WalkParams p) {
+__global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __grid_constant__ WalkParams p) {
+  constexpr bool kOwnIssuers = walk_tc_threads(N) > kWalkThreads;  // warps 16, 17 issue the MMAs
+  constexpr int kWarps = walk_tc_threads(N) / 32;
   constexpr int NC = N / 2;                          // columns per epilogue warp
   constexpr int CH = 8;                              // columns per tensor-memory load
   constexpr int NG = NC / 4;                         // 4-column groups per epilogue thread
@@ -302,9 +306,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const __grid_c
   const bool skip0 = (p.sync.flags & DSPARK_FLAG_SKIP_ARRIVAL_CTA0) && cta == 0;
   const bool producer = warp < 8;
   const int q = warp & 3;                                          // tensor-memory lane quadrant
-  const int half = (warp >> 2) & 1;                                // producers: K half; epilogue: column half
+  // producers and issuers: K half; epilogue: column half
+  const int half = (kOwnIssuers && warp >= 16) ? warp - 16 : (warp >> 2) & 1;
   // MMA issuers: producer warp 0 (K half 0) and 5 (K half 1), on different SM sub-partitions
-  const bool issuer = producer && q == half;
+  const bool issuer = kOwnIssuers ? warp >= 16 : (producer && q == half);
 
   // ---- set-up: zero B, scales, previous tokens, barriers, tensor memory
   for (int t = tid; t < N * 512 / 16; t += blockDim.x) reinterpret_cast<uint4*>(b_s)[t] = make_uint4(0, 0, 0, 0);
@@ -346,7 +351,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const __grid_c
     uint4 wrow[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const int b = warp + kWalkWarps * r;
+      const int b = warp + kWarps * r;
       const int tok = b < p.bs ? prev_s[b] : -1;
       wrow[r] = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(p.w1 + static_cast<size_t>(tok) * kRank) + lane)
                          : make_uint4(0, 0, 0, 0);
@@ -358,7 +363,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const __grid_c
       float amax = 0.f;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int b = warp + kWalkWarps * r;
+        const int b = warp + kWarps * r;
         if (b >= p.bs) break;
         const uint32_t ww[4] = {wrow[r].x, wrow[r].y, wrow[r].z, wrow[r].w};
 #pragma unroll
@@ -381,7 +386,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const __grid_c
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const int b = warp + kWalkWarps * r;
+      const int b = warp + kWarps * r;
       if (b >= p.bs) break;
       uint4 w = wrow[r];
       if constexpr (INT8) {
@@ -484,7 +489,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const __grid_c
         __syncwarp();
         if (lane == 0)
           asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&a_full[buf * 2 + half])) : "memory");
-        if (issuer && lane == 0) {
+        if (!kOwnIssuers && issuer && lane == 0) {
           // MMA issue for this K half: A complete (all 4 quadrants), D buffer free.
           bool good = mbar_wait(&a_full[buf * 2 + half], u & 1, p.sync.timeout_ns);
           if (good && u >= 1) good = mbar_wait(&d_empty[buf], (u - 1) & 1, p.sync.timeout_ns);
@@ -514,6 +519,33 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_tc_kernel(const __grid_c
         if (__shfl_sync(kFull, failed ? 1 : 0, 0)) { failed = true; break; }
       }
       asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (kOwnIssuers && issuer) {
+      // ------------------------------------------------------------- MMA issue
+      // Lane 0 issues this K half's 8 MMAs of every tile into its own accumulator once
+      // the 4 producer warps of the half have stored the tile and the epilogue has
+      // released the D buffer.
+      if (lane == 0) {
+        const uint32_t b_base = smem_u32(b_s);
+        for (int t = 0; t < T; ++t) {
+          const int g = g_base + t, buf = g & 1, u = g >> 1;
+          bool good = mbar_wait(&a_full[buf * 2 + half], u & 1, p.sync.timeout_ns);
+          if (good && u >= 1) good = mbar_wait(&d_empty[buf], (u - 1) & 1, p.sync.timeout_ns);
+          if (!good) { failed = true; break; }
+          tc_fence_after();
+          const uint32_t a_col = buf ? kColA1 : kColA0;
+          const uint32_t d_col = kColD + (2 * buf + half) * N;
+#pragma unroll
+          for (int k8 = 0; k8 < 8; ++k8) {
+            const int kk = 8 * half + k8;
+            const uint64_t bd = sw128_desc(b_base + (kk / 4) * N * 128 + (kk % 4) * 32);
+            mma_f16(tmem + d_col, tmem + a_col + 8 * kk, bd, kIdesc, k8 > 0 ? 1u : 0u);
+          }
+          mma_commit(&d_full[buf]);
+          mma_commit(&a_empty[buf * 2 + half]);
+          last_issued = g;
+        }
+      }
+      __syncwarp();
     } else if constexpr (!PROB) {
       // ------------------------------------------------------- epilogue, greedy
       // Thread = tensor-memory lane = vocabulary row 32 q + lane of the tile; the
