@@ -116,7 +116,7 @@ TcPlan plan_tc(const DeviceCaps& caps, int64_t V, bool int8, bool prob, int bs, 
   const int64_t per_cta = (V + pl.grid - 1) / pl.grid + 32;
   pl.slice_cap = static_cast<int>((per_cta + 31) & ~31LL);
   const int row_bytes = int8 ? kRank : 2 * kRank;
-  const size_t fixed = 1024 + static_cast<size_t>(N) * 512 + walk_tc_stage_bytes(N, prob) +
+  const size_t fixed = 1024 + static_cast<size_t>(N) * 512 + walk_tc_stage_bytes(N) +
                        (int8 ? static_cast<size_t>(pl.slice_cap) * 4 : 0) +
                        walk_tc_misc_smem();
   int64_t rows = caps.smem_optin > static_cast<int>(fixed)
@@ -193,6 +193,7 @@ WalkParams make_params(const dspark_walk_args* a, int grid, int resident_rows, i
   p.top_k = a->top_k;
   p.temperature = a->temperature;
   p.temp_is_one = a->temperature == 1.0f ? 1 : 0;
+  p.inv_temperature = static_cast<float>(1.0 / static_cast<double>(a->temperature));
   p.resident_rows = resident_rows;
   p.slice_cap = slice_cap;
   p.sync = make_sync(a, grid);
@@ -214,12 +215,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Tensor map over the base logits [bs][K][V] for the greedy tensor-core epilogue: box of
-// 32 vocabulary rows x 1 position x N/2 requests. False (and the kernel stages with
-// cp.async) when the layout cannot be described: V not a multiple of 8, or a base
-// pointer not 16-byte aligned.
-bool make_base_map(const dspark_walk_args* a, int N, CUtensorMap* m) {
-  if ((a->V & 7) != 0 || (reinterpret_cast<uintptr_t>(a->base_logits) & 15u) != 0) return false;
+// Tensor map over a [bs][K][V] bf16 tensor (base logits or draft_logits) for the
+// tensor-core epilogue: box of 32 vocabulary rows x 1 position x N/2 requests. False
+// (and the kernel uses per-thread copies) when the layout cannot be described: V not a
+// multiple of 8, or a pointer not 16-byte aligned.
+bool make_bsk_map(const dspark_walk_args* a, const uint16_t* ptr, int N, CUtensorMap* m) {
+  if (!ptr || (a->V & 7) != 0 || (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return false;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a->V), static_cast<cuuint64_t>(a->K),
@@ -228,7 +229,7 @@ bool make_base_map(const dspark_walk_args* a, int N, CUtensorMap* m) {
                                  static_cast<cuuint64_t>(a->V) * 2 * static_cast<cuuint64_t>(a->K)};
   const cuuint32_t box[3] = {32, 1, static_cast<cuuint32_t>(N / 2)};
   const cuuint32_t elem[3] = {1, 1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(a->base_logits),
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(ptr),
                          dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -359,7 +360,8 @@ int32_t dspark_walk(const dspark_walk_args* a, dspark_stream_t stream) {
   if (use_tc) {
     const TcPlan pl = plan_tc(caps, a->V, int8, prob, a->bs, a->resident_rows_cap);
     WalkParams p = make_params(a, pl.grid, pl.resident_rows, pl.slice_cap);
-    if (!prob) p.base_tma = make_base_map(a, pl.nq * 4, &p.base_map) ? 1 : 0;
+    p.base_tma = make_bsk_map(a, a->base_logits, pl.nq * 4, &p.base_map) ? 1 : 0;
+    p.logits_tma = make_bsk_map(a, a->draft_logits, pl.nq * 4, &p.logits_map) ? 1 : 0;
     return launch_coop(walk_tc_kernel_ptr(int8, prob, lg, pl.nq), pl.grid, walk_tc_threads(pl.nq * 4), pl.smem, p,
                        reinterpret_cast<cudaStream_t>(stream));
   }

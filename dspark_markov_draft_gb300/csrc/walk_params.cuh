@@ -25,11 +25,16 @@ struct WalkParams {
   int32_t temp_is_one;
   int32_t resident_rows;     // W2 rows per CTA kept in shared memory (multiple of 32)
   int32_t slice_cap;         // upper bound of the rows of one CTA's vocabulary slice
-  int32_t base_tma;          // base_map is valid (tensor-core walk, greedy)
+  int32_t base_tma;          // base_map is valid (tensor-core walk)
+  int32_t logits_tma;        // logits_map is valid (tensor-core walk)
+  float inv_temperature;     // 1 / temperature, rounded to fp32 (tensor-core walk)
   StepSync sync;
   // Tensor map over base [bs][K][V] (bf16), box {32 rows, 1 position, N/2 requests}:
   // one tile copy brings an epilogue warp's base logits of one 128-row tile.
   CUtensorMap base_map;      // 128-byte aligned type
+  // The same geometry over draft_logits: an epilogue warp's tile of bf16 logits goes
+  // back to global memory in one tile copy.
+  CUtensorMap logits_map;
 };
 
 // Threads per CTA of the persistent walk kernels: 16 warps.
@@ -74,17 +79,16 @@ __host__ __device__ inline int64_t slice_start(int c, int G, int64_t V) {
 // registers per thread.
 __host__ __device__ constexpr int walk_tc_threads(int N) { return N <= 16 ? 576 : 512; }
 
-// Tensor-core walk, greedy epilogue: base logits staged per epilogue warp (8), two
+// Tensor-core walk epilogue: base logits staged per epilogue warp (8), two
 // tiles of 32 rows x N/2 request rows, bf16. The epilogue keeps tile numbers in 8-bit
 // fields, so a CTA's vocabulary slice holds at most kTcMaxTiles tiles of 128 rows.
 constexpr int kTcMaxTiles = 255;
-__host__ __device__ constexpr int walk_tc_stage_bytes(int N, bool prob) {
-  return prob ? 0 : 8 * 2 * (N / 2) * 32 * 2;
-}
+__host__ __device__ constexpr int walk_tc_stage_bytes(int N) { return 8 * 2 * (N / 2) * 32 * 2; }
 
 // Tensor-core walk: shared memory besides the B operand and the resident rows.
 __host__ __device__ inline size_t walk_tc_misc_smem() {
   return 64 * 4          // prev tokens
+         + 64 * 8        // seeds
          + 64 * 8        // per-row argmax words
          + 4 * 64 * 8    // per-quadrant argmax words
          + 2 * 8         // 2^-s as two factors

@@ -19,11 +19,13 @@
 //   * D[128 x N] = A . B^T accumulates in fp32 in tensor memory. One thread issues an
 //     MMA only about every 70 cycles whatever N is, so the K range is split in two
 //     halves issued by two threads into two accumulators, which the epilogue adds.
-//   * Epilogue (8 warps): each warp reads its quadrant's rows for its N/2 columns,
-//     transposes 4 x 4 blocks across lanes so that a thread owns 4 consecutive
-//     vocabulary entries of one request row (one Philox call, one 8-byte base load,
-//     one 8-byte logits store per 4 entries), forms l = base + scale_v 2^-s_b D and
-//     the score, and keeps a running (orderable key, first index) maximum per row.
+//   * Epilogue (8 warps): thread = tensor-memory lane = one vocabulary row of the
+//     tile, for N/2 request rows. It adds the two K-half accumulators, forms
+//     l = base + scale_v 2^-s D (base logits staged one tile ahead by a tensor-map
+//     copy), the score (greedy: l; probabilistic: bf16(l)/T plus Gumbel noise, whose
+//     Philox blocks of 4 consecutive rows are drawn once per lane quad and exchanged
+//     by a 4 x 4 transpose), and keeps per column the running maximum and the tile
+//     where it was first reached; lanes and quadrants are combined once per position.
 //   * Producers, MMA issuers and the epilogue hand tiles over through mbarriers, with
 //     two A and two D buffers, so the three overlap across tiles.
 #include <cstdint>
@@ -128,18 +130,6 @@ __device__ __forceinline__ void tmem_st32_u4(uint32_t taddr, const uint4 (&c)[8]
       : "memory");
 }
 
-template <int NQ>
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&out)[NQ]);
-template <>
-__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, float (&o)[8]) {
-  uint32_t r[8];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                 "=r"(r[6]), "=r"(r[7]) : "r"(taddr) : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int j = 0; j < 8; ++j) o[j] = __uint_as_float(r[j]);
-}
 // Two loads of CH consecutive columns (the two K-half accumulators), one wait.
 template <int CH>
 __device__ __forceinline__ void tmem_ld2(uint32_t a0, uint32_t a1, float (&d0)[CH], float (&d1)[CH]);
@@ -156,26 +146,6 @@ __device__ __forceinline__ void tmem_ld2<8>(uint32_t a0, uint32_t a1, float (&d0
 #pragma unroll
   for (int j = 0; j < 8; ++j) { d0[j] = __uint_as_float(r[j]); d1[j] = __uint_as_float(r[8 + j]); }
 }
-template <>
-__device__ __forceinline__ void tmem_ld2<16>(uint32_t a0, uint32_t a1, float (&d0)[16], float (&d1)[16]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]) : "r"(a0) : "memory");
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15}, [%16];"
-      : "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
-        "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-        "=r"(r[30]), "=r"(r[31]) : "r"(a1) : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int j = 0; j < 16; ++j) { d0[j] = __uint_as_float(r[j]); d1[j] = __uint_as_float(r[16 + j]); }
-}
-
 // Column maxima of NC packed words per lane over the 32 lanes of a warp: plain
 // butterfly rounds while the offset is at least NC, then reduce-scatter rounds that
 // halve the columns a lane holds; lane l returns the maximum of column l % NC.
@@ -263,8 +233,6 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
   constexpr bool kOwnIssuers = walk_tc_threads(N) > kWalkThreads;  // warps 16, 17 issue the MMAs
   constexpr int kWarps = walk_tc_threads(N) / 32;
   constexpr int NC = N / 2;                          // columns per epilogue warp
-  constexpr int CH = 8;                              // columns per tensor-memory load
-  constexpr int NG = NC / 4;                         // 4-column groups per epilogue thread
   constexpr int kRowBytes = INT8 ? kRank : 2 * kRank;
   constexpr int kChunks = kRowBytes / 16;            // 16-byte chunks per W2 row
   constexpr int kHalfChunks = kChunks / 2;           // per producer thread and tile
@@ -277,11 +245,12 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
   // stays a shared-memory pointer (32-bit shared loads and stores)
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char* b_s = smem;                                      // N x 512 bytes
-  uint16_t* base_stage = reinterpret_cast<uint16_t*>(b_s + N * 512);  // greedy: [8 warps][2][N/2][32]
-  unsigned char* w2s = b_s + N * 512 + walk_tc_stage_bytes(N, PROB);  // resident rows
+  uint16_t* base_stage = reinterpret_cast<uint16_t*>(b_s + N * 512);  // [8 warps][2][N/2][32]
+  unsigned char* w2s = b_s + N * 512 + walk_tc_stage_bytes(N);      // resident rows
   float* scale_s = reinterpret_cast<float*>(w2s + static_cast<size_t>(p.resident_rows) * kRowBytes);
   int* prev_s = reinterpret_cast<int*>(scale_s + (INT8 ? p.slice_cap : 0));   // [64]
-  uint64_t* best_s = reinterpret_cast<uint64_t*>(prev_s + 64);
+  uint64_t* seed_s = reinterpret_cast<uint64_t*>(prev_s + 64);    // [64] per-request seeds
+  uint64_t* best_s = seed_s + 64;
   uint64_t* red_s = best_s + 64;                                  // [4][64]
   float2* inv_s = reinterpret_cast<float2*>(red_s + 4 * 64);       // 2^-s as two factors
   uint64_t* mbar = reinterpret_cast<uint64_t*>(inv_s + 2);        // [28]
@@ -315,6 +284,7 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
   for (int t = tid; t < N * 512 / 16; t += blockDim.x) reinterpret_cast<uint4*>(b_s)[t] = make_uint4(0, 0, 0, 0);
   if (INT8)
     for (int r = tid; r < n; r += blockDim.x) scale_s[r] = __ldg(p.scales + v0 + r);
+  for (int t = tid; t < 64; t += blockDim.x) seed_s[t] = (PROB && t < p.bs) ? p.seeds[t] : 0ull;
   for (int t = tid; t < p.bs; t += blockDim.x) {
     const int32_t tok = p.prev[t];
     const bool okt = tok >= 0 && static_cast<int64_t>(tok) < p.V;
@@ -343,7 +313,7 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
   bool ok = true;
   int g_base = 0;        // tiles processed by all earlier positions (buffer / phase bookkeeping)
   int last_issued = -1;  // issuers: last tile whose MMAs were committed
-  uint32_t stage_ph = 0;  // greedy epilogue: bit b = parity of stage buffer b's next completion
+  uint32_t stage_ph = 0;  // epilogue: bit b = parity of stage buffer b's next completion
 
   for (int i = 0; i < p.K && ok; ++i) {
     // ---- B operand: the embedding rows of this position's previous tokens
@@ -546,8 +516,8 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
         }
       }
       __syncwarp();
-    } else if constexpr (!PROB) {
-      // ------------------------------------------------------- epilogue, greedy
+    } else {
+      // -------------------------------------------------------------- epilogue
       // Thread = tensor-memory lane = vocabulary row 32 q + lane of the tile; the
       // warp's NC columns (request rows) are warp-uniform. Each thread keeps, per
       // column, the running maximum of its rows over the tiles (max.NaN: a NaN sticks)
@@ -572,6 +542,8 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
       // start on multiples of 32 rows and, with V a multiple of 8, end on multiples of
       // 8, so a piece is entirely inside or outside), else plain loads.
       const bool tma = p.base_tma != 0;
+      // logits through the stage buffer only when the base arrives by tensor-map copy too
+      [[maybe_unused]] const bool ltma = tma && p.logits_tma != 0;
       const bool vec_ok = (p.V & 7) == 0 && (reinterpret_cast<uintptr_t>(p.base) & 15u) == 0;
       uint64_t* sfull = s_full + 2 * (warp - 8);
       int staged = -1;       // last tile whose copy was issued
@@ -583,6 +555,7 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
         if (tma) {
           if (lane == 0) {
             constexpr uint32_t kBytes = NC * 32 * 2;
+            if (LOGITS && ltma) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                          ::"r"(smem_u32(&sfull[sb])), "r"(kBytes) : "memory");
@@ -641,12 +614,14 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
         if constexpr (INT8) c = __fmul_rn(__fmul_rn(valid ? scale_s[rr] : 0.f, inv.x), inv.y);
         const uint32_t trep = static_cast<uint32_t>(t) * 0x01010101u;
         const uint16_t* bsm = stage_s + (t & 1) * NC * 32 + lane;
+        [[maybe_unused]] uint16_t* bsw = stage_s + (t & 1) * NC * 32 + lane;
 #pragma unroll
         for (int cc = 0; cc < NC / CHG; ++cc) {
           if (cc * CHG >= ncol) break;
           float d0[CHG], d1[CHG];
           const uint32_t dcol = kColD + 2 * buf * N + cb + cc * CHG;
           tmem_ld2<CHG>(tmem + lane_off + dcol, tmem + lane_off + dcol + N, d0, d1);
+          float sc[CHG];  // scores of this thread's row in the chunk's columns
 #pragma unroll
           for (int k = 0; k < CHG; ++k) {
             const int j = cc * CHG + k;  // columns past bs or of dead rows are computed and discarded
@@ -655,11 +630,40 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
             if constexpr (INT8) l = __fmaf_rn(__fadd_rn(d0[k], d1[k]), c, bvl);
             else l = __fadd_rn(__fadd_rn(d0[k], d1[k]), bvl);
             if constexpr (!FULL) l = valid ? l : -INFINITY;
-            if constexpr (LOGITS)
-              if (valid && j < ncol)
-                p.logits[static_cast<size_t>(cb + j) * bstride + static_cast<size_t>(i) * p.V + v0 + rr] = f32_to_bf16_bits(l);
+            [[maybe_unused]] const uint16_t lh = f32_to_bf16_bits(l);
+            if constexpr (LOGITS) {
+              if (ltma) bsw[j * 32] = lh;  // the tile of logits replaces the tile of base
+              else if (valid && j < ncol)
+                p.logits[static_cast<size_t>(cb + j) * bstride + static_cast<size_t>(i) * p.V + v0 + rr] = lh;
+            }
+            if constexpr (PROB) {
+              const float lb = bf16_to_f32(lh);
+              sc[k] = p.temp_is_one ? lb : __fmul_rn(lb, p.inv_temperature);
+            } else {
+              sc[k] = l;
+            }
+          }
+          if constexpr (PROB) {
+            // Gumbel noise: lane 4m + k draws the Philox block of rows 4m..4m+3 (of
+            // this warp's 32) and column jb + k, then a 4 x 4 transpose inside the lane
+            // quad leaves every lane the draws of its own row for columns jb..jb+3.
+            const uint32_t m = (static_cast<uint32_t>(v0) + t * kTile + 32 * q) / 4 + (lane >> 2);
+#pragma unroll
+            for (int h4 = 0; h4 < CHG / 4; ++h4) {
+              const int bq = cb + cc * CHG + 4 * h4 + (lane & 3);
+              const uint4 w = philox_block(seed_s[bq], bq, i, m);
+              float g4[4] = {gumbel_from_word(w.x), gumbel_from_word(w.y), gumbel_from_word(w.z),
+                             gumbel_from_word(w.w)};
+              transpose4(g4, lane);
+#pragma unroll
+              for (int r = 0; r < 4; ++r) sc[4 * h4 + r] = __fadd_rn(sc[4 * h4 + r], g4[r]);
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < CHG; ++k) {
+            const int j = cc * CHG + k;
             float nv;
-            asm("max.NaN.f32 %0, %1, %2;" : "=f"(nv) : "f"(bv[j]), "f"(l));
+            asm("max.NaN.f32 %0, %1, %2;" : "=f"(nv) : "f"(bv[j]), "f"(sc[k]));
             asm("{ .reg .pred r, u; setp.num.f32 r, %1, %1; setp.neu.and.f32 u, %2, %1, r; "
                 "@u lop3.b32 %0, %0, %3, %4, 0xB8; }"
                 : "+r"(bt[j >> 2]) : "f"(bv[j]), "f"(nv), "r"(0xFFu << (8 * (j & 3))), "r"(trep));
@@ -679,10 +683,25 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
         else tile(std::false_type{}, t, buf);
         tc_fence_before();
         __syncwarp();
+        if constexpr (LOGITS) {
+          // the warp's 32 rows of logits, unless they all lie past the slice (rows past
+          // V and requests past bs are clipped by the copy)
+          if (ltma && lane == 0 && t * kTile + 32 * q < n) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile(
+                "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+                ::"l"(reinterpret_cast<uint64_t>(&p.logits_map)), "r"(static_cast<int>(v0) + t * kTile + 32 * q),
+                  "r"(i), "r"(cb), "r"(smem_u32(stage_s + (t & 1) * NC * 32))
+                : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          }
+        }
         if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&d_empty[buf])) : "memory");
       }
-      // copies still in flight after a failure land before the CTA can leave
+      // copies still in flight after a failure land before the CTA can leave; logits
+      // stores are complete before the position ends
       for (int t = landed + 1; t <= staged; ++t) land(t);
+      if (LOGITS && ltma && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
       asm volatile("cp.async.wait_all;" ::: "memory");
       // per column: (orderable key, first index) maximum over the warp's 32 rows
       const uint32_t vlane = static_cast<uint32_t>(v0) + 32u * q + lane;
@@ -698,128 +717,6 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
         }
         const uint64_t xm = column_max_scatter<RG>(x, lane);
         if (lane < RG && g0 + lane < ncol) red_s[q * 64 + cb + g0 + lane] = xm;
-      }
-    } else {
-      // ---------------------------------------------------- epilogue, probabilistic
-      // Column c of this thread's group j: b = half * NC + 4 j + (lane & 3).
-      uint32_t live_mask = 0;
-      uint64_t best[NG];
-#pragma unroll
-      for (int j = 0; j < NG; ++j) {
-        const int b = half * NC + 4 * j + (lane & 3);
-        if (b < p.bs && prev_s[b] >= 0) live_mask |= 1u << j;
-        best[j] = 0ull;
-      }
-      auto fetch_base = [&](int t, uint2 (&bw)[NG]) {
-        const int rr0 = t * kTile + 32 * q + 4 * (lane >> 2);
-#pragma unroll
-        for (int j = 0; j < NG; ++j) {
-          bw[j] = make_uint2(0u, 0u);
-          if (!((live_mask >> j) & 1u) || rr0 >= n) continue;
-          const int b = half * NC + 4 * j + (lane & 3);
-          const uint16_t* src = p.base + (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v0 + rr0;
-          if (rr0 + 3 < n && (reinterpret_cast<uintptr_t>(src) & 7u) == 0) {
-            bw[j] = __ldg(reinterpret_cast<const uint2*>(src));
-          } else {
-            uint16_t h[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) h[k] = rr0 + k < n ? src[k] : 0;
-            bw[j] = make_uint2(static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 16),
-                               static_cast<uint32_t>(h[2]) | (static_cast<uint32_t>(h[3]) << 16));
-          }
-        }
-      };
-      uint2 bcur[NG], bnext[NG];
-      if (T > 0) fetch_base(0, bcur);
-      for (int t = 0; t < T; ++t) {
-        const int g = g_base + t, buf = g & 1, u = g >> 1;
-        if (t + 1 < T) fetch_base(t + 1, bnext);
-        if (!mbar_wait(&d_full[buf], u & 1, p.sync.timeout_ns)) failed = true;
-        if (__shfl_sync(kFull, failed ? 1 : 0, 0)) { failed = true; break; }
-        tc_fence_after();
-        const int rr0 = t * kTile + 32 * q + 4 * (lane >> 2);  // this thread's 4 rows
-        float sc[4] = {1.f, 1.f, 1.f, 1.f};
-        if constexpr (INT8) {
-          if (rr0 + 3 < n) {
-            const float4 s4 = *reinterpret_cast<const float4*>(scale_s + rr0);
-            sc[0] = s4.x; sc[1] = s4.y; sc[2] = s4.z; sc[3] = s4.w;
-          } else {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) sc[k] = rr0 + k < n ? scale_s[rr0 + k] : 0.f;
-          }
-        }
-#pragma unroll
-        for (int cc = 0; cc < NC / CH; ++cc) {
-          float d[CH], d2[CH];
-          const uint32_t dcol = kColD + 2 * buf * N + half * NC + cc * CH;
-          tmem_ld<CH>(tmem + lane_off + dcol, d);        // K half 0
-          tmem_ld<CH>(tmem + lane_off + dcol + N, d2);   // K half 1
-#pragma unroll
-          for (int k = 0; k < CH; ++k) d[k] = __fadd_rn(d[k], d2[k]);
-#pragma unroll
-          for (int gg = 0; gg < CH / 4; ++gg) {
-            const int j = cc * (CH / 4) + gg;
-            float x[4] = {d[4 * gg + 0], d[4 * gg + 1], d[4 * gg + 2], d[4 * gg + 3]};
-            transpose4(x, lane);
-            if (!((live_mask >> j) & 1u) || rr0 >= n) continue;
-            const int b = half * NC + 4 * j + (lane & 3);
-            const size_t o = (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v0 + rr0;
-            const float bv[4] = {bf16_lo(bcur[j].x), bf16_hi(bcur[j].x), bf16_lo(bcur[j].y), bf16_hi(bcur[j].y)};
-            float l[4];
-            const float2 inv = INT8 ? inv_s[0] : make_float2(1.f, 1.f);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              float bias = x[k];
-              if constexpr (INT8) bias = __fmul_rn(__fmul_rn(__fmul_rn(bias, sc[k]), inv.x), inv.y);
-              l[k] = __fadd_rn(bv[k], bias);
-            }
-            if constexpr (LOGITS) {
-              uint16_t h[4];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) h[k] = f32_to_bf16_bits(l[k]);
-              if (rr0 + 3 < n && (reinterpret_cast<uintptr_t>(p.logits + o) & 7u) == 0) {
-                *reinterpret_cast<uint2*>(p.logits + o) =
-                    make_uint2(static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 16),
-                               static_cast<uint32_t>(h[2]) | (static_cast<uint32_t>(h[3]) << 16));
-              } else {
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  if (rr0 + k < n) p.logits[o + k] = h[k];
-              }
-            }
-            float sco[4] = {l[0], l[1], l[2], l[3]};
-            if constexpr (PROB) {
-              const uint4 w = philox_block(p.seeds[b], b, i, static_cast<uint32_t>((v0 + rr0) >> 2));
-              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float lb = bf16_to_f32(f32_to_bf16_bits(l[k]));
-                const float xs = p.temp_is_one ? lb : __fdiv_rn(lb, p.temperature);
-                sco[k] = __fadd_rn(xs, gumbel_from_word(ws[k]));
-              }
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              if (rr0 + k < n)
-                best[j] = umax64(best[j], pack_best(order_key(sco[k]), static_cast<uint32_t>(v0 + rr0 + k)));
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&d_empty[buf])) : "memory");
-        if (t + 1 < T) {
-#pragma unroll
-          for (int j = 0; j < NG; ++j) bcur[j] = bnext[j];
-        }
-      }
-      // CTA argmax per request row: lanes sharing (lane & 3) hold the same column.
-#pragma unroll
-      for (int j = 0; j < NG; ++j) {
-        uint64_t x = best[j];
-        x = umax64(x, __shfl_xor_sync(kFull, x, 4));
-        x = umax64(x, __shfl_xor_sync(kFull, x, 8));
-        x = umax64(x, __shfl_xor_sync(kFull, x, 16));
-        if (lane < 4) red_s[q * 64 + half * NC + 4 * j + lane] = x;
       }
     }
     g_base += T;
