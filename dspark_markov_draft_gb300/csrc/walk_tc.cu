@@ -134,6 +134,17 @@ __device__ __forceinline__ void tmem_st32_u4(uint32_t taddr, const uint4 (&c)[8]
 template <int CH>
 __device__ __forceinline__ void tmem_ld2(uint32_t a0, uint32_t a1, float (&d0)[CH], float (&d1)[CH]);
 template <>
+__device__ __forceinline__ void tmem_ld2<4>(uint32_t a0, uint32_t a1, float (&d0)[4], float (&d1)[4]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a0) : "memory");
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]) : "r"(a1) : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 4; ++j) { d0[j] = __uint_as_float(r[j]); d1[j] = __uint_as_float(r[4 + j]); }
+}
+template <>
 __device__ __forceinline__ void tmem_ld2<8>(uint32_t a0, uint32_t a1, float (&d0)[8], float (&d1)[8]) {
   uint32_t r[16];
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
@@ -527,7 +538,7 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
       // Tiles are 8-bit fields, four columns per register. The lanes and quadrants are
       // combined once per position. The base logits of the warp's rows and columns are
       // staged in shared memory one tile ahead.
-      constexpr int CHG = NC < 8 ? NC : 8;
+      constexpr int CHG = NC < 8 ? NC : (PROB ? 4 : 8);
       const int cb = half * NC;                                 // first column of the warp
       const int ncol = max(0, min(NC, p.bs - cb));              // live columns (uniform)
       const int ew = warp - 8;
