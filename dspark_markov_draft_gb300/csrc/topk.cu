@@ -4,12 +4,19 @@
 // (their bf16 W2 rows are gathered), and each step's argmax or Gumbel-max sample runs
 // over the dense row that is -inf everywhere off the candidates.
 //
-// topk_select_kernel: one CTA per (b, i) row. Two 256-bin histogram passes over the
-// 16-bit orderable key of the bf16 base logits find the k-th largest key T and how
-// many entries equal to T are still needed; a third pass compacts, in ascending
-// vocabulary order, every entry above T plus the first `need` entries equal to T
-// (ties at the boundary go to the smaller index; NaN is the largest key). With
-// draft_logits requested it also writes -inf at every non-candidate entry.
+// topk_select_kernel: one CTA per (b, i) row; candidates are written in no particular
+// order (only the set matters). Keys are 16-bit orderable keys of the bf16 base logits
+// (NaN largest, -0 equal to +0); the set is every entry with key above the k-th
+// largest key T plus, among the entries equal to T, the ones with the smallest
+// vocabulary indices. Fast path: a histogram of the 11-bit key prefix of ~4096 evenly
+// spaced samples gives a pivot prefix that at least ~1.15 k entries reach; one pass
+// over the row collects every entry at or above the pivot into shared memory (warp-
+// aggregated appends); T is found by a two-byte radix select on that list; boundary
+// ties are resolved by ranking the tied indices. Rows where the pivot collects fewer
+// than k or more than kSelCap entries, or the tie at T is wider than kSelTies, take the
+// exact path over the whole row: two 256-bin histogram passes and an ordered
+// compaction. With draft_logits requested the row is first filled with -inf (the walk
+// writes the candidates).
 //
 // topk_walk_kernel: persistent cooperative kernel over the K positions; the bs*k
 // (row, candidate) items are split evenly over the grid; 8 lanes share a gathered W2
@@ -24,8 +31,12 @@ namespace dspark {
 
 namespace {
 
-constexpr int kSelThreads = 1024;
+constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelCap = 8192;    // entries collected by the fast path
+constexpr int kSelTies = 2048;   // widest tie at the k-th key the fast path resolves
+constexpr int kSelBins = 2048;   // 11-bit key prefixes
+constexpr int kSelSamples = 4096;
 
 // Orderable 16-bit key of a bf16 pattern: NaN largest, -0 equal to +0.
 __device__ __forceinline__ uint32_t key16(uint16_t h) {
@@ -65,14 +76,10 @@ __device__ __forceinline__ int block_exscan(int x, int* sh, int& total) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const uint16_t* base, int64_t V,
-                                                                  int k, int32_t* cand,
-                                                                  uint16_t* logits) {
-  __shared__ int hist[256];
-  __shared__ int scan_sh[80];
-  __shared__ int sel[4];
-  const size_t row = blockIdx.x;
-  const uint16_t* x = base + row * static_cast<size_t>(V);
+// Exact selection over the whole row (the fast path's fallback): candidates in
+// ascending vocabulary order.
+__device__ void select_exact(const uint16_t* x, int64_t V, int k, int32_t* out, int* hist,
+                             int* scan_sh, int* sel) {
 
   // Pass 1 and 2: histograms of the high and then the low byte of the key.
   uint32_t prefix = 0;
@@ -132,11 +139,238 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const uint16_t
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
       if (vb + t >= V) continue;
-      if (take[t]) cand[row * k + pos++] = static_cast<int32_t>(vb + t);
-      else if (logits) logits[row * static_cast<size_t>(V) + vb + t] = 0xFF80u;  // -inf
+      if (take[t]) out[pos++] = static_cast<int32_t>(vb + t);
     }
     eq_seen += eq_total;
     out_base += take_total;
+  }
+}
+
+
+// Per-halfword unsigned maximum of two packed pairs.
+__device__ __forceinline__ uint32_t umax_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Warp-aggregated append: every lane adds `c` items; returns this lane's first slot of
+// a block-wide counter (all lanes of the warp call it).
+__device__ __forceinline__ int warp_append(int c, int* counter) {
+  const int lane = threadIdx.x & 31;
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int base = 0;
+  if (lane == 31) base = atomicAdd(counter, incl);
+  base = __shfl_sync(kFull, base, 31);
+  return base + incl - c;
+}
+
+__global__ void __launch_bounds__(kSelThreads, 3) topk_select_kernel(const uint16_t* base, int64_t V,
+                                                                  int k, int32_t* cand,
+                                                                  uint16_t* logits) {
+  extern __shared__ __align__(16) unsigned char sel_smem[];
+  int* hist = reinterpret_cast<int*>(sel_smem);                           // [kSelBins]
+  uint32_t* lidx = reinterpret_cast<uint32_t*>(hist + kSelBins);           // [kSelCap]
+  uint16_t* lkey = reinterpret_cast<uint16_t*>(lidx + kSelCap);            // [kSelCap]
+  int* scan_sh = reinterpret_cast<int*>(lkey + kSelCap);                   // [80]
+  int* sel = scan_sh + 80;                                                 // [8]
+  const int tid = threadIdx.x;
+  const size_t row = blockIdx.x;
+  const uint16_t* x = base + row * static_cast<size_t>(V);
+  int32_t* out = cand + row * static_cast<size_t>(k);
+
+  if (logits) {  // -inf everywhere; the walk overwrites the candidates
+    uint16_t* lr = logits + row * static_cast<size_t>(V);
+    for (int64_t v = tid; v < V; v += kSelThreads) lr[v] = 0xFF80u;
+  }
+
+  // 1. pivot prefix from a sample histogram
+  for (int t = tid; t < kSelBins; t += kSelThreads) hist[t] = 0;
+  if (tid < 8) sel[tid] = 0;
+  __syncthreads();
+  // samples: kSelSamples / 64 blocks of 64 consecutive entries, evenly spaced (whole
+  // cache lines); rows shorter than kSelSamples are taken whole
+  const int64_t nblk = kSelSamples / 64;
+  const int64_t stride = V > kSelSamples ? V / kSelSamples : 1;  // entries per sample
+  const int64_t ns = V > kSelSamples ? kSelSamples : V;
+  const int64_t bstep = V > kSelSamples ? V / nblk : 0;
+  for (int64_t s0 = 0; s0 < ns; s0 += 8 * kSelThreads) {  // loads first, then the atomics
+    uint16_t sv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int64_t sj = s0 + j * kSelThreads + tid;
+      const int64_t v = V > kSelSamples ? (sj >> 6) * bstep + (sj & 63) : sj;
+      sv[j] = sj < ns ? __ldg(x + v) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (s0 + j * kSelThreads + tid < ns) atomicAdd(&hist[key16(sv[j]) >> 5], 1);
+  }
+  __syncthreads();
+  // bins in descending order, 4 per thread: the largest prefix whose suffix count
+  // reaches the target
+  const int target = static_cast<int>(static_cast<double>(k) * 1.15 / static_cast<double>(stride)) + 12;
+  int c4 = 0;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) c4 += hist[kSelBins - 1 - (4 * tid + t)];
+  int total;
+  const int before = block_exscan(c4, scan_sh, total);
+  if (tid == 0) sel[0] = 0;  // pivot prefix (0: collect everything)
+  __syncthreads();
+  if (before < target && before + c4 >= target) {
+    int acc = before;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int bin = kSelBins - 1 - (4 * tid + t);
+      acc += hist[bin];
+      if (acc >= target) { sel[0] = bin; break; }
+    }
+  }
+  __syncthreads();
+  const uint32_t pivot = static_cast<uint32_t>(sel[0]) << 5;
+
+  // 2. collect every entry with key >= pivot: 16-byte loads of 8 entries, four per
+  // thread in flight, when the row is 16-byte aligned; single entries otherwise
+  int* n_col = sel + 1;
+  auto append = [&](uint32_t take, auto index_of) {
+    int pos = warp_append(__popc(take), n_col);
+    while (take) {
+      const int t = __ffs(take) - 1;
+      take &= take - 1;
+      const int64_t v = index_of(t);
+      if (pos < kSelCap) {
+        lidx[pos] = static_cast<uint32_t>(v);
+        lkey[pos] = static_cast<uint16_t>(key16(x[v]));
+      }
+      ++pos;
+    }
+  };
+  if ((V & 7) == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
+    const uint4* x4 = reinterpret_cast<const uint4*>(x);
+    const int64_t n8 = V / 8;
+    auto load4 = [&](int64_t c0, uint4 (&w)[4]) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t c = c0 + j * kSelThreads + tid;
+        w[j] = c < n8 ? __ldg(x4 + c) : make_uint4(0, 0, 0, 0);
+      }
+    };
+    const bool quick = pivot > 0x8000u;  // pivot above the keys of -0 / +0
+    uint4 w[4], wn[4];
+    load4(0, w);
+    for (int64_t c0 = 0; c0 < n8; c0 += 4 * kSelThreads) {
+      if (c0 + 4 * kSelThreads < n8) load4(c0 + 4 * kSelThreads, wn);  // next batch in flight
+      uint32_t take = 0;  // bit 8 j + e: entry 8 (c0 + j kSelThreads + tid) + e
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t c = c0 + j * kSelThreads + tid;
+        const uint32_t ww[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+        // Quick reject of 8 entries: with the pivot above -0, only non-negative
+        // entries (whose key is the pattern with the sign bit set) or NaNs can pass.
+        if (quick) {
+          const uint32_t m = umax_u16x2(umax_u16x2(ww[0] ^ 0x80008000u, ww[1] ^ 0x80008000u),
+                                        umax_u16x2(ww[2] ^ 0x80008000u, ww[3] ^ 0x80008000u));
+          const uint32_t a = umax_u16x2(umax_u16x2(ww[0] & 0x7FFF7FFFu, ww[1] & 0x7FFF7FFFu),
+                                        umax_u16x2(ww[2] & 0x7FFF7FFFu, ww[3] & 0x7FFF7FFFu));
+          const bool any_nan = (a & 0xFFFFu) > 0x7F80u || (a >> 16) > 0x7F80u;
+          if (!any_nan && (m & 0xFFFFu) < pivot && (m >> 16) < pivot) continue;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint16_t h = static_cast<uint16_t>((e & 1) ? (ww[e >> 1] >> 16) : (ww[e >> 1] & 0xFFFFu));
+          if (c < n8 && key16(h) >= pivot) take |= 1u << (8 * j + e);
+        }
+      }
+      append(take, [&](int t) { return 8 * (c0 + (t >> 3) * kSelThreads + tid) + (t & 7); });
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = wn[j];
+    }
+  } else {
+    for (int64_t v0 = 0; v0 < V; v0 += 32 * kSelThreads) {
+      uint32_t take = 0;  // bit t: entry v0 + t kSelThreads + tid
+#pragma unroll
+      for (int t = 0; t < 32; ++t) {
+        const int64_t v = v0 + static_cast<int64_t>(t) * kSelThreads + tid;
+        if (v < V && key16(x[v]) >= pivot) take |= 1u << t;
+      }
+      append(take, [&](int t) { return v0 + static_cast<int64_t>(t) * kSelThreads + tid; });
+    }
+  }
+  __syncthreads();
+  const int n = *n_col;
+  bool exact = n < k || n > kSelCap;
+
+  // 3. k-th largest key T on the list (two byte passes)
+  uint32_t T = 0;
+  int above = 0, n_eq = 0;
+  if (!exact) {
+    uint32_t prefix = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+      for (int t = tid; t < 256; t += kSelThreads) hist[t] = 0;
+      __syncthreads();
+      for (int e = tid; e < n; e += kSelThreads) {
+        const uint32_t kk = lkey[e];
+        if (pass == 0) atomicAdd(&hist[kk >> 8], 1);
+        else if ((kk >> 8) == prefix) atomicAdd(&hist[kk & 0xFFu], 1);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        int acc = above, bin = 0;
+        for (int h = 255; h >= 0; --h) {
+          if (acc + hist[h] >= k) { bin = h; break; }
+          acc += hist[h];
+        }
+        sel[2] = bin;
+        sel[3] = acc;
+        sel[4] = hist[bin];
+      }
+      __syncthreads();
+      prefix = pass == 0 ? static_cast<uint32_t>(sel[2]) : ((prefix << 8) | static_cast<uint32_t>(sel[2]));
+      above = sel[3];
+      n_eq = sel[4];
+      __syncthreads();
+    }
+    T = prefix;
+    if (n_eq > k - above && n_eq > kSelTies) exact = true;
+  }
+  if (exact) {
+    select_exact(x, V, k, out, hist, scan_sh, sel);
+    return;
+  }
+  const int need_eq = k - above;  // 1 <= need_eq <= n_eq
+
+  // 4. output: every key above T, and the need_eq smallest indices among keys == T
+  int* n_out = sel + 5;
+  int* n_tie = sel + 6;
+  if (tid == 0) { *n_out = 0; *n_tie = 0; }
+  __syncthreads();
+  uint32_t* ties = reinterpret_cast<uint32_t*>(hist);  // reused: [kSelTies]
+  const bool all_ties = need_eq == n_eq;
+  for (int e0 = 0; e0 < n; e0 += kSelThreads) {
+    const int e = e0 + tid;
+    const uint32_t kk = e < n ? lkey[e] : 0u;
+    const bool take = e < n && (kk > T || (kk == T && all_ties));
+    const int pos = warp_append(take ? 1 : 0, n_out);
+    if (take && pos < k) out[pos] = static_cast<int32_t>(lidx[e]);
+    if (!all_ties) {
+      const bool tie = e < n && kk == T;
+      const int tp = warp_append(tie ? 1 : 0, n_tie);
+      if (tie) ties[tp] = lidx[e];
+    }
+  }
+  __syncthreads();
+  if (!all_ties) {
+    for (int e = tid; e < n_eq; e += kSelThreads) {
+      const uint32_t me = ties[e];
+      int rank = 0;
+      for (int f = 0; f < n_eq; ++f) rank += ties[f] < me ? 1 : 0;
+      if (rank < need_eq && *n_out + rank < k) out[*n_out + rank] = static_cast<int32_t>(me);
+    }
   }
 }
 
@@ -289,7 +523,15 @@ const void* topk_walk_kernel_ptr(bool prob, bool logits) {
 
 cudaError_t launch_topk_select(const uint16_t* base, int64_t V, int k, int rows, int32_t* cand,
                                uint16_t* logits, cudaStream_t stream) {
-  topk_select_kernel<<<rows, kSelThreads, 0, stream>>>(base, V, k, cand, logits);
+  constexpr size_t smem = kSelBins * 4 + kSelCap * 6 + 96 * 4;
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  topk_select_kernel<<<rows, kSelThreads, smem, stream>>>(base, V, k, cand, logits);
   return cudaGetLastError();
 }
 
