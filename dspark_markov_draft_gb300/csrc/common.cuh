@@ -206,7 +206,8 @@ __device__ __forceinline__ bool exchange_best(const StepSync& s, int i, int bs,
   if (threadIdx.x == 0) {
     bool failed = false;
     uint32_t* ctr = s.counter(i);
-    __threadfence();
+    // the release add is cumulative: the CTA barrier above orders every thread's
+    // atomicMax before it, so no separate fence is needed
     if (!skip_arrival) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
     uint64_t t0 = 0;
     uint32_t it = 0;
