@@ -344,7 +344,7 @@ def cpu_baseline(cfg, target_s: float = 12.0):
     runner = OracleRunner(cfg, cfg["bs"])
     t1 = runner.run(1, cores)
     rows = int(min(cfg["bs"], max(1, target_s / max(t1, 1e-6))))
-    reps = 1 if rows < cfg["bs"] else int(min(5, max(1, target_s / max(rows * t1, 1e-6))))
+    reps = 1 if rows < cfg["bs"] else int(min(20, max(1, target_s / max(rows * t1, 1e-6))))
     dt = sum(runner.run(rows, cores) for _ in range(reps))
     toks = reps * rows * cfg["K"]
     return {"value": toks / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
