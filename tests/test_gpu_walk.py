@@ -358,11 +358,13 @@ FULL = [
     (151936, 7, 1, True, capi.GREEDY, 1.0, 8.0, False, [0]),
     (151936, 7, 1, True, capi.PROBABILISTIC, 1.0, 8.0, False, [0]),
     (151936, 7, 16, True, capi.GREEDY, 1.0, 8.0, False, [0, 7, 15]),
+    (151936, 7, 16, True, capi.PROBABILISTIC, 1.0, 8.0, False, [3, 12]),
     (151936, 7, 64, True, capi.GREEDY, 1.0, 8.0, False, [0, 33, 63]),
     (151936, 7, 64, True, capi.PROBABILISTIC, 1.0, 8.0, False, [1, 62]),
     (151936, 16, 1, False, capi.PROBABILISTIC, 0.7, 8.0, True, [0]),
     (151936, 16, 64, False, capi.PROBABILISTIC, 0.7, 8.0, True, [0, 63]),
     (248320, 16, 1, True, capi.GREEDY, 1.0, None, False, [0]),
+    (248320, 16, 16, True, capi.GREEDY, 1.0, None, False, [2, 14]),
     (248320, 16, 64, True, capi.GREEDY, 1.0, None, False, [5, 60]),
 ]
 
