@@ -16,6 +16,7 @@ namespace dspark {
 const void* walk_cc_kernel_ptr(bool int8, bool prob, bool logits);
 const void* walk_tc_kernel_ptr(bool int8, bool prob, bool logits, int nq);
 const void* topk_walk_kernel_ptr(bool prob, bool logits);
+size_t topk_walk_smem(int bs);
 cudaError_t launch_topk_select(const uint16_t* base, int64_t V, int k, int rows, int32_t* cand,
                                uint16_t* logits, cudaStream_t stream);
 cudaError_t launch_quantize_w2(const uint16_t* w2, int64_t V, int8_t* q, float* scales,
@@ -338,7 +339,7 @@ int32_t dspark_walk_topk(const dspark_walk_args* a, dspark_stream_t stream) {
   cudaError_t e = launch_topk_select(a->base_logits, a->V, a->top_k, rows,
                                      const_cast<int32_t*>(p.cand), a->draft_logits, s);
   if (e != cudaSuccess) return cuda_fail(e, "topk_select_kernel launch");
-  const size_t smem = static_cast<size_t>(a->bs) * kRank * 4 + 64 * 4 + 64 * 8 + kWalkWarps * 8 + 64 + 256;
+  const size_t smem = topk_walk_smem(a->bs);
   const bool prob = a->mode == DSPARK_PROBABILISTIC, lg = a->draft_logits != nullptr;
   const void* fn = topk_walk_kernel_ptr(prob, lg);
   return launch_coop(fn, caps.sms, kWalkThreads, smem, p, s);

@@ -195,6 +195,41 @@ __device__ __forceinline__ void give_up(const StepSync& s) {
 // wall-clock time and watches the workspace abort flag; on either, the wait gives up
 // and false is returned (the same value in every thread), and the caller returns from
 // the kernel.
+// The exchange in two halves, for kernels with work to do while the grid arrives:
+// exchange_arrive publishes this CTA's words and arrives at the step counter;
+// exchange_wait waits for the grid and reads the winners back.
+__device__ __forceinline__ void exchange_arrive(const StepSync& s, int i, int bs, bool skip_arrival,
+                                                const uint64_t* best_s) {
+  __syncthreads();
+  if (threadIdx.x < bs && best_s[threadIdx.x] != 0ull)
+    atomicMax(reinterpret_cast<unsigned long long*>(s.slots + static_cast<size_t>(i) * bs + threadIdx.x),
+              static_cast<unsigned long long>(best_s[threadIdx.x]));
+  __syncthreads();
+  if (threadIdx.x == 0 && !skip_arrival)
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(s.counter(i)) : "memory");
+}
+__device__ __forceinline__ bool exchange_wait(const StepSync& s, int i, int bs, uint64_t* best_s,
+                                              int* sh_flag) {
+  if (threadIdx.x == 0) {
+    bool failed = false;
+    uint32_t* ctr = s.counter(i);
+    uint64_t t0 = 0;
+    uint32_t it = 0;
+    while (ld_acquire_u32(ctr) < s.grid) {
+      if ((++it & 63u) != 0u) continue;
+      if (t0 == 0) t0 = globaltimer_ns();
+      if (*reinterpret_cast<volatile uint32_t*>(&s.hdr->abort) != 0u) { failed = true; break; }
+      if (globaltimer_ns() - t0 > s.timeout_ns) { give_up(s); failed = true; break; }
+    }
+    *sh_flag = failed ? 0 : 1;
+  }
+  __syncthreads();
+  if (*sh_flag == 0) return false;
+  if (threadIdx.x < bs) best_s[threadIdx.x] = ld_relaxed_u64(s.slots + static_cast<size_t>(i) * bs + threadIdx.x);
+  __syncthreads();
+  return true;
+}
+
 __device__ __forceinline__ bool exchange_best(const StepSync& s, int i, int bs,
                                               bool skip_arrival, uint64_t* best_s,
                                               int* sh_flag) {

@@ -374,18 +374,25 @@ __global__ void __launch_bounds__(kSelThreads, 3) topk_select_kernel(const uint1
   }
 }
 
+constexpr int kChunk = 2048;  // candidates per chunk of a CTA (its whole range at the configs)
+
 template <bool PROB, bool LOGITS>
 __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int G = gridDim.x, cta = blockIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int j8 = lane & 7, grp = lane >> 3;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int j8 = lane & 7, grp = tid >> 3;                     // 64 groups of 8 lanes
+  constexpr int kGroups = kWalkThreads / 8;
   float* e_s = reinterpret_cast<float*>(smem);                 // [bs][256] fp32
-  int* prev_s = reinterpret_cast<int*>(e_s + static_cast<size_t>(p.bs) * kRank);
-  uint64_t* best_s = reinterpret_cast<uint64_t*>(prev_s + 64);
-  uint64_t* red = best_s + 64;
-  int* flag = reinterpret_cast<int*>(red + kWalkWarps);
+  int32_t* it_v = reinterpret_cast<int32_t*>(e_s + static_cast<size_t>(p.bs) * kRank);  // [kChunk]
+  float* it_base = reinterpret_cast<float*>(it_v + kChunk);    // [kChunk] base logit
+  float* it_g = it_base + kChunk;                              // [kChunk] Gumbel noise
+  int* prev_s = reinterpret_cast<int*>(it_g + kChunk);         // [64]
+  uint64_t* best_s = reinterpret_cast<uint64_t*>(prev_s + 64); // [64]
+  int* flag = reinterpret_cast<int*>(best_s + 64);
 
+  // This CTA's candidates: a contiguous range of the bs * k (row, candidate) items,
+  // walked in chunks of at most kChunk items.
   const int64_t items = static_cast<int64_t>(p.bs) * p.top_k;
   const int64_t lo = static_cast<int64_t>(cta) * items / G;
   const int64_t hi = static_cast<int64_t>(cta + 1) * items / G;
@@ -393,17 +400,50 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
   const unsigned char* w2g = reinterpret_cast<const unsigned char*>(p.w2);
   constexpr int kRowBytes = 2 * kRank;
 
-  for (int t = threadIdx.x; t < p.bs; t += blockDim.x) {
+  for (int t = tid; t < p.bs; t += blockDim.x) {
     const int32_t tok = p.prev[t];
     const bool ok = tok >= 0 && static_cast<int64_t>(tok) < p.V;
     prev_s[t] = ok ? tok : -1;
     if (!ok && cta == 0) report(p.sync.status_dev, DSPARK_ERR_BAD_TOKEN);
   }
 
+  // Phase P of position i for the chunk [c_lo, c_hi): everything that does not depend on
+  // the previous token -- candidate id, base logit, Gumbel noise -- and the W2 row
+  // towards L2.
+  auto phase_p = [&](int i, int64_t c_lo, int64_t c_hi) {
+    for (int64_t it = c_lo + tid; it < c_hi; it += blockDim.x) {
+      const int e = static_cast<int>(it - c_lo);
+      const int b = static_cast<int>(it / p.top_k);
+      const int64_t j = it - static_cast<int64_t>(b) * p.top_k;
+      const int64_t v = min(max(static_cast<int64_t>(p.cand[(static_cast<size_t>(b) * p.K + i) * p.top_k + j]),
+                                int64_t{0}), p.V - 1);
+      it_v[e] = static_cast<int32_t>(v);
+      it_base[e] = bf16_to_f32(__ldg(p.base + (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v));
+      float g = 0.f;
+      if constexpr (PROB) {
+        const uint4 w = philox_block(p.seeds[b], b, i, static_cast<uint32_t>(v >> 2));
+        g = gumbel_from_word(uint4_get(w, static_cast<int>(v & 3)));
+      }
+      it_g[e] = g;
+      const unsigned char* row = w2g + static_cast<size_t>(v) * kRowBytes;
+#pragma unroll
+      for (int m = 0; m < kRowBytes / 128; ++m) prefetch_l2(row + 128 * m);
+    }
+  };
+
+  bool have_p = false;  // phase P of the first chunk of position i already done
+  if (lo < hi) {
+    phase_p(0, lo, min(hi, lo + kChunk));
+    have_p = true;
+  }
+
   for (int i = 0; i < p.K; ++i) {
     __syncthreads();
-    for (int t = threadIdx.x; t < p.bs; t += blockDim.x) best_s[t] = 0ull;
-    for (int b = warp; b < p.bs; b += kWalkWarps) {
+    for (int t = tid; t < p.bs; t += blockDim.x) best_s[t] = 0ull;
+    // embeddings of the rows this CTA touches, as fp32
+    const int b_first = lo < hi ? static_cast<int>(lo / p.top_k) : 0;
+    const int b_last = lo < hi ? static_cast<int>((hi - 1) / p.top_k) : -1;
+    for (int b = b_first + warp; b <= b_last; b += kWalkWarps) {
       const int tok = prev_s[b];
       if (tok < 0) continue;
       const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.w1 + static_cast<size_t>(tok) * kRank) + lane);
@@ -417,91 +457,137 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
     }
     __syncthreads();
 
-    const int b_first = lo < hi ? static_cast<int>(lo / p.top_k) : 0;
-    const int b_last = lo < hi ? static_cast<int>((hi - 1) / p.top_k) : -1;
-    for (int b = b_first; b <= b_last; ++b) {
-      if (prev_s[b] < 0) continue;
-      const int64_t j_lo = max(lo, static_cast<int64_t>(b) * p.top_k) - static_cast<int64_t>(b) * p.top_k;
-      const int64_t j_hi = min(hi, static_cast<int64_t>(b + 1) * p.top_k) - static_cast<int64_t>(b) * p.top_k;
-      const int32_t* cand = p.cand + (static_cast<size_t>(b) * p.K + i) * p.top_k;
-      const uint64_t seed = PROB ? p.seeds[b] : 0ull;
+    // Phase D: tasks of up to 8 consecutive candidates of one request row; group g of
+    // 8 lanes takes tasks g, g + 64, ...; each lane holds 32 of the 256 positions.
+    for (int64_t c_lo = lo; c_lo < hi; c_lo += kChunk) {
+      const int64_t c_hi = min(hi, c_lo + kChunk);
+      if (!have_p) {
+        phase_p(i, c_lo, c_hi);
+        __syncthreads();
+      }
+      have_p = false;
+      // tasks: the chunk split at row boundaries into runs of 8
+      const int b0 = static_cast<int>(c_lo / p.top_k);
+      const int64_t first_end = min(c_hi, static_cast<int64_t>(b0 + 1) * p.top_k);  // end of the first row's run
+      const int n0 = static_cast<int>(first_end - c_lo);
+      const int t0 = (n0 + 7) / 8;                                          // tasks of the first row
+      const int ntask = t0 + static_cast<int>((c_hi - first_end + 7) / 8 +
+                                              (c_hi - first_end) / p.top_k + 1);  // upper bound
+      int cur_b = -1;
       float ef[32];
+      for (int task = grp; task < ntask; task += kGroups) {
+        // task -> [e0, e1) in chunk numbering, all in row b
+        int64_t s0;
+        int b;
+        int64_t e_end;
+        if (task < t0) {
+          s0 = c_lo + 8 * task;
+          b = b0;
+          e_end = first_end;
+        } else {
+          // later rows start at first_end; each row has k candidates (the last may be cut)
+          const int64_t kk = p.top_k;
+          const int64_t tasks_per_row = (kk + 7) / 8;
+          const int64_t rt = task - t0;
+          const int64_t rrow = rt / tasks_per_row;
+          const int64_t rstart = first_end + rrow * kk;
+          s0 = rstart + 8 * (rt - rrow * tasks_per_row);
+          b = b0 + 1 + static_cast<int>(rrow);
+          e_end = min(c_hi, rstart + kk);
+        }
+        if (s0 >= e_end) continue;  // past the chunk (uniform per group)
+        if (prev_s[b] < 0) continue;
+        const int e0 = static_cast<int>(s0 - c_lo);
+        const int nt = static_cast<int>(e_end - s0 < 8 ? e_end - s0 : 8);
+        if (b != cur_b) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) ef[c] = e_s[static_cast<size_t>(b) * kRank + (j8 + 8 * (c / 8)) * 8 + (c % 8)];
-
-      uint64_t best = 0ull;
-      for (int64_t r0 = j_lo + 32 * warp; r0 < j_hi; r0 += 32 * kWalkWarps) {
-        const int64_t rbase = r0 + 8 * grp;
+          for (int c = 0; c < 4; ++c) {
+            const float4 lo4 = *reinterpret_cast<const float4*>(e_s + static_cast<size_t>(b) * kRank + (j8 + 8 * c) * 8);
+            const float4 hi4 = *reinterpret_cast<const float4*>(e_s + static_cast<size_t>(b) * kRank + (j8 + 8 * c) * 8 + 4);
+            ef[8 * c + 0] = lo4.x; ef[8 * c + 1] = lo4.y; ef[8 * c + 2] = lo4.z; ef[8 * c + 3] = lo4.w;
+            ef[8 * c + 4] = hi4.x; ef[8 * c + 5] = hi4.y; ef[8 * c + 6] = hi4.z; ef[8 * c + 7] = hi4.w;
+          }
+          cur_b = b;
+        }
         float part[8];
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr) {
-          const int64_t r = rbase + rr;
-          float a = 0.f;
-          if (r < j_hi) {
-            const int64_t cv = min(max(static_cast<int64_t>(cand[r]), int64_t{0}), p.V - 1);
-            const unsigned char* row = w2g + static_cast<size_t>(cv) * kRowBytes;
+        for (int h = 0; h < 2; ++h) {  // two batches of 4 rows: 16 loads in flight per lane
+          uint4 q[4][4];
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            const int r = 4 * h + rr;
+            const unsigned char* row = w2g + static_cast<size_t>(it_v[e0 + min(r, nt - 1)]) * kRowBytes;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              q[rr][c] = r < nt ? __ldg(reinterpret_cast<const uint4*>(row) + j8 + 8 * c) : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            float a = 0.f;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-              const uint4 q = __ldg(reinterpret_cast<const uint4*>(row) + j8 + 8 * c);
-              const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+              const uint32_t qw[4] = {q[rr][c].x, q[rr][c].y, q[rr][c].z, q[rr][c].w};
 #pragma unroll
               for (int w = 0; w < 4; ++w) {
                 a = __fmaf_rn(bf16_lo(qw[w]), ef[8 * c + 2 * w], a);
                 a = __fmaf_rn(bf16_hi(qw[w]), ef[8 * c + 2 * w + 1], a);
               }
             }
+            part[4 * h + rr] = a;
           }
-          part[rr] = a;
         }
-        // butterfly over the 8 lanes of the group (same tree as the dense walk)
+        // butterfly over the 8 lanes of the group: lane j8 ends with candidate e0 + j8
+        const unsigned gmask = 0xFFu << (lane & 24);
         const bool u4 = lane & 4, u2 = lane & 2, u1 = lane & 1;
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const float send = u4 ? part[t] : part[t + 4];
           const float keep = u4 ? part[t + 4] : part[t];
-          part[t] = keep + __shfl_xor_sync(kFull, send, 4);
+          part[t] = keep + __shfl_xor_sync(gmask, send, 4);
         }
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const float send = u2 ? part[t] : part[t + 2];
           const float keep = u2 ? part[t + 2] : part[t];
-          part[t] = keep + __shfl_xor_sync(kFull, send, 2);
+          part[t] = keep + __shfl_xor_sync(gmask, send, 2);
         }
         const float send = u1 ? part[0] : part[1];
         const float keep = u1 ? part[1] : part[0];
-        const float bias = keep + __shfl_xor_sync(kFull, send, 1);
+        const float bias = keep + __shfl_xor_sync(gmask, send, 1);
 
-        const int64_t r = rbase + j8;
-        if (r < j_hi) {
-          const int64_t v = min(max(static_cast<int64_t>(cand[r]), int64_t{0}), p.V - 1);
-          const size_t o = (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v;
-          const float l = __fadd_rn(bf16_to_f32(p.base[o]), bias);
-          if (LOGITS) p.logits[o] = f32_to_bf16_bits(l);
-          float s = l;
-          if (PROB) {
-            const float lb = bf16_to_f32(f32_to_bf16_bits(l));
+        if (j8 < nt) {
+          const int e = e0 + j8;
+          const int64_t v = it_v[e];
+          const float l = __fadd_rn(it_base[e], bias);
+          const uint16_t lh = f32_to_bf16_bits(l);
+          if (LOGITS) p.logits[(static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v] = lh;
+          float sco = l;
+          if constexpr (PROB) {
+            const float lb = bf16_to_f32(lh);
             const float xs = p.temp_is_one ? lb : __fdiv_rn(lb, p.temperature);
-            const uint4 w = philox_block(seed, b, i, static_cast<uint32_t>(v >> 2));
-            s = __fadd_rn(xs, gumbel_from_word(uint4_get(w, static_cast<int>(v & 3))));
+            sco = __fadd_rn(xs, it_g[e]);
           }
-          best = umax64(best, pack_best(order_key(s), static_cast<uint32_t>(v)));
+          atomicMax(reinterpret_cast<unsigned long long*>(&best_s[b]),
+                    static_cast<unsigned long long>(pack_best(order_key(sco), static_cast<uint32_t>(v))));
         }
       }
-      best = warp_max64(best);
-      if (lane == 0) red[warp] = best;
-      __syncthreads();
-      if (warp == 0) {
-        uint64_t xw = lane < kWalkWarps ? red[lane] : 0ull;
-        xw = warp_max64(xw);
-        if (lane == 0) best_s[b] = umax64(best_s[b], xw);
-        if (xw != 0ull && lane < 4 && i + 1 < p.K)
-          prefetch_l2(p.w1 + static_cast<size_t>(unpack_idx(xw)) * kRank + 64 * lane);
-      }
-      __syncthreads();
+      __syncthreads();  // the chunk's item arrays are free again
     }
 
-    if (!exchange_best(p.sync, i, p.bs, skip0 && i == 0, best_s, flag)) return;
-    for (int t = threadIdx.x; t < p.bs; t += blockDim.x) {
+    // Prefetch the CTA winners' embedding rows, publish, do the next position's first
+    // phase P while the grid arrives, then read the winners back.
+    if (tid < p.bs && best_s[tid] != 0ull && i + 1 < p.K) {
+      const uint16_t* row = p.w1 + static_cast<size_t>(unpack_idx(best_s[tid])) * kRank;
+#pragma unroll
+      for (int l4 = 0; l4 < 4; ++l4) prefetch_l2(row + 64 * l4);
+    }
+    exchange_arrive(p.sync, i, p.bs, skip0 && i == 0, best_s);
+    if (i + 1 < p.K && lo < hi) {
+      phase_p(i + 1, lo, min(hi, lo + kChunk));
+      have_p = true;
+    }
+    if (!exchange_wait(p.sync, i, p.bs, best_s, flag)) return;
+    for (int t = tid; t < p.bs; t += blockDim.x) {
       int tok = -1;
       if (prev_s[t] >= 0) {
         const uint64_t w = best_s[t];
@@ -514,6 +600,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
     reset_behind(p.sync, i, p.bs);
   }
   finish_walk(p.sync, p.K, p.bs, flag);
+}
+
+size_t topk_walk_smem(int bs) {
+  return static_cast<size_t>(bs) * kRank * 4 + 3 * kChunk * 4 + 64 * 4 + 64 * 8 + 16 + 128;
 }
 
 const void* topk_walk_kernel_ptr(bool prob, bool logits) {
