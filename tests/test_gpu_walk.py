@@ -302,6 +302,33 @@ def test_topk_small_parity(oracle, k, mode, T):
     check_walk(oracle, inp, tokens, mode=mode, T=T, top_k=k, gpu_logits=lg)
 
 
+@pytest.mark.parametrize("case", ["sampled", "ranked_ties", "wide_tie", "overflow"])
+def test_topk_select_paths(oracle, case):
+    """Every path of the candidate selection gives the oracle's candidate set (draft_logits
+    are -inf exactly off the candidates) and tokens: a list collected above a sampled
+    pivot; a boundary tie ranked by index; a tie too wide to rank and a list too long
+    for shared memory, both taking the exact whole-row selection."""
+    V, K, bs = 20000, 2, 2  # V a multiple of 8: 16-byte row loads
+    inp = synth.make(V, bs, K, seed=41)
+    g = torch.Generator().manual_seed(7)
+    base = inp.base.float()
+    k = 300
+    if case == "ranked_ties":  # 500 equal top keys, 300 of them taken by index
+        base[:, :, torch.randperm(V, generator=g)[:500]] = 12.0
+    elif case == "wide_tie":  # 3000 equal top keys, 1000 taken
+        base[:, :, torch.randperm(V, generator=g)[:3000]] = 12.0
+        k = 1000
+    elif case == "overflow":  # every key equal
+        base[:] = 1.0
+    inp.base = base.bfloat16()
+    w1, w2, basedev, prev, seeds = to_dev(inp)
+    for mode in (capi.GREEDY, capi.PROBABILISTIC):
+        tokens, lg = capi.walk(basedev, w1, prev, w2=w2, seeds=seeds, mode=mode, top_k=k,
+                               want_logits=True)
+        torch.cuda.synchronize()
+        check_walk(oracle, inp, tokens, mode=mode, top_k=k, gpu_logits=lg)
+
+
 def test_topk_full_vocab_equals_dense():
     V, K, bs = 2003, 4, 3
     inp = synth.make(V, bs, K, seed=31)
