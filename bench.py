@@ -297,6 +297,21 @@ def time_e2e(cfg, t, args, steps, dev):
     return ms, h2d, d2h
 
 
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The slowest replica's time (every rank walks its own batch; the job ends with the
+    slowest one)."""
+    if dist is None:
+        return ms
+    x = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(x, op=dist.ReduceOp.MAX)
+    return float(x.item())
+
+
+def job_throughput(ms_max: float, world: int, tokens_per_rank: int) -> float:
+    """Draft tokens/s of the whole job: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (ms_max * 1e-3)
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -470,13 +485,9 @@ def main():
         wall = time.perf_counter() - wall0
     if dist:
         dist.barrier()
-    ms = statistics.mean(times)
-    if dist:
-        x = torch.tensor([ms], device=dev)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        ms = float(x.item())
+    ms = max_over_ranks(statistics.mean(times), dist, dev)
     toks = cfg["bs"] * cfg["K"]
-    value = world * toks / (ms * 1e-3)
+    value = job_throughput(ms, world, toks)
 
     e2e_ms, h2d, d2h = (float("nan"), 0, 0) if a.no_e2e else time_e2e(cfg, t, args, max(3, a.steps // 2), dev)
     fl, res_rows = floors_of(cfg)
