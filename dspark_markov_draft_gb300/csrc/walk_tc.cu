@@ -539,6 +539,8 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
       // combined once per position. The base logits of the warp's rows and columns are
       // staged in shared memory one tile ahead.
       constexpr int CHG = NC < 8 ? NC : (PROB ? 4 : 8);
+      static_assert(NC % CHG == 0, "the column chunks must tile the warp's columns");
+      static_assert(!PROB || CHG % 4 == 0, "Philox blocks are drawn for groups of 4 columns");
       const int cb = half * NC;                                 // first column of the warp
       const int ncol = max(0, min(NC, p.bs - cb));              // live columns (uniform)
       const int ew = warp - 8;
@@ -717,6 +719,7 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
       // per column: (orderable key, first index) maximum over the warp's 32 rows
       const uint32_t vlane = static_cast<uint32_t>(v0) + 32u * q + lane;
       constexpr int RG = NC < 16 ? NC : 16;  // columns per reduction group (register budget)
+      static_assert(NC % RG == 0 && (RG & (RG - 1)) == 0, "reduction groups: a power of two tiling NC");
 #pragma unroll
       for (int g0 = 0; g0 < NC; g0 += RG) {
         uint64_t x[RG];
