@@ -94,15 +94,15 @@ def hbm_bytes(cfg) -> float:
 
 
 def uses_tensor_cores(cfg) -> bool:
-    return cfg["top_k"] == 0 and cfg["bs"] >= 2
+    return cfg["top_k"] == 0 and cfg["bs"] >= 3
 
 
 def floors(cfg, peaks, sms: int, resident_rows: int, l2_gbs: float):
     """Lower bounds (µs) of one walk, per resource. Memory: HBM (W2 once, base logits,
     outputs), shared memory (the resident W2 rows read at every position), L2 (the
     streamed W2 rows at positions 1..K-1). Contraction: 2 V 256 bs K flops on the
-    tensor cores (bs >= 2), or the dp4a / fp32 FMA instructions of the CUDA-core
-    contraction (bs = 1). The roofline is the slowest of them."""
+    tensor cores (bs >= 3), or the dp4a / fp32 FMA instructions of the CUDA-core
+    contraction (bs <= 2). The roofline is the slowest of them."""
     V, K, bs = cfg["V"], cfg["K"], cfg["bs"]
     clk = peaks["sm_mhz"] * 1e6
     out = {"hbm_us": hbm_bytes(cfg) / (peaks["hbm_gbs"] * 1e9) * 1e6}

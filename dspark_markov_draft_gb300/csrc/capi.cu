@@ -97,7 +97,7 @@ Plan plan_dense(const DeviceCaps& caps, int64_t V, bool int8, int bs, int cap_ro
 }
 
 // Smallest batch that takes the tensor-core contraction by default.
-constexpr int kTcMinBs = 2;
+constexpr int kTcMinBs = 3;
 
 struct TcPlan {
   int grid;

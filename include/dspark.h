@@ -159,7 +159,7 @@ size_t dspark_walk_workspace_size(int64_t V, int32_t bs, int32_t K, int32_t top_
 
 /*
  * Launch plan dspark_walk takes by default on `device` for this batch size (CUDA-core
- * contraction at bs = 1, tensor cores from bs = 2): cooperative grid size (CTAs) and
+ * contraction at bs <= 2, tensor cores from bs = 3): cooperative grid size (CTAs) and
  * the number of W2 rows kept resident in shared memory over the whole grid (greedy
  * plan; a probabilistic tensor-core walk keeps a few more). Queries
  * the device once and caches it (the only host-synchronous work of the library).
