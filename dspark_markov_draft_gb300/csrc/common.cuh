@@ -78,7 +78,10 @@ __device__ __forceinline__ float neg_log_unit(float u) {
 // g = -ln(-ln(u)): the inner logarithm as above, the outer one (argument in
 // [6e-8, 16.7]) from the hardware base-2 logarithm, absolute error below 5e-6.
 __device__ __forceinline__ float gumbel_from_word(uint32_t w) {
-  const float u = static_cast<float>(2u * (w >> 9) + 1u) * 5.9604644775390625e-08f;
+  // (1 + x 2^-23) - 1 is exact (both in [1, 2)) and adding 2^-24 to x 2^-23 is exact for
+  // x < 2^23, so this is the same u without an integer-to-float conversion.
+  const float f = __uint_as_float(0x3F800000u | (w >> 9));
+  const float u = __fadd_rn(__fsub_rn(f, 1.0f), 5.9604644775390625e-08f);
   float l2;
   asm("lg2.approx.f32 %0, %1;" : "=f"(l2) : "f"(neg_log_unit(u)));
   return -l2 * 0.693147180559945f;
