@@ -82,15 +82,14 @@ __device__ __forceinline__ void mma_commit(uint64_t* mbar) {
                ::"r"(smem_u32(mbar)) : "memory");
 }
 
-// Longest time (ns) one try_wait may suspend the thread before it returns false; the
-// thread wakes as soon as the phase completes, so waiting costs no issue slots.
-constexpr uint32_t kSuspendHintNs = 1000000;
-
+// One try_wait suspends the thread for up to a hardware-chosen time and returns false
+// if the phase has not completed by then. No suspend-time hint: with one, a waiting
+// thread took ~200 cycles to resume after the completing arrival, ~125 without.
 __device__ __forceinline__ bool mbar_try(uint64_t* mbar, uint32_t parity) {
   uint32_t done;
   asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
-      : "=r"(done) : "r"(smem_u32(mbar)), "r"(parity), "r"(kSuspendHintNs) : "memory");
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
   return done != 0;
 }
 
@@ -717,20 +716,40 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
       if (LOGITS && ltma && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
       asm volatile("cp.async.wait_all;" ::: "memory");
       // per column: (orderable key, first index) maximum over the warp's 32 rows
-      const uint32_t vlane = static_cast<uint32_t>(v0) + 32u * q + lane;
-      constexpr int RG = NC < 16 ? NC : 16;  // columns per reduction group (register budget)
-      static_assert(NC % RG == 0 && (RG & (RG - 1)) == 0, "reduction groups: a power of two tiling NC");
+      if constexpr (NC <= 8) {
+        // few columns: one warp-wide integer max of the keys per column; the first
+        // index among the lanes that reach it is the smallest (tile, lane)
 #pragma unroll
-      for (int g0 = 0; g0 < NC; g0 += RG) {
-        uint64_t x[RG];
-#pragma unroll
-        for (int k = 0; k < RG; ++k) {
-          const int j = g0 + k;
+        for (int j = 0; j < NC; ++j) {
+          if (j >= ncol) break;
+          const uint32_t key = order_key(bv[j]);
+          const uint32_t kmax = __reduce_max_sync(kFull, key);
+          const uint32_t cand = __ballot_sync(kFull, key == kmax);
           const uint32_t tj = (bt[j >> 2] >> (8 * (j & 3))) & 0xFFu;
-          x[k] = j < ncol ? pack_best(order_key(bv[j]), vlane + tj * kTile) : 0ull;
+          uint32_t pos = key == kmax ? ((tj << 5) | static_cast<uint32_t>(lane)) : 0xFFFFFFFFu;
+          if (__popc(cand) > 1) pos = __reduce_min_sync(kFull, pos);
+          else pos = __shfl_sync(kFull, pos, __ffs(cand) - 1);
+          if (lane == 0)
+            red_s[q * 64 + cb + j] =
+                pack_best(kmax, static_cast<uint32_t>(v0) + 32u * q + (pos & 31u) + (pos >> 5) * kTile);
         }
-        const uint64_t xm = column_max_scatter<RG>(x, lane);
-        if (lane < RG && g0 + lane < ncol) red_s[q * 64 + cb + g0 + lane] = xm;
+      } else {
+        // many columns: packed words, reduce-scattered across the lanes
+        const uint32_t vlane = static_cast<uint32_t>(v0) + 32u * q + lane;
+        constexpr int RG = NC < 16 ? NC : 16;  // columns per reduction group (register budget)
+        static_assert(NC % RG == 0 && (RG & (RG - 1)) == 0, "reduction groups: a power of two tiling NC");
+#pragma unroll
+        for (int g0 = 0; g0 < NC; g0 += RG) {
+          uint64_t x[RG];
+#pragma unroll
+          for (int k = 0; k < RG; ++k) {
+            const int j = g0 + k;
+            const uint32_t tj = (bt[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+            x[k] = j < ncol ? pack_best(order_key(bv[j]), vlane + tj * kTile) : 0ull;
+          }
+          const uint64_t xm = column_max_scatter<RG>(x, lane);
+          if (lane < RG && g0 + lane < ncol) red_s[q * 64 + cb + g0 + lane] = xm;
+        }
       }
     }
     g_base += T;
