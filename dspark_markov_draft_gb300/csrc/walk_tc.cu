@@ -17,8 +17,9 @@
 //     conflict-free for this access), brought in at position 0 with cp.async; the
 //     rest are re-read from L2.
 //   * D[128 x N] = A . B^T accumulates in fp32 in tensor memory. One thread issues an
-//     MMA only about every 70 cycles whatever N is, so the K range is split in two
-//     halves issued by two threads into two accumulators, which the epilogue adds.
+//     MMA only about every 50 cycles whatever N is (up to 128), so the K range is
+//     split in two halves issued by two threads into two accumulators, which the
+//     epilogue adds.
 //   * Epilogue (8 warps): thread = tensor-memory lane = one vocabulary row of the
 //     tile, for N/2 request rows. It adds the two K-half accumulators, forms
 //     l = base + scale_v 2^-s D (base logits staged one tile ahead by a tensor-map
