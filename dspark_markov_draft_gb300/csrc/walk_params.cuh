@@ -92,7 +92,7 @@ __host__ __device__ inline size_t walk_tc_misc_smem() {
          + 64 * 8        // per-row argmax words
          + 4 * 64 * 8    // per-quadrant argmax words
          + 2 * 8         // 2^-s as two factors
-         + 28 * 8 + 16;  // mbarriers, TMEM base, flag, batch |e| maximum
+         + 30 * 8 + 16;  // mbarriers, TMEM base, flag, batch |e| maximum
 }
 
 }  // namespace dspark

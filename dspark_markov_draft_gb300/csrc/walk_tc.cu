@@ -18,10 +18,11 @@
 //     rest are re-read from L2.
 //   * D[128 x N] = A . B^T accumulates in fp32 in tensor memory. One thread issues an
 //     MMA only about every 50 cycles whatever N is (up to 128), so the K range is
-//     split in two halves issued by two threads into two accumulators, which the
-//     epilogue adds.
+//     split in two halves issued by two threads: for N <= 32 into two accumulators
+//     (issued concurrently, added by the epilogue), for N = 64 into one (half 1 issued
+//     after half 0, ordered through an mbarrier and tensor-core fences).
 //   * Epilogue (8 warps): thread = tensor-memory lane = one vocabulary row of the
-//     tile, for N/2 request rows. It adds the two K-half accumulators, forms
+//     tile, for N/2 request rows. It reads D (adding the K-half accumulators), forms
 //     l = base + scale_v 2^-s D (base logits staged one tile ahead by a tensor-map
 //     copy), the score (greedy: l; probabilistic: bf16(l)/T plus Gumbel noise, whose
 //     Philox blocks of 4 consecutive rows are drawn once per lane quad and exchanged
@@ -157,6 +158,29 @@ __device__ __forceinline__ void tmem_ld2<8>(uint32_t a0, uint32_t a1, float (&d0
 #pragma unroll
   for (int j = 0; j < 8; ++j) { d0[j] = __uint_as_float(r[j]); d1[j] = __uint_as_float(r[8 + j]); }
 }
+// One load of CH consecutive columns (a single accumulator), one wait.
+template <int CH>
+__device__ __forceinline__ void tmem_ld1(uint32_t a0, float (&d0)[CH]);
+template <>
+__device__ __forceinline__ void tmem_ld1<4>(uint32_t a0, float (&d0)[4]) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a0) : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 4; ++j) d0[j] = __uint_as_float(r[j]);
+}
+template <>
+__device__ __forceinline__ void tmem_ld1<8>(uint32_t a0, float (&d0)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7]) : "r"(a0) : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 8; ++j) d0[j] = __uint_as_float(r[j]);
+}
+
 // Column maxima of NC packed words per lane over the 32 lanes of a warp: plain
 // butterfly rounds while the offset is at least NC, then reduce-scatter rounds that
 // halve the columns a lane holds; lane l returns the maximum of column l % NC.
@@ -249,7 +273,15 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
   constexpr int kHalfChunks = kChunks / 2;           // per producer thread and tile
   constexpr int kPassChunks = INT8 ? 4 : 8;          // chunks per 32-column store
   constexpr uint32_t kIdesc = f16_idesc(INT8 ? 0u : 1u, N);
-  constexpr uint32_t kColD = 256;                    // D[buf][half] at kColD + (2 buf + half) N
+  constexpr uint32_t kColD = 256;                    // D buffers from column 256
+  // N = 64: one accumulator per D buffer, K half 1 issued after K half 0 (ordered by
+  // an mbarrier between the two issuing threads) onto half 0's partial sums, so the
+  // epilogue loads and adds nothing twice; smaller N: one accumulator per K half at
+  // kColD + (2 buf + half) N, the two halves issued concurrently.
+  constexpr bool kOneAcc = N == 64;
+  // N = 64 with scores through bf16 or draft_logits (the heavier register load):
+  // column maxima reduced through shared memory instead of lane shuffles
+  constexpr bool kSmemReduce = N == 64 && (PROB || LOGITS);
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte aligned start, by an offset from smem_raw so that every derived pointer
@@ -264,13 +296,14 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
   uint64_t* best_s = seed_s + 64;
   uint64_t* red_s = best_s + 64;                                  // [4][64]
   float2* inv_s = reinterpret_cast<float2*>(red_s + 4 * 64);       // 2^-s as two factors
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(inv_s + 2);        // [28]
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(inv_s + 2);        // [30]
   uint64_t* a_full = mbar;        // [buf * 2 + half], 4 arrivals
   uint64_t* a_empty = mbar + 4;   // [buf * 2 + half], 1 commit
   uint64_t* d_full = mbar + 8;    // [buf], 2 commits
   uint64_t* d_empty = mbar + 10;  // [buf], 8 arrivals
   uint64_t* s_full = mbar + 12;   // [epilogue warp * 2 + stage buffer], 1 arrival + bytes
-  uint32_t* tbase_s = reinterpret_cast<uint32_t*>(mbar + 28);
+  uint64_t* h0_done = mbar + 28;  // [buf], one accumulator: K half 0 of the tile issued
+  uint32_t* tbase_s = reinterpret_cast<uint32_t*>(mbar + 30);
   int* flag = reinterpret_cast<int*>(tbase_s + 1);
   int* sh_amax = flag + 1;        // largest finite |e| of the batch, as fp32 bits
 
@@ -304,7 +337,7 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
   }
   if (tid == 0) {
     const uint32_t counts[12] = {4, 4, 4, 4, 1, 1, 1, 1, 2, 2, 8, 8};
-    for (int b = 0; b < 28; ++b)
+    for (int b = 0; b < 30; ++b)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&mbar[b])), "r"(b < 12 ? counts[b] : 1u));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *sh_amax = 0;
@@ -395,6 +428,29 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
     if (tid == 0) *sh_amax = 0;  // every thread read it before the barrier
 
     bool failed = false;
+    // This K half's 8 MMAs of tile g into D buffer buf (the caller has waited for A,
+    // the D buffer and, with one accumulator, for K half 0), then the commits.
+    auto issue_half = [&](int buf, int g) {
+      tc_fence_after();
+      const uint32_t a_col = buf ? kColA1 : kColA0;
+      const uint32_t d_col = kColD + (kOneAcc ? buf * N : (2 * buf + half) * N);
+      const uint32_t b_base = smem_u32(b_s);
+      const uint32_t acc0 = (kOneAcc && half == 1) ? 1u : 0u;  // half 1 adds onto half 0
+#pragma unroll
+      for (int k8 = 0; k8 < 8; ++k8) {
+        const int kk = 8 * half + k8;
+        const uint64_t bd = sw128_desc(b_base + (kk / 4) * N * 128 + (kk % 4) * 32);
+        mma_f16(tmem + d_col, tmem + a_col + 8 * kk, bd, kIdesc, k8 > 0 ? 1u : acc0);
+      }
+      mma_commit(&d_full[buf]);
+      mma_commit(&a_empty[buf * 2 + half]);
+      if (kOneAcc && half == 0) {
+        // K half 1's MMAs are issued after these (tensor-core ops ordered across threads)
+        tc_fence_before();
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&h0_done[buf])) : "memory");
+      }
+      last_issued = g;
+    };
     if (producer) {
       // ---------------------------------------------------------------- producers
       const bool fill_now = (i == 0);
@@ -474,22 +530,11 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
           // MMA issue for this K half: A complete (all 4 quadrants), D buffer free.
           bool good = mbar_wait(&a_full[buf * 2 + half], u & 1, p.sync.timeout_ns);
           if (good && u >= 1) good = mbar_wait(&d_empty[buf], (u - 1) & 1, p.sync.timeout_ns);
+          if (kOneAcc && good && half == 1) good = mbar_wait(&h0_done[buf], u & 1, p.sync.timeout_ns);
           if (!good) {
             failed = true;
           } else {
-            tc_fence_after();
-            const uint32_t a_col = buf ? kColA1 : kColA0;
-            const uint32_t d_col = kColD + (2 * buf + half) * N;
-            const uint32_t b_base = smem_u32(b_s);
-#pragma unroll
-            for (int k8 = 0; k8 < 8; ++k8) {
-              const int kk = 8 * half + k8;
-              const uint64_t bd = sw128_desc(b_base + (kk / 4) * N * 128 + (kk % 4) * 32);
-              mma_f16(tmem + d_col, tmem + a_col + 8 * kk, bd, kIdesc, k8 > 0 ? 1u : 0u);
-            }
-            mma_commit(&d_full[buf]);
-            mma_commit(&a_empty[buf * 2 + half]);
-            last_issued = g;
+            issue_half(buf, g);
           }
         }
         if (t + 1 < T) {  // next tile's data in flight while this warp waits (issuers: after the MMAs)
@@ -506,24 +551,13 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
       // the 4 producer warps of the half have stored the tile and the epilogue has
       // released the D buffer.
       if (lane == 0) {
-        const uint32_t b_base = smem_u32(b_s);
         for (int t = 0; t < T; ++t) {
           const int g = g_base + t, buf = g & 1, u = g >> 1;
           bool good = mbar_wait(&a_full[buf * 2 + half], u & 1, p.sync.timeout_ns);
           if (good && u >= 1) good = mbar_wait(&d_empty[buf], (u - 1) & 1, p.sync.timeout_ns);
+          if (kOneAcc && good && half == 1) good = mbar_wait(&h0_done[buf], u & 1, p.sync.timeout_ns);
           if (!good) { failed = true; break; }
-          tc_fence_after();
-          const uint32_t a_col = buf ? kColA1 : kColA0;
-          const uint32_t d_col = kColD + (2 * buf + half) * N;
-#pragma unroll
-          for (int k8 = 0; k8 < 8; ++k8) {
-            const int kk = 8 * half + k8;
-            const uint64_t bd = sw128_desc(b_base + (kk / 4) * N * 128 + (kk % 4) * 32);
-            mma_f16(tmem + d_col, tmem + a_col + 8 * kk, bd, kIdesc, k8 > 0 ? 1u : 0u);
-          }
-          mma_commit(&d_full[buf]);
-          mma_commit(&a_empty[buf * 2 + half]);
-          last_issued = g;
+          issue_half(buf, g);
         }
       }
       __syncwarp();
@@ -631,17 +665,24 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
 #pragma unroll
         for (int cc = 0; cc < NC / CHG; ++cc) {
           if (cc * CHG >= ncol) break;
-          float d0[CHG], d1[CHG];
-          const uint32_t dcol = kColD + 2 * buf * N + cb + cc * CHG;
-          tmem_ld2<CHG>(tmem + lane_off + dcol, tmem + lane_off + dcol + N, d0, d1);
+          float dsum[CHG];  // the contraction D of the thread's row, the chunk's columns
+          if constexpr (kOneAcc) {
+            tmem_ld1<CHG>(tmem + lane_off + kColD + buf * N + cb + cc * CHG, dsum);
+          } else {
+            float d1[CHG];
+            const uint32_t dcol = kColD + 2 * buf * N + cb + cc * CHG;
+            tmem_ld2<CHG>(tmem + lane_off + dcol, tmem + lane_off + dcol + N, dsum, d1);
+#pragma unroll
+            for (int k = 0; k < CHG; ++k) dsum[k] = __fadd_rn(dsum[k], d1[k]);
+          }
           float sc[CHG];  // scores of this thread's row in the chunk's columns
 #pragma unroll
           for (int k = 0; k < CHG; ++k) {
             const int j = cc * CHG + k;  // columns past bs or of dead rows are computed and discarded
             const float bvl = __uint_as_float(static_cast<uint32_t>(bsm[j * 32]) << 16);
             float l;
-            if constexpr (INT8) l = __fmaf_rn(__fadd_rn(d0[k], d1[k]), c, bvl);
-            else l = __fadd_rn(__fadd_rn(d0[k], d1[k]), bvl);
+            if constexpr (INT8) l = __fmaf_rn(dsum[k], c, bvl);
+            else l = __fadd_rn(dsum[k], bvl);
             if constexpr (!FULL) l = valid ? l : -INFINITY;
             [[maybe_unused]] const uint16_t lh = f32_to_bf16_bits(l);
             if constexpr (LOGITS) {
@@ -734,6 +775,36 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
             red_s[q * 64 + cb + j] =
                 pack_best(kmax, static_cast<uint32_t>(v0) + 32u * q + (pos & 31u) + (pos >> 5) * kTile);
         }
+      } else if constexpr (kSmemReduce) {
+        // packed words transposed through the warp's stage buffer (idle now), in two
+        // rounds of RW = NC / 2 columns: lane l writes its RW words as row l ([32][RW],
+        // word k at slot k ^ (l % RW)); lane g RW + k then takes the maximum of column
+        // k over rows g RW .. g RW + RW - 1, and the 32 / RW row groups are combined by
+        // butterflies.
+        __syncwarp();
+        constexpr int RW = NC / 2;
+        static_assert((RW & (RW - 1)) == 0 && RW >= 8 && RW <= 16, "transpose rounds of 8 or 16 columns");
+        uint64_t* tr = reinterpret_cast<uint64_t*>(stage_s);  // 32 x RW words: the 2 x NC x 32 stage
+        const uint32_t vlane = static_cast<uint32_t>(v0) + 32u * q + lane;
+        const int kc = lane & (RW - 1), gr = lane / RW;
+#pragma unroll
+        for (int r0 = 0; r0 < NC; r0 += RW) {
+#pragma unroll
+          for (int k = 0; k < RW; ++k) {
+            const int j = r0 + k;
+            const uint32_t tj = (bt[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+            tr[lane * RW + (k ^ (lane & (RW - 1)))] = j < ncol ? pack_best(order_key(bv[j]), vlane + tj * kTile) : 0ull;
+          }
+          __syncwarp();
+          uint64_t m = 0ull;
+#pragma unroll
+          for (int rr = 0; rr < RW; ++rr) m = umax64(m, tr[(gr * RW + rr) * RW + (kc ^ rr)]);
+#pragma unroll
+          for (int o = RW; o < 32; o <<= 1) m = umax64(m, __shfl_xor_sync(kFull, m, o));
+          if (lane < RW && r0 + lane < ncol) red_s[q * 64 + cb + r0 + lane] = m;
+          __syncwarp();
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before the next tensor-map copies
       } else {
         // many columns: packed words, reduce-scattered across the lanes
         const uint32_t vlane = static_cast<uint32_t>(v0) + 32u * q + lane;
