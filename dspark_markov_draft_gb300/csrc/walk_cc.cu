@@ -5,8 +5,10 @@
 //
 // Work split. CTA c owns the contiguous vocabulary slice [c*V/G, (c+1)*V/G). The first
 // `resident_rows` rows of the slice are copied into shared memory while draft position
-// 0 streams them from HBM, and are read from shared memory at every later position;
-// the remaining rows are re-read from global memory (L2) at each position.
+// 0 streams them from HBM, and are read from shared memory at every later position.
+// Of the remaining rows, each warp keeps its first 32-row blocks (int8: two, bf16: one)
+// in tensor memory, which this kernel otherwise leaves idle: written at the first pass
+// and read back (tcgen05.ld) at every later one. The rest are re-read from L2.
 //
 // Contraction. Eight lanes share one W2 row; lane j owns the 16-byte chunks j, j+8
 // (int8: 32 values) or j, j+8, j+16, j+24 (bf16: 32 values) of every row, so the
@@ -168,6 +170,43 @@ __device__ __forceinline__ uint64_t score_entry(const WalkParams& p, int b, int 
   return pack_best(order_key(s), static_cast<uint32_t>(v));
 }
 
+// One W2 row's chunks of this lane (int8: 2, bf16: 4 x 16 bytes) to / from tensor
+// memory: 8 or 16 consecutive 32-bit columns of the lane's own row of tensor memory.
+template <int C>
+__device__ __forceinline__ void tmem_st_chunks(uint32_t taddr, const uint4 (&q)[C]);
+template <>
+__device__ __forceinline__ void tmem_st_chunks<2>(uint32_t taddr, const uint4 (&q)[2]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               ::"r"(taddr), "r"(q[0].x), "r"(q[0].y), "r"(q[0].z), "r"(q[0].w), "r"(q[1].x), "r"(q[1].y),
+                 "r"(q[1].z), "r"(q[1].w) : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st_chunks<4>(uint32_t taddr, const uint4 (&q)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+               "%11, %12, %13, %14, %15, %16};"
+               ::"r"(taddr), "r"(q[0].x), "r"(q[0].y), "r"(q[0].z), "r"(q[0].w), "r"(q[1].x), "r"(q[1].y),
+                 "r"(q[1].z), "r"(q[1].w), "r"(q[2].x), "r"(q[2].y), "r"(q[2].z), "r"(q[2].w), "r"(q[3].x),
+                 "r"(q[3].y), "r"(q[3].z), "r"(q[3].w) : "memory");
+}
+template <int C>
+__device__ __forceinline__ void tmem_ld_chunks(uint32_t taddr, uint4 (&q)[C]);
+template <>
+__device__ __forceinline__ void tmem_ld_chunks<2>(uint32_t taddr, uint4 (&q)[2]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(q[0].x), "=r"(q[0].y), "=r"(q[0].z), "=r"(q[0].w), "=r"(q[1].x), "=r"(q[1].y),
+                 "=r"(q[1].z), "=r"(q[1].w) : "r"(taddr) : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_ld_chunks<4>(uint32_t taddr, uint4 (&q)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+               "%11, %12, %13, %14, %15}, [%16];"
+               : "=r"(q[0].x), "=r"(q[0].y), "=r"(q[0].z), "=r"(q[0].w), "=r"(q[1].x), "=r"(q[1].y),
+                 "=r"(q[1].z), "=r"(q[1].w), "=r"(q[2].x), "=r"(q[2].y), "=r"(q[2].z), "=r"(q[2].w),
+                 "=r"(q[3].x), "=r"(q[3].y), "=r"(q[3].z), "=r"(q[3].w) : "r"(taddr) : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 }  // namespace
 
 template <bool INT8, bool PROB, bool LOGITS>
@@ -195,6 +234,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkPara
   uint64_t* best_s = reinterpret_cast<uint64_t*>(prev_s + 64);
   uint64_t* red = best_s + 64;
   int* flag = reinterpret_cast<int*>(red + kWalkWarps);
+  uint32_t* tbase_s = reinterpret_cast<uint32_t*>(flag + 1);  // tensor-memory base address
 
   const unsigned char* w2g = INT8 ? reinterpret_cast<const unsigned char*>(p.w2q)
                                   : reinterpret_cast<const unsigned char*>(p.w2);
@@ -215,6 +255,29 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkPara
   prefetch_base_slice(p, v0, n, 0);
   prefetch_base_slice(p, v0, n, 1);
   bool filled = false;
+
+  // Tensor memory (all 512 columns, idle otherwise in this kernel) keeps the first
+  // kTmBlocks of each warp's 32-row blocks beyond the resident rows, written at the
+  // walk's first pass over them and read back at every later one instead of from L2.
+  // Warp w owns the lanes of quadrant w % 4 and columns 128 (w / 4) .. + 127.
+  constexpr int kChunksPerRow = INT8 ? 2 : 4;
+  constexpr int kTmBlocks = 128 / (8 * kChunksPerRow * 4);  // blocks per warp: int8 2, bf16 1
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;"
+                 ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(tbase_s))) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tm_warp = *tbase_s + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 128u * (warp >> 2);
+  auto release_tmem = [&]() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (warp == 0)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(*tbase_s) : "memory");
+  };
 
   for (int i = 0; i < p.K; ++i) {
     __syncthreads();
@@ -333,6 +396,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkPara
           const bool resident = r0 + 32 <= res;
           const bool from_smem = resident && (i > 0 || !fill || fill_now);
           const bool store_smem = false;
+          // streamed blocks come first: block k < kTmBlocks of them lives in tensor memory
+          const bool in_tm = !resident && k < kTmBlocks;
+          const bool tm_store = in_tm && fill, tm_load = in_tm && !fill;
+          const uint32_t tm_blk = tm_warp + static_cast<uint32_t>(k) * (8 * kChunksPerRow * 4);
           if (fill_now && resident) cp_async_wait(nblk - 1 - k);
           const int rbase = r0 + 8 * grp;
           // The lane's own epilogue row: its base logit was loaded one block ahead.
@@ -347,18 +414,23 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkPara
             const int r = rbase + rr;
             constexpr int kChunks = INT8 ? 2 : 4;
             uint4 q[kChunks];
+            if (tm_load) {
+              tmem_ld_chunks<kChunks>(tm_blk + rr * (kChunks * 4), q);
+            } else {
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
-              if (r < n) {
-                if (from_smem)
-                  q[c] = reinterpret_cast<const uint4*>(w2s + static_cast<size_t>(r) * kRowBytes)[j8 + 8 * c];
-                else
-                  q[c] = ld_row_chunk(w2g + static_cast<size_t>(r) * kRowBytes, j8 + 8 * c);
-                if (store_smem)
-                  reinterpret_cast<uint4*>(w2s + static_cast<size_t>(r) * kRowBytes)[j8 + 8 * c] = q[c];
-              } else {
-                q[c] = make_uint4(0u, 0u, 0u, 0u);
+              for (int c = 0; c < kChunks; ++c) {
+                if (r < n) {
+                  if (from_smem)
+                    q[c] = reinterpret_cast<const uint4*>(w2s + static_cast<size_t>(r) * kRowBytes)[j8 + 8 * c];
+                  else
+                    q[c] = ld_row_chunk(w2g + static_cast<size_t>(r) * kRowBytes, j8 + 8 * c);
+                  if (store_smem)
+                    reinterpret_cast<uint4*>(w2s + static_cast<size_t>(r) * kRowBytes)[j8 + 8 * c] = q[c];
+                } else {
+                  q[c] = make_uint4(0u, 0u, 0u, 0u);
+                }
               }
+              if (tm_store) tmem_st_chunks<kChunks>(tm_blk + rr * (kChunks * 4), q);
             }
             if constexpr (LIMBS) {
               int h = 0, m = 0, l = 0;
@@ -378,6 +450,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkPara
               fpart[rr] = a;
             }
           }
+          if (tm_store) asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           float bias_raw;
           if constexpr (LIMBS) {
             const int H = butterfly8(hpart, lane);
@@ -422,7 +495,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkPara
     for (int t = threadIdx.x; t < p.bs; t += blockDim.x)
       if (prev_s[t] < 0) best_s[t] = 0ull;
 
-    if (!exchange_best(p.sync, i, p.bs, skip0 && i == 0, best_s, flag)) return;
+    if (!exchange_best(p.sync, i, p.bs, skip0 && i == 0, best_s, flag)) {
+      release_tmem();
+      return;
+    }
     if (i + 2 < p.K) prefetch_base_slice(p, v0, n, i + 2);
     for (int t = threadIdx.x; t < p.bs; t += blockDim.x) {
       const int tok = prev_s[t] >= 0 ? unpack_idx(best_s[t]) : -1;
@@ -431,6 +507,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkPara
     }
     reset_behind(p.sync, i, p.bs);
   }
+  release_tmem();
   finish_walk(p.sync, p.K, p.bs, flag);
 }
 
