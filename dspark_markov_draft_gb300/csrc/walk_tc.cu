@@ -131,54 +131,46 @@ __device__ __forceinline__ void tmem_st32_u4(uint32_t taddr, const uint4 (&c)[8]
       : "memory");
 }
 
-// Two loads of CH consecutive columns (the two K-half accumulators), one wait.
-template <int CH>
-__device__ __forceinline__ void tmem_ld2(uint32_t a0, uint32_t a1, float (&d0)[CH], float (&d1)[CH]);
-template <>
-__device__ __forceinline__ void tmem_ld2<4>(uint32_t a0, uint32_t a1, float (&d0)[4], float (&d1)[4]) {
-  uint32_t r[8];
+// Loads of tensor-memory columns into registers: x4 / x8 pieces without a wait, then
+// one tcgen05.wait::ld for all of them.
+__device__ __forceinline__ void tmem_ld4_nowait(uint32_t a, float* d) {
+  uint32_t r0, r1, r2, r3;
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a0) : "memory");
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]) : "r"(a1) : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int j = 0; j < 4; ++j) { d0[j] = __uint_as_float(r[j]); d1[j] = __uint_as_float(r[4 + j]); }
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a) : "memory");
+  d[0] = __uint_as_float(r0); d[1] = __uint_as_float(r1); d[2] = __uint_as_float(r2); d[3] = __uint_as_float(r3);
 }
-template <>
-__device__ __forceinline__ void tmem_ld2<8>(uint32_t a0, uint32_t a1, float (&d0)[8], float (&d1)[8]) {
-  uint32_t r[16];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                 "=r"(r[6]), "=r"(r[7]) : "r"(a0) : "memory");
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-                 "=r"(r[14]), "=r"(r[15]) : "r"(a1) : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int j = 0; j < 8; ++j) { d0[j] = __uint_as_float(r[j]); d1[j] = __uint_as_float(r[8 + j]); }
-}
-// One load of CH consecutive columns (a single accumulator), one wait.
-template <int CH>
-__device__ __forceinline__ void tmem_ld1(uint32_t a0, float (&d0)[CH]);
-template <>
-__device__ __forceinline__ void tmem_ld1<4>(uint32_t a0, float (&d0)[4]) {
-  uint32_t r[4];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a0) : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int j = 0; j < 4; ++j) d0[j] = __uint_as_float(r[j]);
-}
-template <>
-__device__ __forceinline__ void tmem_ld1<8>(uint32_t a0, float (&d0)[8]) {
+__device__ __forceinline__ void tmem_ld8_nowait(uint32_t a, float* d) {
   uint32_t r[8];
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                 "=r"(r[6]), "=r"(r[7]) : "r"(a0) : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                 "=r"(r[6]), "=r"(r[7]) : "r"(a) : "memory");
 #pragma unroll
-  for (int j = 0; j < 8; ++j) d0[j] = __uint_as_float(r[j]);
+  for (int j = 0; j < 8; ++j) d[j] = __uint_as_float(r[j]);
+}
+template <int CH>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t a, float* d) {
+  static_assert(CH == 4 || CH % 8 == 0, "4 or a multiple of 8 columns");
+  if constexpr (CH == 4) {
+    tmem_ld4_nowait(a, d);
+  } else {
+#pragma unroll
+    for (int c = 0; c < CH; c += 8) tmem_ld8_nowait(a + c, d + c);
+  }
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// CH consecutive columns of one accumulator, one wait.
+template <int CH>
+__device__ __forceinline__ void tmem_ld1(uint32_t a0, float (&d0)[CH]) {
+  tmem_ld_cols<CH>(a0, d0);
+  tmem_wait_ld();
+}
+// CH consecutive columns of each of the two K-half accumulators, one wait.
+template <int CH>
+__device__ __forceinline__ void tmem_ld2(uint32_t a0, uint32_t a1, float (&d0)[CH], float (&d1)[CH]) {
+  tmem_ld_cols<CH>(a0, d0);
+  tmem_ld_cols<CH>(a1, d1);
+  tmem_wait_ld();
 }
 
 // Column maxima of NC packed words per lane over the 32 lanes of a warp: plain
@@ -572,7 +564,9 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
       // Tiles are 8-bit fields, four columns per register. The lanes and quadrants are
       // combined once per position. The base logits of the warp's rows and columns are
       // staged in shared memory one tile ahead.
-      constexpr int CHG = NC < 8 ? NC : (PROB ? 4 : 8);
+      // columns per accumulator load: as many as the registers allow (one accumulator at
+      // N = 64 leaves room for twice as many)
+      constexpr int CHG = NC < 8 ? NC : (kOneAcc ? (PROB ? 8 : 16) : (PROB ? 4 : 8));
       static_assert(NC % CHG == 0, "the column chunks must tile the warp's columns");
       static_assert(!PROB || CHG % 4 == 0, "Philox blocks are drawn for groups of 4 columns");
       const int cb = half * NC;                                 // first column of the warp
