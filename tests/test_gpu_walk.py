@@ -212,8 +212,11 @@ def test_ties_nan_and_signed_zero(oracle, int8):
         check_walk(oracle, inp, tokens, mode=mode, gpu_logits=lg, **okw)
 
 
-def test_bad_token_reported():
-    V, K, bs = 4000, 3, 3
+@pytest.mark.parametrize("bs", [2, 3])
+def test_bad_token_reported(bs):
+    """An out-of-range previous token: BAD_TOKEN, that row's tokens are -1, the other
+    rows walk on (bs = 2: CUDA cores; bs = 3: tensor cores)."""
+    V, K = 4000, 3
     inp = synth.make(V, bs, K, seed=2)
     inp.prev[1] = V
     w1, w2, base, prev, seeds = to_dev(inp)
@@ -222,7 +225,23 @@ def test_bad_token_reported():
     torch.cuda.synchronize()
     assert int(status.item()) == 6
     t = tokens.cpu().numpy()
-    assert list(t[1]) == [-1] * K and np.all(t[[0, 2]] >= 0)
+    live = [r for r in range(bs) if r != 1]
+    assert list(t[1]) == [-1] * K and np.all(t[live] >= 0)
+
+
+@pytest.mark.parametrize("bs", [1, 2, 4, 20])
+def test_vocabulary_smaller_than_grid(oracle, bs):
+    """V below the number of CTAs: CTAs without vocabulary rows still take part in every
+    position's exchange (bs <= 2: CUDA-core walk, else tensor cores)."""
+    V, K = 100, 4
+    inp = synth.make(V, bs, K, seed=60 + bs, peak=8.0)
+    w1, w2, base, prev, seeds = to_dev(inp)
+    q, sc = capi.quantize_w2(w2)
+    _, q_ref, sc_ref = oracle.quantize_w2(bits(inp.w2))
+    for mode in (capi.GREEDY, capi.PROBABILISTIC):
+        tokens, lg = capi.walk(base, w1, prev, seeds=seeds, mode=mode, want_logits=True, w2q=q, scales=sc)
+        torch.cuda.synchronize()
+        check_walk(oracle, inp, tokens, mode=mode, q=q_ref, sc=sc_ref, gpu_logits=lg)
 
 
 @pytest.mark.parametrize("bs", [1, 8])
@@ -246,7 +265,7 @@ def test_timeout_returns_status_and_context_survives(bs):
     assert int(status.item()) == 0 and torch.equal(t1, t2)
 
 
-@pytest.mark.parametrize("bs", [1, 4, 8])
+@pytest.mark.parametrize("bs", [1, 2, 4, 8])
 def test_workspace_left_zeroed_and_reusable(bs):
     V, K = 7000, 6
     inp = synth.make(V, bs, K, seed=8)
