@@ -10,8 +10,9 @@
 // largest key T plus, among the entries equal to T, the ones with the smallest
 // vocabulary indices. Fast path: a histogram of the 11-bit key prefix of ~4096 evenly
 // spaced samples gives a pivot prefix that at least ~1.15 k entries reach; one pass
-// over the row collects every entry at or above the pivot into shared memory (warp-
-// aggregated appends); T is found by a two-byte radix select on that list; boundary
+// over the row collects every entry at or above the pivot into shared memory (a pivot
+// above +0 is tested on two packed entries at once, without branches; warp-aggregated
+// appends); T is found by a two-byte radix select on that list; boundary
 // ties are resolved by ranking the tied indices. Rows where the pivot collects fewer
 // than k or more than kSelCap entries, or the tie at T is wider than kSelTies, take the
 // exact path over the whole row: two 256-bin histogram passes and an ordered
@@ -147,12 +148,6 @@ __device__ void select_exact(const uint16_t* x, int64_t V, int k, int32_t* out, 
 }
 
 
-// Per-halfword unsigned maximum of two packed pairs.
-__device__ __forceinline__ uint32_t umax_u16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
 
 // Warp-aggregated append: every lane adds `c` items; returns this lane's first slot of
 // a block-wide counter (all lanes of the warp call it).
@@ -261,25 +256,44 @@ __global__ void __launch_bounds__(kSelThreads, 3) topk_select_kernel(const uint1
       }
     };
     const bool quick = pivot > 0x8000u;  // pivot above the keys of -0 / +0
+    // With the pivot above +0 an entry passes iff it is a NaN or non-negative with
+    // pattern >= pv = pivot - 0x8000 (its key is the pattern with the sign bit set).
+    // Both tests on two 16-bit entries at once without carries between the halves:
+    // for a magnitude y < 0x8000, y + (0x8000 - pv) has bit 15 set iff y >= pv, and
+    // y + 0x7F has it iff y > 0x7F80 (NaN).
+    const uint32_t pv = pivot - 0x8000u;
+    const uint32_t d2 = (0x8000u - pv) * 0x00010001u;
     uint4 w[4], wn[4];
     load4(0, w);
     for (int64_t c0 = 0; c0 < n8; c0 += 4 * kSelThreads) {
       if (c0 + 4 * kSelThreads < n8) load4(c0 + 4 * kSelThreads, wn);  // next batch in flight
+      if (quick) {
+        // bit 4 j + jj (+16 for the high half): entry 8 (c0 + j kSelThreads + tid) + 2 jj (+1);
+        // the zero words past the row never pass
+        uint32_t take = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t ww[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const uint32_t y = ww[jj] & 0x7FFF7FFFu;
+            const uint32_t r = (((y + d2) & ~ww[jj]) | (y + 0x007F007Fu)) & 0x80008000u;
+            take |= r >> (15 - (4 * j + jj));
+          }
+        }
+        append(take, [&](int t) {
+          const int hi = t >> 4, j = (t >> 2) & 3, jj = t & 3;
+          return 8 * (c0 + j * kSelThreads + tid) + 2 * jj + hi;
+        });
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[j] = wn[j];
+        continue;
+      }
       uint32_t take = 0;  // bit 8 j + e: entry 8 (c0 + j kSelThreads + tid) + e
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int64_t c = c0 + j * kSelThreads + tid;
         const uint32_t ww[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
-        // Quick reject of 8 entries: with the pivot above -0, only non-negative
-        // entries (whose key is the pattern with the sign bit set) or NaNs can pass.
-        if (quick) {
-          const uint32_t m = umax_u16x2(umax_u16x2(ww[0] ^ 0x80008000u, ww[1] ^ 0x80008000u),
-                                        umax_u16x2(ww[2] ^ 0x80008000u, ww[3] ^ 0x80008000u));
-          const uint32_t a = umax_u16x2(umax_u16x2(ww[0] & 0x7FFF7FFFu, ww[1] & 0x7FFF7FFFu),
-                                        umax_u16x2(ww[2] & 0x7FFF7FFFu, ww[3] & 0x7FFF7FFFu));
-          const bool any_nan = (a & 0xFFFFu) > 0x7F80u || (a >> 16) > 0x7F80u;
-          if (!any_nan && (m & 0xFFFFu) < pivot && (m >> 16) < pivot) continue;
-        }
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const uint16_t h = static_cast<uint16_t>((e & 1) ? (ww[e >> 1] >> 16) : (ww[e >> 1] & 0xFFFFu));
