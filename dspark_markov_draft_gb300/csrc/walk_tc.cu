@@ -266,10 +266,10 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
   constexpr int kPassChunks = INT8 ? 4 : 8;          // chunks per 32-column store
   constexpr uint32_t kIdesc = f16_idesc(INT8 ? 0u : 1u, N);
   constexpr uint32_t kColD = 256;                    // D buffers from column 256
-  // N = 64: one accumulator per D buffer, K half 1 issued after K half 0 (ordered by
-  // an mbarrier between the two issuing threads) onto half 0's partial sums, so the
-  // epilogue loads and adds nothing twice; smaller N: one accumulator per K half at
-  // kColD + (2 buf + half) N, the two halves issued concurrently.
+  // N = 64: one accumulator per D buffer; K half 1's MMAs are issued once K half 0's
+  // first (accumulator-initialising) MMA is (ordered by an mbarrier between the two
+  // issuing threads), so the epilogue loads and adds nothing twice; smaller N: one
+  // accumulator per K half at kColD + (2 buf + half) N, the halves issued concurrently.
   constexpr bool kOneAcc = N == 64;
   // N = 64 with scores through bf16 or draft_logits (the heavier register load):
   // column maxima reduced through shared memory instead of lane shuffles
@@ -433,14 +433,16 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
         const int kk = 8 * half + k8;
         const uint64_t bd = sw128_desc(b_base + (kk / 4) * N * 128 + (kk % 4) * 32);
         mma_f16(tmem + d_col, tmem + a_col + 8 * kk, bd, kIdesc, k8 > 0 ? 1u : acc0);
+        if (kOneAcc && half == 0 && k8 == 0) {
+          // K half 1's MMAs may follow once the accumulator-initialising one is issued
+          // (tensor-core operations ordered across threads through the fence and the
+          // mbarrier); the two halves then accumulate interleaved
+          tc_fence_before();
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&h0_done[buf])) : "memory");
+        }
       }
       mma_commit(&d_full[buf]);
       mma_commit(&a_empty[buf * 2 + half]);
-      if (kOneAcc && half == 0) {
-        // K half 1's MMAs are issued after these (tensor-core ops ordered across threads)
-        tc_fence_before();
-        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&h0_done[buf])) : "memory");
-      }
       last_issued = g;
     };
     if (producer) {
