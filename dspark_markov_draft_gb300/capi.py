@@ -44,7 +44,7 @@ class WalkArgs(C.Structure):
         ("top_k", C.c_int32), ("draft_tokens", C.c_void_p), ("draft_logits", C.c_void_p),
         ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t),
         ("status_dev", C.c_void_p), ("flags", C.c_uint32), ("resident_rows_cap", C.c_int32),
-        ("timeout_us", C.c_uint32),
+        ("timeout_us", C.c_uint32), ("temperatures", C.c_void_p), ("row_modes", C.c_void_p),
     ]
 
 
@@ -143,19 +143,22 @@ def quantize_w2(w2: torch.Tensor, q: torch.Tensor | None = None, scales: torch.T
 
 def make_args(base, w1, prev, tokens, workspace, *, w2=None, w2q=None, scales=None, seeds=None,
               mode=GREEDY, temperature=1.0, top_k=0, logits=None, status=None, flags=0,
-              resident_rows_cap=-1, timeout_us=0) -> WalkArgs:
+              resident_rows_cap=-1, timeout_us=0, temperatures=None, row_modes=None) -> WalkArgs:
+    """temperatures (fp32 [bs]) and row_modes (int32 [bs]), device tensors, override the
+    scalar temperature and mode row by row."""
     bs, K, V = base.shape
     wsp, wsn = _ws_view(workspace)
     return WalkArgs(
         _dev_ptr(base), _dev_ptr(w1), _dev_ptr(w2), _dev_ptr(w2q), _dev_ptr(scales),
         _dev_ptr(prev), _dev_ptr(seeds), V, w1.shape[1], bs, K, mode, temperature, top_k,
         _dev_ptr(tokens), _dev_ptr(logits), wsp, wsn, _dev_ptr(status), flags,
-        resident_rows_cap, timeout_us)
+        resident_rows_cap, timeout_us, _dev_ptr(temperatures), _dev_ptr(row_modes))
 
 
 def walk(base, w1, prev, *, w2=None, w2q=None, scales=None, seeds=None, mode=GREEDY,
          temperature=1.0, top_k=0, tokens=None, logits=None, want_logits=False, workspace=None,
-         status=None, flags=0, resident_rows_cap=-1, timeout_us=0, stream=None):
+         status=None, flags=0, resident_rows_cap=-1, timeout_us=0, stream=None,
+         temperatures=None, row_modes=None):
     """Run dspark_walk (or dspark_walk_topk when top_k > 0). Returns (tokens, logits)."""
     bs, K, V = base.shape
     dev = base.device
@@ -168,7 +171,7 @@ def walk(base, w1, prev, *, w2=None, w2q=None, scales=None, seeds=None, mode=GRE
     a = make_args(base, w1, prev, tokens, workspace, w2=w2, w2q=w2q, scales=scales,
                   seeds=seeds, mode=mode, temperature=temperature, top_k=top_k, logits=logits,
                   status=status, flags=flags, resident_rows_cap=resident_rows_cap,
-                  timeout_us=timeout_us)
+                  timeout_us=timeout_us, temperatures=temperatures, row_modes=row_modes)
     _check(lib().dspark_walk(C.byref(a), _stream(stream)), "dspark_walk")
     return tokens, logits
 

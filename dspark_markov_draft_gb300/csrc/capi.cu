@@ -14,7 +14,7 @@
 namespace dspark {
 
 const void* walk_cc_kernel_ptr(bool int8, bool prob, bool logits);
-const void* walk_tc_kernel_ptr(bool int8, bool prob, bool logits, int nq);
+const void* walk_tc_kernel_ptr(bool int8, bool prob, bool logits, int nq, bool rows);
 const void* topk_walk_kernel_ptr(bool prob, bool logits);
 size_t topk_walk_smem(int bs);
 cudaError_t launch_topk_select(const uint16_t* base, int64_t V, int k, int rows, int32_t* cand,
@@ -144,9 +144,12 @@ int32_t check_common(const dspark_walk_args* a) {
   if (a->V <= 0 || a->V > DSPARK_MAX_V) return DSPARK_ERR_INVALID_ARG;
   if (a->bs < 1 || a->bs > DSPARK_MAX_BS || a->K < 1 || a->K > DSPARK_MAX_K) return DSPARK_ERR_INVALID_ARG;
   if (a->mode != DSPARK_GREEDY && a->mode != DSPARK_PROBABILISTIC) return DSPARK_ERR_INVALID_ARG;
-  if (a->mode == DSPARK_PROBABILISTIC) {
+  // with per-row modes any row may be sampled; per-row temperatures are checked on the
+  // device (a bad one invalidates its row only)
+  if (a->mode == DSPARK_PROBABILISTIC || a->row_modes) {
     if (!a->seeds) return DSPARK_ERR_INVALID_ARG;
-    if (!(a->temperature > 0.f) || !(a->temperature < 3.4e38f)) return DSPARK_ERR_INVALID_ARG;
+    if (!a->temperatures && (!(a->temperature > 0.f) || !(a->temperature < 3.4e38f)))
+      return DSPARK_ERR_INVALID_ARG;
   }
   const bool have_bf16 = a->w2 != nullptr;
   const bool have_int8 = a->w2q != nullptr;
@@ -195,6 +198,8 @@ WalkParams make_params(const dspark_walk_args* a, int grid, int resident_rows, i
   p.temperature = a->temperature;
   p.temp_is_one = a->temperature == 1.0f ? 1 : 0;
   p.inv_temperature = static_cast<float>(1.0 / static_cast<double>(a->temperature));
+  p.temps = a->temperatures;
+  p.modes = a->row_modes;
   p.resident_rows = resident_rows;
   p.slice_cap = slice_cap;
   p.sync = make_sync(a, grid);
@@ -340,7 +345,7 @@ int32_t dspark_walk_topk(const dspark_walk_args* a, dspark_stream_t stream) {
                                      const_cast<int32_t*>(p.cand), a->draft_logits, s);
   if (e != cudaSuccess) return cuda_fail(e, "topk_select_kernel launch");
   const size_t smem = topk_walk_smem(a->bs);
-  const bool prob = a->mode == DSPARK_PROBABILISTIC, lg = a->draft_logits != nullptr;
+  const bool prob = a->mode == DSPARK_PROBABILISTIC || a->row_modes, lg = a->draft_logits != nullptr;
   const void* fn = topk_walk_kernel_ptr(prob, lg);
   return launch_coop(fn, caps.sms, kWalkThreads, smem, p, s);
 }
@@ -354,7 +359,7 @@ int32_t dspark_walk(const dspark_walk_args* a, dspark_stream_t stream) {
   if (!caps.coop) return DSPARK_ERR_UNSUPPORTED;
   const bool int8 = a->w2q != nullptr;
   const bool lg = a->draft_logits != nullptr;
-  const bool prob = a->mode == DSPARK_PROBABILISTIC;
+  const bool prob = a->mode == DSPARK_PROBABILISTIC || a->row_modes;  // any sampled row
   const bool use_tc = !(a->flags & DSPARK_FLAG_FORCE_CUDA_CORES) &&
                       (a->bs >= kTcMinBs || (a->flags & DSPARK_FLAG_FORCE_TENSOR_CORES)) &&
                       tc_fits(caps, a->V);
@@ -363,7 +368,8 @@ int32_t dspark_walk(const dspark_walk_args* a, dspark_stream_t stream) {
     WalkParams p = make_params(a, pl.grid, pl.resident_rows, pl.slice_cap);
     p.base_tma = make_bsk_map(a, a->base_logits, pl.nq * 4, &p.base_map) ? 1 : 0;
     p.logits_tma = make_bsk_map(a, a->draft_logits, pl.nq * 4, &p.logits_map) ? 1 : 0;
-    return launch_coop(walk_tc_kernel_ptr(int8, prob, lg, pl.nq), pl.grid, walk_tc_threads(pl.nq * 4), pl.smem, p,
+    const bool rows = prob && (a->temperatures || a->row_modes);  // per-row settings
+    return launch_coop(walk_tc_kernel_ptr(int8, prob, lg, pl.nq, rows), pl.grid, walk_tc_threads(pl.nq * 4), pl.smem, p,
                        reinterpret_cast<cudaStream_t>(stream));
   }
   const Plan pl = plan_dense(caps, a->V, int8, a->bs, a->resident_rows_cap);

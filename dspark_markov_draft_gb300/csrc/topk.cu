@@ -417,8 +417,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
   for (int t = tid; t < p.bs; t += blockDim.x) {
     const int32_t tok = p.prev[t];
     const bool ok = tok >= 0 && static_cast<int64_t>(tok) < p.V;
-    prev_s[t] = ok ? tok : -1;
+    const bool settings = row_settings_ok(p, PROB, t);
+    prev_s[t] = ok && settings ? tok : -1;
     if (!ok && cta == 0) report(p.sync.status_dev, DSPARK_ERR_BAD_TOKEN);
+    if (!settings && cta == 0) report(p.sync.status_dev, DSPARK_ERR_INVALID_ARG);
   }
 
   // Phase P of position i for the chunk [c_lo, c_hi): everything that does not depend on
@@ -434,7 +436,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
       it_v[e] = static_cast<int32_t>(v);
       it_base[e] = bf16_to_f32(__ldg(p.base + (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v));
       float g = 0.f;
-      if constexpr (PROB) {
+      if (row_sampled(p, PROB, b)) {
         const uint4 w = philox_block(p.seeds[b], b, i, static_cast<uint32_t>(v >> 2));
         g = gumbel_from_word(uint4_get(w, static_cast<int>(v & 3)));
       }
@@ -576,9 +578,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
           const uint16_t lh = f32_to_bf16_bits(l);
           if (LOGITS) p.logits[(static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v] = lh;
           float sco = l;
-          if constexpr (PROB) {
+          if (row_sampled(p, PROB, b)) {
             const float lb = bf16_to_f32(lh);
-            const float xs = p.temp_is_one ? lb : __fdiv_rn(lb, p.temperature);
+            const float T = row_temperature(p, b);
+            const float xs = T == 1.0f ? lb : __fdiv_rn(lb, T);
             sco = __fadd_rn(xs, it_g[e]);
           }
           atomicMax(reinterpret_cast<unsigned long long*>(&best_s[b]),

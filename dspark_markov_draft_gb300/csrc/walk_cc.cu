@@ -153,17 +153,18 @@ __device__ __forceinline__ float dot_bf16_chunk(const uint4& q, const float* e, 
   return acc;
 }
 
-// Score of one vocabulary entry and its argmax word.
+// Score of one vocabulary entry and its argmax word. sampled / T: row b's settings.
 template <bool PROB, bool LOGITS>
 __device__ __forceinline__ uint64_t score_entry(const WalkParams& p, int b, int i, int64_t v,
-                                                float base_v, float bias, uint64_t seed) {
+                                                float base_v, float bias, uint64_t seed,
+                                                bool sampled, float T) {
   const size_t o = (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v;
   const float l = __fadd_rn(base_v, bias);
   if (LOGITS) p.logits[o] = f32_to_bf16_bits(l);
   float s = l;
-  if (PROB) {
+  if (PROB && sampled) {
     const float lb = bf16_to_f32(f32_to_bf16_bits(l));
-    const float x = p.temp_is_one ? lb : __fdiv_rn(lb, p.temperature);
+    const float x = T == 1.0f ? lb : __fdiv_rn(lb, T);
     const uint4 w = philox_block(seed, b, i, static_cast<uint32_t>(v >> 2));
     s = __fadd_rn(x, gumbel_from_word(uint4_get(w, static_cast<int>(v & 3))));
   }
@@ -245,8 +246,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkPara
   for (int t = threadIdx.x; t < p.bs; t += blockDim.x) {
     const int32_t tok = p.prev[t];
     const bool ok = tok >= 0 && static_cast<int64_t>(tok) < p.V;
-    prev_s[t] = ok ? tok : -1;
+    const bool settings = row_settings_ok(p, PROB, t);
+    prev_s[t] = ok && settings ? tok : -1;
     if (!ok && cta == 0) report(p.sync.status_dev, DSPARK_ERR_BAD_TOKEN);
+    if (!settings && cta == 0) report(p.sync.status_dev, DSPARK_ERR_INVALID_ARG);
   }
   if (INT8)
     for (int r = threadIdx.x; r < n; r += blockDim.x) scale_s[r] = __ldg(p.scales + v0 + r);
@@ -332,7 +335,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkPara
 
     for (int b = 0; b < p.bs; ++b) {
       if (prev_s[b] < 0) continue;  // uniform over the CTA
-      const uint64_t seed = PROB ? p.seeds[b] : 0ull;
+      const bool sampled = row_sampled(p, PROB, b);
+      const float T_b = sampled ? row_temperature(p, b) : 1.0f;
+      const uint64_t seed = sampled ? p.seeds[b] : 0ull;
       const uint16_t* eb = e_s + static_cast<size_t>(b) * kRank;
       const int shift = sh_shift[b];
       const bool float_path = INT8 && shift == (1 << 30);
@@ -468,7 +473,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkPara
               bias = __fmul_rn(bias_raw, scale_v);
               if constexpr (LIMBS) bias = __fmul_rn(__fmul_rn(bias, inv_lo), inv_hi);
             }
-            best = umax64(best, score_entry<PROB, LOGITS>(p, b, i, v, base_v, bias, seed));
+            best = umax64(best, score_entry<PROB, LOGITS>(p, b, i, v, base_v, bias, seed, sampled, T_b));
           }
         }
         return best;

@@ -28,6 +28,8 @@ struct WalkParams {
   int32_t base_tma;          // base_map is valid (tensor-core walk)
   int32_t logits_tma;        // logits_map is valid (tensor-core walk)
   float inv_temperature;     // 1 / temperature, rounded to fp32 (tensor-core walk)
+  const float* temps;        // [bs] per-row temperatures, or null (then `temperature`)
+  const int32_t* modes;      // [bs] per-row modes, or null (then the kernel's mode)
   StepSync sync;
   // Tensor map over base [bs][K][V] (bf16), box {32 rows, 1 position, N/2 requests}:
   // one tile copy brings an epilogue warp's base logits of one 128-row tile.
@@ -36,6 +38,22 @@ struct WalkParams {
   // back to global memory in one tile copy.
   CUtensorMap logits_map;
 };
+
+// Per-row sampling settings. A PROB kernel serves batches with at least one sampled
+// row: row b is sampled unless the per-row modes say greedy.
+__device__ __forceinline__ bool row_sampled(const WalkParams& p, bool prob_kernel, int b) {
+  return prob_kernel && (!p.modes || p.modes[b] == DSPARK_PROBABILISTIC);
+}
+__device__ __forceinline__ float row_temperature(const WalkParams& p, int b) {
+  return p.temps ? p.temps[b] : p.temperature;
+}
+// Valid settings of row b: a known mode, and T > 0 and finite if the row is sampled.
+__device__ __forceinline__ bool row_settings_ok(const WalkParams& p, bool prob_kernel, int b) {
+  if (p.modes && p.modes[b] != DSPARK_GREEDY && p.modes[b] != DSPARK_PROBABILISTIC) return false;
+  if (!row_sampled(p, prob_kernel, b)) return true;
+  const float T = row_temperature(p, b);
+  return T > 0.f && T < 3.4e38f;
+}
 
 // Threads per CTA of the persistent walk kernels: 16 warps.
 constexpr int kWalkThreads = 512;
@@ -92,6 +110,7 @@ __host__ __device__ inline size_t walk_tc_misc_smem() {
          + 64 * 8        // per-row argmax words
          + 4 * 64 * 8    // per-quadrant argmax words
          + 2 * 8         // 2^-s as two factors
+         + 64 * 4 + 8    // 1/T per row, greedy-row mask
          + 30 * 8 + 16;  // mbarriers, TMEM base, flag, batch |e| maximum
 }
 

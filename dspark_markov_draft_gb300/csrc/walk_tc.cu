@@ -255,8 +255,11 @@ __device__ __forceinline__ void cp_async_wait_pending(int pending) {
 //               and 64, where the epilogue needs every register of a 512-thread CTA.
 // Roles hand tiles over through mbarriers (A full/empty per buffer and K half, D
 // full/empty per buffer), with two A and two D buffers in tensor memory.
-template <bool INT8, bool PROB, bool LOGITS, int N>
+// ROWS (with PROB): per-row modes or temperatures; the other instances score every
+// column with the kernel's mode and temperature.
+template <bool INT8, bool PROB, bool LOGITS, int N, bool ROWS>
 __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __grid_constant__ WalkParams p) {
+  static_assert(PROB || !ROWS, "per-row settings come with sampled rows");
   constexpr bool kOwnIssuers = walk_tc_threads(N) > kWalkThreads;  // warps 16, 17 issue the MMAs
   constexpr int kWarps = walk_tc_threads(N) / 32;
   constexpr int NC = N / 2;                          // columns per epilogue warp
@@ -266,10 +269,10 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
   constexpr int kPassChunks = INT8 ? 4 : 8;          // chunks per 32-column store
   constexpr uint32_t kIdesc = f16_idesc(INT8 ? 0u : 1u, N);
   constexpr uint32_t kColD = 256;                    // D buffers from column 256
-  // N = 64: one accumulator per D buffer; K half 1's MMAs are issued once K half 0's
-  // first (accumulator-initialising) MMA is (ordered by an mbarrier between the two
-  // issuing threads), so the epilogue loads and adds nothing twice; smaller N: one
-  // accumulator per K half at kColD + (2 buf + half) N, the halves issued concurrently.
+  // N = 64: one accumulator per D buffer, K half 1 issued after K half 0 (ordered by
+  // an mbarrier between the two issuing threads) onto half 0's partial sums, so the
+  // epilogue loads and adds nothing twice; smaller N: one accumulator per K half at
+  // kColD + (2 buf + half) N, the two halves issued concurrently.
   constexpr bool kOneAcc = N == 64;
   // N = 64 with scores through bf16 or draft_logits (the heavier register load):
   // column maxima reduced through shared memory instead of lane shuffles
@@ -288,7 +291,9 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
   uint64_t* best_s = seed_s + 64;
   uint64_t* red_s = best_s + 64;                                  // [4][64]
   float2* inv_s = reinterpret_cast<float2*>(red_s + 4 * 64);       // 2^-s as two factors
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(inv_s + 2);        // [30]
+  float* invT_s = reinterpret_cast<float*>(inv_s + 2);            // [64] 1/T per row (fp32)
+  uint64_t* gmask_s = reinterpret_cast<uint64_t*>(invT_s + 64);   // bit b: row b greedy
+  uint64_t* mbar = gmask_s + 1;                                    // [30]
   uint64_t* a_full = mbar;        // [buf * 2 + half], 4 arrivals
   uint64_t* a_empty = mbar + 4;   // [buf * 2 + half], 1 commit
   uint64_t* d_full = mbar + 8;    // [buf], 2 commits
@@ -320,12 +325,19 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
   for (int t = tid; t < N * 512 / 16; t += blockDim.x) reinterpret_cast<uint4*>(b_s)[t] = make_uint4(0, 0, 0, 0);
   if (INT8)
     for (int r = tid; r < n; r += blockDim.x) scale_s[r] = __ldg(p.scales + v0 + r);
-  for (int t = tid; t < 64; t += blockDim.x) seed_s[t] = (PROB && t < p.bs) ? p.seeds[t] : 0ull;
+  for (int t = tid; t < 64; t += blockDim.x) {
+    const bool sampled = t < p.bs && row_sampled(p, PROB, t);
+    seed_s[t] = sampled ? p.seeds[t] : 0ull;
+    // 1/T rounded to fp32 from the double quotient, as the host does for the scalar T
+    if constexpr (ROWS) invT_s[t] = sampled ? static_cast<float>(1.0 / static_cast<double>(row_temperature(p, t))) : 1.0f;
+  }
   for (int t = tid; t < p.bs; t += blockDim.x) {
     const int32_t tok = p.prev[t];
     const bool okt = tok >= 0 && static_cast<int64_t>(tok) < p.V;
-    prev_s[t] = okt ? tok : -1;
+    const bool settings = row_settings_ok(p, PROB, t);
+    prev_s[t] = okt && settings ? tok : -1;
     if (!okt && cta == 0) report(p.sync.status_dev, DSPARK_ERR_BAD_TOKEN);
+    if (!settings && cta == 0) report(p.sync.status_dev, DSPARK_ERR_INVALID_ARG);
   }
   if (tid == 0) {
     const uint32_t counts[12] = {4, 4, 4, 4, 1, 1, 1, 1, 2, 2, 8, 8};
@@ -333,6 +345,12 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&mbar[b])), "r"(b < 12 ? counts[b] : 1u));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *sh_amax = 0;
+    if constexpr (ROWS) {
+      uint64_t gm = 0ull;
+      for (int b = 0; b < p.bs; ++b)
+        if (!row_sampled(p, PROB, b)) gm |= 1ull << b;
+      *gmask_s = gm;
+    }
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -433,16 +451,16 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
         const int kk = 8 * half + k8;
         const uint64_t bd = sw128_desc(b_base + (kk / 4) * N * 128 + (kk % 4) * 32);
         mma_f16(tmem + d_col, tmem + a_col + 8 * kk, bd, kIdesc, k8 > 0 ? 1u : acc0);
-        if (kOneAcc && half == 0 && k8 == 0) {
-          // K half 1's MMAs may follow once the accumulator-initialising one is issued
-          // (tensor-core operations ordered across threads through the fence and the
-          // mbarrier); the two halves then accumulate interleaved
-          tc_fence_before();
-          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&h0_done[buf])) : "memory");
-        }
       }
       mma_commit(&d_full[buf]);
       mma_commit(&a_empty[buf * 2 + half]);
+      if (kOneAcc && half == 0) {
+        // K half 1's MMAs are issued after all of these (tensor-core operations ordered
+        // across threads through the fence and the mbarrier): a fixed summation order,
+        // so the walk is deterministic
+        tc_fence_before();
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&h0_done[buf])) : "memory");
+      }
       last_issued = g;
     };
     if (producer) {
@@ -574,6 +592,7 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
       const int cb = half * NC;                                 // first column of the warp
       const int ncol = max(0, min(NC, p.bs - cb));              // live columns (uniform)
       const int ew = warp - 8;
+      [[maybe_unused]] const uint32_t wg = ROWS ? static_cast<uint32_t>(*gmask_s >> cb) : 0u;  // greedy columns
       uint16_t* stage_s = base_stage + static_cast<size_t>(ew) * 2 * NC * 32;  // [2][NC][32]
       // request rows whose previous token was out of range are skipped
       const uint32_t live = __ballot_sync(kFull, lane < ncol && prev_s[cb + min(lane, NC - 1)] >= 0);
@@ -688,7 +707,10 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
             }
             if constexpr (PROB) {
               const float lb = bf16_to_f32(lh);
-              sc[k] = p.temp_is_one ? lb : __fmul_rn(lb, p.inv_temperature);
+              if constexpr (ROWS)  // greedy rows of a mixed batch score the fp32 logit
+                sc[k] = ((wg >> j) & 1u) ? l : __fmul_rn(lb, invT_s[cb + j]);
+              else  // 1/T = 1 multiplies exactly
+                sc[k] = __fmul_rn(lb, p.inv_temperature);
             } else {
               sc[k] = l;
             }
@@ -706,7 +728,8 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
                              gumbel_from_word(w.w)};
               transpose4(g4, lane);
 #pragma unroll
-              for (int r = 0; r < 4; ++r) sc[4 * h4 + r] = __fadd_rn(sc[4 * h4 + r], g4[r]);
+              for (int r = 0; r < 4; ++r)
+                if (!ROWS || !((wg >> (cc * CHG + 4 * h4 + r)) & 1u)) sc[4 * h4 + r] = __fadd_rn(sc[4 * h4 + r], g4[r]);
             }
           }
 #pragma unroll
@@ -860,21 +883,25 @@ __global__ void __launch_bounds__(walk_tc_threads(N), 1) walk_tc_kernel(const __
   if (ok) finish_walk(p.sync, p.K, p.bs, flag);
 }
 
-const void* walk_tc_kernel_ptr(bool int8, bool prob, bool logits, int nq) {
-#define DSPARK_TC(I, P, L)                                                  \
-  if (int8 == I && prob == P && logits == L) {                              \
-    if (nq == 4) return (const void*)walk_tc_kernel<I, P, L, 16>;           \
-    if (nq == 8) return (const void*)walk_tc_kernel<I, P, L, 32>;           \
-    return (const void*)walk_tc_kernel<I, P, L, 64>;                        \
+const void* walk_tc_kernel_ptr(bool int8, bool prob, bool logits, int nq, bool rows) {
+#define DSPARK_TC(I, P, L, R)                                                  \
+  if (int8 == I && prob == P && logits == L && rows == R) {                    \
+    if (nq == 4) return (const void*)walk_tc_kernel<I, P, L, 16, R>;           \
+    if (nq == 8) return (const void*)walk_tc_kernel<I, P, L, 32, R>;           \
+    return (const void*)walk_tc_kernel<I, P, L, 64, R>;                        \
   }
-  DSPARK_TC(true, false, false)
-  DSPARK_TC(true, false, true)
-  DSPARK_TC(true, true, false)
-  DSPARK_TC(true, true, true)
-  DSPARK_TC(false, false, false)
-  DSPARK_TC(false, false, true)
-  DSPARK_TC(false, true, false)
-  DSPARK_TC(false, true, true)
+  DSPARK_TC(true, false, false, false)
+  DSPARK_TC(true, false, true, false)
+  DSPARK_TC(true, true, false, false)
+  DSPARK_TC(true, true, true, false)
+  DSPARK_TC(true, true, false, true)
+  DSPARK_TC(true, true, true, true)
+  DSPARK_TC(false, false, false, false)
+  DSPARK_TC(false, false, true, false)
+  DSPARK_TC(false, true, false, false)
+  DSPARK_TC(false, true, true, false)
+  DSPARK_TC(false, true, false, true)
+  DSPARK_TC(false, true, true, true)
 #undef DSPARK_TC
   return nullptr;
 }

@@ -103,6 +103,14 @@ typedef struct dspark_walk_args {
   uint32_t flags;      /* DSPARK_FLAG_* */
   int32_t resident_rows_cap; /* tuning: cap on smem-resident W2 rows per CTA; -1 = automatic */
   uint32_t timeout_us; /* limit of every device-side wait; 0 = 1,000,000 us */
+  /* Per-request sampling settings (both optional, device memory): */
+  const float* temperatures; /* fp32 [bs]: row b's temperature, overriding `temperature`;
+                                a probabilistic row needs T > 0 and finite, else the walk
+                                reports DSPARK_ERR_INVALID_ARG in *status_dev and writes
+                                -1 for that row's tokens */
+  const int32_t* row_modes;  /* int32 [bs]: row b's dspark_mode, overriding `mode` (then
+                                `seeds` is required); a value other than 0 / 1 is
+                                reported like an invalid temperature */
 } dspark_walk_args;
 
 /*

@@ -72,7 +72,9 @@ def test_invalid_arguments_rejected_on_host(L):
         return x
     for bad in (dict(rank=128), dict(bs=0), dict(bs=65), dict(K=0), dict(K=33), dict(V=0),
                 dict(mode=2), dict(mode=1, seeds=fake, temperature=0.0),
-                dict(mode=1, seeds=None), dict(w2q=fake), dict(top_k=1001)):
+                dict(mode=1, seeds=None), dict(w2q=fake), dict(top_k=1001),
+                dict(row_modes=fake, seeds=None),                      # per-row modes need seeds
+                dict(row_modes=fake, seeds=fake, temperature=0.0)):    # ... and a valid scalar T
         assert L.dspark_walk(C.byref(args(**bad)), None) == 1, bad
     assert L.dspark_walk(C.byref(args(workspace_bytes=16)), None) == 8
     assert L.dspark_walk(C.byref(args(workspace=None)), None) == 8

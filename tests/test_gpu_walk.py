@@ -281,6 +281,94 @@ def test_workspace_left_zeroed_and_reusable(bs):
         assert torch.equal(t, ref)
 
 
+@pytest.mark.parametrize("bs,path", [(2, "default"), (6, "default"), (40, "default"),
+                                     (6, "cuda_cores"), (2, "tensor_cores")])
+@pytest.mark.parametrize("int8", [True, False])
+def test_per_row_modes_and_temperatures(oracle, bs, path, int8):
+    """Per-request mode and temperature in one walk: every group of rows with the same
+    (mode, T) matches the oracle run with that mode and T, and every row equals the same
+    row of a walk that gives all rows its settings (bit for bit: tokens and logits)."""
+    V, K = 5003, 4
+    inp = synth.make(V, bs, K, seed=70 + bs, peak=8.0)
+    w1, w2, base, prev, seeds = to_dev(inp)
+    okw, wk = {}, dict(w2=w2)
+    if int8:
+        q, sc = capi.quantize_w2(w2)
+        _, q_ref, sc_ref = oracle.quantize_w2(bits(inp.w2))
+        wk, okw = dict(w2q=q, scales=sc), dict(q=q_ref, sc=sc_ref)
+    Ts = [0.5, 1.0, 0.7, 1.3]
+    sampled = [b % 3 != 0 for b in range(bs)]
+    T_row = [Ts[b % 4] for b in range(bs)]
+    modes = torch.tensor([1 if s else 0 for s in sampled], dtype=torch.int32, device=DEV)
+    temps = torch.tensor(T_row, dtype=torch.float32, device=DEV)
+    flags = PATH_FLAGS.get(path, 0)
+    tokens, lg = capi.walk(base, w1, prev, seeds=seeds, temperatures=temps, row_modes=modes,
+                           want_logits=True, flags=flags, **wk)
+    torch.cuda.synchronize()
+    greedy_rows = [b for b in range(bs) if not sampled[b]]
+    check_walk(oracle, inp, tokens, mode=capi.GREEDY, gpu_logits=lg, rows=greedy_rows, **okw)
+    t_ref, l_ref = capi.walk(base, w1, prev, seeds=seeds, want_logits=True, flags=flags, **wk)
+    torch.cuda.synchronize()
+    assert torch.equal(tokens[greedy_rows], t_ref[greedy_rows])
+    assert torch.equal(lg[greedy_rows].view(torch.int16), l_ref[greedy_rows].view(torch.int16))
+    for T in Ts:
+        rows = [b for b in range(bs) if sampled[b] and T_row[b] == T]
+        if not rows:
+            continue
+        check_walk(oracle, inp, tokens, mode=capi.PROBABILISTIC, T=T, gpu_logits=lg, rows=rows, **okw)
+        t_ref, _ = capi.walk(base, w1, prev, seeds=seeds, mode=capi.PROBABILISTIC, temperature=T,
+                             flags=flags, **wk)
+        torch.cuda.synchronize()
+        assert torch.equal(tokens[rows], t_ref[rows]), T
+
+
+@pytest.mark.parametrize("bs", [3, 40])
+def test_per_row_settings_topk(oracle, bs):
+    """The top-k walk with per-request mode and temperature equals, row by row, top-k
+    walks that give every row those settings."""
+    V, K, k = 3001, 3, 17
+    inp = synth.make(V, bs, K, seed=80 + bs)
+    w1, w2, base, prev, seeds = to_dev(inp)
+    sampled = [b % 2 == 1 for b in range(bs)]
+    T_row = [0.7 if b % 4 == 1 else 1.0 for b in range(bs)]
+    modes = torch.tensor([1 if s else 0 for s in sampled], dtype=torch.int32, device=DEV)
+    temps = torch.tensor(T_row, dtype=torch.float32, device=DEV)
+    tokens, _ = capi.walk(base, w1, prev, w2=w2, seeds=seeds, top_k=k, temperatures=temps,
+                          row_modes=modes)
+    torch.cuda.synchronize()
+    for mode, T in ((capi.GREEDY, 1.0), (capi.PROBABILISTIC, 1.0), (capi.PROBABILISTIC, 0.7)):
+        rows = [b for b in range(bs) if sampled[b] == (mode == capi.PROBABILISTIC)
+                and (mode == capi.GREEDY or T_row[b] == T)]
+        if not rows:
+            continue
+        t_ref, _ = capi.walk(base, w1, prev, w2=w2, seeds=seeds, top_k=k, mode=mode, temperature=T)
+        torch.cuda.synchronize()
+        assert torch.equal(tokens[rows], t_ref[rows]), (mode, T)
+        check_walk(oracle, inp, tokens, mode=mode, T=T, top_k=k, rows=rows)
+
+
+@pytest.mark.parametrize("bs", [2, 5])
+def test_invalid_per_row_settings_reported(bs):
+    """An unknown per-row mode, or a sampled row with T <= 0 or NaN: INVALID_ARG, that
+    row's tokens are -1, the other rows (a greedy row with T = 0 among them) walk on."""
+    V, K = 4000, 3
+    inp = synth.make(V, bs, K, seed=5)
+    w1, w2, base, prev, seeds = to_dev(inp)
+    m = [0, 7] + [1] * (bs - 2)
+    T = [0.0, 1.0] + [float("nan") if b == 2 else 0.8 for b in range(2, bs)]
+    modes = torch.tensor(m, dtype=torch.int32, device=DEV)
+    temps = torch.tensor(T, dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    tokens, _ = capi.walk(base, w1, prev, w2=w2, seeds=seeds, temperatures=temps, row_modes=modes,
+                          status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    t = tokens.cpu().numpy()
+    bad = [1] + ([2] if bs > 2 else [])
+    assert all(list(t[r]) == [-1] * K for r in bad)
+    assert all(np.all(t[r] >= 0) for r in range(bs) if r not in bad)
+
+
 def test_walk_from_host_matches_device_walk():
     V, K, bs = 6000, 4, 3
     inp = synth.make(V, bs, K, seed=9)
