@@ -15,7 +15,7 @@ namespace dspark {
 
 const void* walk_cc_kernel_ptr(bool int8, bool prob, bool logits);
 const void* walk_tc_kernel_ptr(bool int8, bool prob, bool logits, int nq, bool rows);
-const void* topk_walk_kernel_ptr(bool prob, bool logits);
+const void* topk_walk_kernel_ptr(bool int8, bool prob, bool logits);
 size_t topk_walk_smem(int bs);
 cudaError_t launch_topk_select(const uint16_t* base, int64_t V, int k, int rows, int32_t* cand,
                                uint16_t* logits, cudaStream_t stream);
@@ -334,7 +334,6 @@ int32_t dspark_walk_topk(const dspark_walk_args* a, dspark_stream_t stream) {
   int32_t st = check_common(a);
   if (st != DSPARK_OK) return st;
   if (a->top_k < 1) return DSPARK_ERR_INVALID_ARG;
-  if (!a->w2) return DSPARK_ERR_UNSUPPORTED;
   DeviceCaps caps;
   if ((st = current_caps(&caps)) != DSPARK_OK) return st;
   if (!caps.coop) return DSPARK_ERR_UNSUPPORTED;
@@ -346,7 +345,7 @@ int32_t dspark_walk_topk(const dspark_walk_args* a, dspark_stream_t stream) {
   if (e != cudaSuccess) return cuda_fail(e, "topk_select_kernel launch");
   const size_t smem = topk_walk_smem(a->bs);
   const bool prob = a->mode == DSPARK_PROBABILISTIC || a->row_modes, lg = a->draft_logits != nullptr;
-  const void* fn = topk_walk_kernel_ptr(prob, lg);
+  const void* fn = topk_walk_kernel_ptr(a->w2q != nullptr, prob, lg);
   return launch_coop(fn, caps.sms, kWalkThreads, smem, p, s);
 }
 

@@ -390,7 +390,9 @@ __global__ void __launch_bounds__(kSelThreads, 3) topk_select_kernel(const uint1
 
 constexpr int kChunk = 2048;  // candidates per chunk of a CTA (its whole range at the configs)
 
-template <bool PROB, bool LOGITS>
+// INT8: the candidates' W2 rows are int8 codes (256 bytes) times the row scale, else
+// bf16 rows (512 bytes).
+template <bool INT8, bool PROB, bool LOGITS>
 __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int G = gridDim.x, cta = blockIdx.x;
@@ -411,8 +413,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
   const int64_t lo = static_cast<int64_t>(cta) * items / G;
   const int64_t hi = static_cast<int64_t>(cta + 1) * items / G;
   const bool skip0 = (p.sync.flags & DSPARK_FLAG_SKIP_ARRIVAL_CTA0) && cta == 0;
-  const unsigned char* w2g = reinterpret_cast<const unsigned char*>(p.w2);
-  constexpr int kRowBytes = 2 * kRank;
+  const unsigned char* w2g = INT8 ? reinterpret_cast<const unsigned char*>(p.w2q)
+                                  : reinterpret_cast<const unsigned char*>(p.w2);
+  constexpr int kRowBytes = INT8 ? kRank : 2 * kRank;
+  constexpr int kLaneChunks = kRowBytes / 16 / 8;  // 16-byte chunks j8 + 8 c of a row per lane
 
   for (int t = tid; t < p.bs; t += blockDim.x) {
     const int32_t tok = p.prev[t];
@@ -491,6 +495,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
                                               (c_hi - first_end) / p.top_k + 1);  // upper bound
       int cur_b = -1;
       float ef[32];
+      bool samp_b = false;  // row cur_b's sampling settings
+      float T_b = 1.0f;
       for (int task = grp; task < ntask; task += kGroups) {
         // task -> [e0, e1) in chunk numbering, all in row b
         int64_t s0;
@@ -516,37 +522,55 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
         const int e0 = static_cast<int>(s0 - c_lo);
         const int nt = static_cast<int>(e_end - s0 < 8 ? e_end - s0 : 8);
         if (b != cur_b) {
+          // the lane's 32 embedding values: positions 16 (j8 + 8 c) .. + 15 (int8 chunks
+          // of 16 codes) or 8 (j8 + 8 c) .. + 7 (bf16 chunks of 8 values)
+          constexpr int kPer = 32 / kLaneChunks;  // values per chunk
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float4 lo4 = *reinterpret_cast<const float4*>(e_s + static_cast<size_t>(b) * kRank + (j8 + 8 * c) * 8);
-            const float4 hi4 = *reinterpret_cast<const float4*>(e_s + static_cast<size_t>(b) * kRank + (j8 + 8 * c) * 8 + 4);
-            ef[8 * c + 0] = lo4.x; ef[8 * c + 1] = lo4.y; ef[8 * c + 2] = lo4.z; ef[8 * c + 3] = lo4.w;
-            ef[8 * c + 4] = hi4.x; ef[8 * c + 5] = hi4.y; ef[8 * c + 6] = hi4.z; ef[8 * c + 7] = hi4.w;
-          }
+          for (int c = 0; c < kLaneChunks; ++c)
+#pragma unroll
+            for (int f = 0; f < kPer / 4; ++f) {
+              const float4 x4 = *reinterpret_cast<const float4*>(e_s + static_cast<size_t>(b) * kRank +
+                                                                 (j8 + 8 * c) * kPer + 4 * f);
+              ef[kPer * c + 4 * f + 0] = x4.x; ef[kPer * c + 4 * f + 1] = x4.y;
+              ef[kPer * c + 4 * f + 2] = x4.z; ef[kPer * c + 4 * f + 3] = x4.w;
+            }
+          samp_b = row_sampled(p, PROB, b);
+          T_b = samp_b ? row_temperature(p, b) : 1.0f;
           cur_b = b;
         }
         float part[8];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {  // two batches of 4 rows: 16 loads in flight per lane
-          uint4 q[4][4];
+          uint4 q[4][kLaneChunks];
 #pragma unroll
           for (int rr = 0; rr < 4; ++rr) {
             const int r = 4 * h + rr;
             const unsigned char* row = w2g + static_cast<size_t>(it_v[e0 + min(r, nt - 1)]) * kRowBytes;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < kLaneChunks; ++c)
               q[rr][c] = r < nt ? __ldg(reinterpret_cast<const uint4*>(row) + j8 + 8 * c) : make_uint4(0, 0, 0, 0);
           }
 #pragma unroll
           for (int rr = 0; rr < 4; ++rr) {
             float a = 0.f;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < kLaneChunks; ++c) {
               const uint32_t qw[4] = {q[rr][c].x, q[rr][c].y, q[rr][c].z, q[rr][c].w};
 #pragma unroll
               for (int w = 0; w < 4; ++w) {
-                a = __fmaf_rn(bf16_lo(qw[w]), ef[8 * c + 2 * w], a);
-                a = __fmaf_rn(bf16_hi(qw[w]), ef[8 * c + 2 * w + 1], a);
+                if constexpr (INT8) {
+                  // 4 codes, each exact in fp32 (the row scale comes later): the biased
+                  // byte q + 128 as the mantissa of 2^23 + q + 128, minus 2^23 + 128
+                  const uint32_t bw = qw[w] ^ 0x80808080u;
+#pragma unroll
+                  for (int e8 = 0; e8 < 4; ++e8) {
+                    const float f = __fsub_rn(__uint_as_float(__byte_perm(bw, 0x4B000000u, 0x7650u + e8)), 8388736.0f);
+                    a = __fmaf_rn(f, ef[16 * c + 4 * w + e8], a);
+                  }
+                } else {
+                  a = __fmaf_rn(bf16_lo(qw[w]), ef[8 * c + 2 * w], a);
+                  a = __fmaf_rn(bf16_hi(qw[w]), ef[8 * c + 2 * w + 1], a);
+                }
               }
             }
             part[4 * h + rr] = a;
@@ -569,19 +593,19 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
         }
         const float send = u1 ? part[0] : part[1];
         const float keep = u1 ? part[1] : part[0];
-        const float bias = keep + __shfl_xor_sync(gmask, send, 1);
+        float bias = keep + __shfl_xor_sync(gmask, send, 1);
 
         if (j8 < nt) {
           const int e = e0 + j8;
           const int64_t v = it_v[e];
+          if constexpr (INT8) bias = __fmul_rn(bias, __ldg(p.scales + v));
           const float l = __fadd_rn(it_base[e], bias);
           const uint16_t lh = f32_to_bf16_bits(l);
           if (LOGITS) p.logits[(static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v] = lh;
           float sco = l;
-          if (row_sampled(p, PROB, b)) {
+          if (samp_b) {
             const float lb = bf16_to_f32(lh);
-            const float T = row_temperature(p, b);
-            const float xs = T == 1.0f ? lb : __fdiv_rn(lb, T);
+            const float xs = T_b == 1.0f ? lb : __fdiv_rn(lb, T_b);
             sco = __fadd_rn(xs, it_g[e]);
           }
           atomicMax(reinterpret_cast<unsigned long long*>(&best_s[b]),
@@ -623,9 +647,19 @@ size_t topk_walk_smem(int bs) {
   return static_cast<size_t>(bs) * kRank * 4 + 3 * kChunk * 4 + 64 * 4 + 64 * 8 + 16 + 128;
 }
 
-const void* topk_walk_kernel_ptr(bool prob, bool logits) {
-  if (prob) return logits ? (const void*)topk_walk_kernel<true, true> : (const void*)topk_walk_kernel<true, false>;
-  return logits ? (const void*)topk_walk_kernel<false, true> : (const void*)topk_walk_kernel<false, false>;
+const void* topk_walk_kernel_ptr(bool int8, bool prob, bool logits) {
+#define DSPARK_TK(I, P, L) \
+  if (int8 == I && prob == P && logits == L) return (const void*)topk_walk_kernel<I, P, L>;
+  DSPARK_TK(true, true, true)
+  DSPARK_TK(true, true, false)
+  DSPARK_TK(true, false, true)
+  DSPARK_TK(true, false, false)
+  DSPARK_TK(false, true, true)
+  DSPARK_TK(false, true, false)
+  DSPARK_TK(false, false, true)
+  DSPARK_TK(false, false, false)
+#undef DSPARK_TK
+  return nullptr;
 }
 
 cudaError_t launch_topk_select(const uint16_t* base, int64_t V, int k, int rows, int32_t* cand,

@@ -94,7 +94,7 @@ typedef struct dspark_walk_args {
   int32_t K;           /* 1 .. DSPARK_MAX_K */
   int32_t mode;        /* dspark_mode */
   float temperature;   /* > 0 and finite in probabilistic mode; 1.0 skips the divide */
-  int32_t top_k;       /* 0: full vocabulary; 1..V: top-k walk (bf16 w2 only) */
+  int32_t top_k;       /* 0: full vocabulary; 1..V: top-k walk */
   int32_t* draft_tokens;
   uint16_t* draft_logits;
   void* workspace;
@@ -144,7 +144,9 @@ int32_t dspark_walk(const dspark_walk_args* args, dspark_stream_t stream);
  * smaller index), the bias is computed for those candidates only (bf16 W2 rows
  * gathered), and the step's argmax or sample runs over the dense row that is -inf
  * off the candidates. Gumbel noise is keyed by the vocabulary id, so top_k == V
- * reproduces dspark_walk. Requires bf16 w2; int8 returns DSPARK_ERR_UNSUPPORTED.
+ * reproduces dspark_walk. W2 bf16, or int8 codes with per-row scales (the gathered
+ * candidate rows are then 256-byte int8 rows, the bias scale_v times their dot
+ * product with the embedding).
  */
 int32_t dspark_walk_topk(const dspark_walk_args* args, dspark_stream_t stream);
 

@@ -284,7 +284,6 @@ int32_t oracle_walk(const oracle_walk_args* a) {
   if (a->mode == 1 && (!a->seeds || !(a->temperature > 0.0f) || !std::isfinite(a->temperature)))
     return ORACLE_INVALID_ARG;
   if (a->top_k < 0 || a->top_k > a->V) return ORACLE_INVALID_ARG;
-  if (a->top_k > 0 && int8_w2) return ORACLE_UNSUPPORTED;
   std::fesetround(FE_TONEAREST);
 #ifdef _OPENMP
   const int nthreads = a->nthreads > 0 ? a->nthreads : 1;

@@ -78,7 +78,6 @@ def test_invalid_arguments_rejected_on_host(L):
         assert L.dspark_walk(C.byref(args(**bad)), None) == 1, bad
     assert L.dspark_walk(C.byref(args(workspace_bytes=16)), None) == 8
     assert L.dspark_walk(C.byref(args(workspace=None)), None) == 8
-    assert L.dspark_walk_topk(C.byref(args(w2=None, w2q=fake, w2_scales=fake, top_k=5)), None) == 2
     assert L.dspark_quantize_w2(None, 10, 256, None, None, None, None) == 1
     assert L.dspark_quantize_w2(fake, 10, 255, fake, fake, None, None) == 1
     assert L.dspark_gumbel_noise(None, 1, 1, 10, None, None, None) == 1

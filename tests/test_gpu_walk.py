@@ -399,14 +399,20 @@ def test_walk_from_host_matches_device_walk():
 @pytest.mark.parametrize("k", [1, 17, 300])
 @pytest.mark.parametrize("mode,T", [(capi.GREEDY, 1.0), (capi.PROBABILISTIC, 1.0),
                                     (capi.PROBABILISTIC, 0.7)])
-def test_topk_small_parity(oracle, k, mode, T):
+@pytest.mark.parametrize("int8", [False, True])
+def test_topk_small_parity(oracle, k, mode, T, int8):
     V, K, bs = 3001, 3, 5
     inp = synth.make(V, bs, K, seed=20 + k)
     w1, w2, base, prev, seeds = to_dev(inp)
-    tokens, lg = capi.walk(base, w1, prev, w2=w2, seeds=seeds, mode=mode, temperature=T,
-                           top_k=k, want_logits=True)
+    wk, okw = dict(w2=w2), {}
+    if int8:  # int8 codes with per-row scales: 256-byte gathered rows
+        q, sc = capi.quantize_w2(w2)
+        _, q_ref, sc_ref = oracle.quantize_w2(bits(inp.w2))
+        wk, okw = dict(w2q=q, scales=sc), dict(q=q_ref, sc=sc_ref)
+    tokens, lg = capi.walk(base, w1, prev, seeds=seeds, mode=mode, temperature=T,
+                           top_k=k, want_logits=True, **wk)
     torch.cuda.synchronize()
-    check_walk(oracle, inp, tokens, mode=mode, T=T, top_k=k, gpu_logits=lg)
+    check_walk(oracle, inp, tokens, mode=mode, T=T, top_k=k, gpu_logits=lg, **okw)
 
 
 @pytest.mark.parametrize("case", ["sampled", "ranked_ties", "wide_tie", "overflow"])

@@ -376,6 +376,32 @@ def test_topk_full_vocab_equals_dense(oracle):
             assert mask[part.tokens[r, i]]
 
 
+def test_topk_full_vocab_equals_dense_int8(oracle):
+    """int8 W2 in the top-k walk: the candidates' bias is the dense int8 walk's, so
+    k = V reproduces the dense int8 walk and every other k scores only candidates."""
+    V, R, K, bs = 300, 16, 4, 3
+    g = torch.Generator().manual_seed(4)
+    w1 = torch.randn(V, R, generator=g).to(torch.bfloat16)
+    q = torch.randint(-127, 128, (V, R), generator=g, dtype=torch.int64).to(torch.int8).numpy()
+    sc = (torch.rand(V, generator=g) / 64).numpy().astype(np.float32)
+    base = (torch.randn(bs, K, V, generator=g) * 3).to(torch.bfloat16)
+    prev = np.array([4, 5, 6], np.int32)
+    for mode in (oracle.GREEDY, oracle.PROBABILISTIC):
+        kw = dict(w2q=q, scales=sc, seeds=np.arange(bs, dtype=np.uint64), mode=mode,
+                  temperature=0.9, want_logits=True)
+        dense = oracle.walk(WalkBits(base), WalkBits(w1), prev, K, **kw)
+        full = oracle.walk(WalkBits(base), WalkBits(w1), prev, K, top_k=V, **kw)
+        assert dense.status == 0 and full.status == 0
+        np.testing.assert_array_equal(dense.tokens, full.tokens)
+        np.testing.assert_array_equal(dense.logits, full.logits)
+        part = oracle.walk(WalkBits(base), WalkBits(w1), prev, K, top_k=5, want_cand=True, **kw)
+        for r in range(bs):
+            for i in range(K):
+                mask = np.zeros(V, bool)
+                mask[part.cand[r, i]] = True
+                assert np.all(np.isneginf(part.logits[r, i][~mask])) and mask[part.tokens[r, i]]
+
+
 # ---------------------------------------------------------------- errors and follow classes
 
 def test_bad_token_and_invalid_args(oracle):
