@@ -271,6 +271,32 @@ def time_walks(cfg, steps, warmup, dev, flush):
     return times, t, args
 
 
+def time_graph(args, steps, flush):
+    """The same walk captured once in a CUDA graph and replayed: per-replay CUDA-event
+    times (ms), the L2 flushed before each replay (outside the events), as the pages'
+    kernel benchmark replays a graph of one walk."""
+    from dspark_markov_draft_gb300 import capi
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st = capi.walk_args_call(args, torch.cuda.current_stream())
+    if st:
+        raise RuntimeError(f"walk capture failed: {capi.STATUS.get(st, st)}")
+    for _ in range(3):
+        flush.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for s, e in evs:
+        flush.zero_()
+        s.record(stream)
+        g.replay()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in evs]
+
+
 def time_e2e(cfg, t, args, steps, dev):
     """Walk through dspark_walk_from_host: per-step H2D of base/prev/seeds from pinned
     host memory, the walk, D2H of the tokens; timed with events around all of it."""
@@ -490,6 +516,7 @@ def main():
     value = job_throughput(ms, world, toks)
 
     e2e_ms, h2d, d2h = (float("nan"), 0, 0) if a.no_e2e else time_e2e(cfg, t, args, max(3, a.steps // 2), dev)
+    graph_times = time_graph(args, max(5, a.steps), flush)  # outside the timed region
     fl, res_rows = floors_of(cfg)
     us = 1000 * ms
     roof = roofline(cfg, peaks, fl, us, sms)
@@ -538,6 +565,8 @@ def main():
                        "l2": "flushed before every walk (256 MB write)",
                        "parallelism": f"replicas x{world}"},
             "us_per_walk": us,
+            "graph": {"us_per_walk": 1000 * statistics.median(graph_times), "replays": len(graph_times),
+                      "l2": "flushed before every replay"},
             "roofline": roof,
             "floors": floor_rec,
             "cpu_baseline": cpu,

@@ -369,6 +369,41 @@ def test_invalid_per_row_settings_reported(bs):
     assert all(np.all(t[r] >= 0) for r in range(bs) if r not in bad)
 
 
+@pytest.mark.parametrize("bs,top_k", [(1, 0), (5, 0), (40, 0), (3, 17)])
+def test_walk_captured_in_cuda_graph(bs, top_k):
+    """The walk captured in a CUDA graph and replayed: every replay equals an eager walk
+    on the inputs the graph's buffers hold at replay time (the workspace returns to zero
+    after each replay)."""
+    V, K = 6000, 4
+    inp = synth.make(V, bs, K, seed=90 + bs)
+    w1, w2, base, prev, seeds = to_dev(inp)
+    tokens = torch.empty((bs, K), dtype=torch.int32, device=DEV)
+    logits = torch.empty((bs, K, V), dtype=torch.bfloat16, device=DEV)
+    ws = capi.alloc_workspace(V, bs, K, top_k)
+    a = capi.make_args(base, w1, prev, tokens, ws, w2=w2, seeds=seeds, mode=capi.PROBABILISTIC,
+                       temperature=0.8, top_k=top_k, logits=logits)
+    assert capi.walk_args_call(a) == 0  # eager first: device query and kernel attributes
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        assert capi.walk_args_call(a, torch.cuda.current_stream()) == 0
+    other = synth.make(V, bs, K, seed=190 + bs)
+    for step in range(3):
+        if step == 1:  # new inputs in the captured buffers
+            base.copy_(other.base.to(DEV))
+            prev.copy_(other.prev.to(DEV))
+        tokens.fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        ref, lref = capi.walk(base, w1, prev, w2=w2, seeds=seeds, mode=capi.PROBABILISTIC,
+                              temperature=0.8, top_k=top_k, want_logits=True)
+        torch.cuda.synchronize()
+        assert torch.equal(tokens, ref), step
+        assert torch.equal(logits.view(torch.int16), lref.view(torch.int16)), step
+        if top_k == 0:  # (the top-k candidate lists stay in the workspace)
+            assert int(ws.count_nonzero()) == 0
+
+
 def test_walk_from_host_matches_device_walk():
     V, K, bs = 6000, 4, 3
     inp = synth.make(V, bs, K, seed=9)
