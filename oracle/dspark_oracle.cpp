@@ -107,9 +107,11 @@ void philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]
   out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
 }
 
-uint32_t philox_word(uint64_t seed, int32_t b, int32_t i, int64_t v) {
+// Counter (v >> 2, i, b, domain), word v & 3. Domain 0: the drafter's Gumbel noise;
+// 1: the verifier's acceptance uniforms (v = 0); 2: the verifier's resampling noise.
+uint32_t philox_word(uint64_t seed, int32_t b, int32_t i, int64_t v, uint32_t domain = 0u) {
   const uint32_t ctr[4] = {static_cast<uint32_t>(v >> 2), static_cast<uint32_t>(i),
-                           static_cast<uint32_t>(b), 0u};
+                           static_cast<uint32_t>(b), domain};
   const uint32_t key[2] = {static_cast<uint32_t>(seed & 0xFFFFFFFFull),
                            static_cast<uint32_t>(seed >> 32)};
   uint32_t out[4];
@@ -125,6 +127,12 @@ float uniform_from_word(uint32_t w) {
 
 double gumbel(uint64_t seed, int32_t b, int32_t i, int64_t v) {
   const double u = static_cast<double>(uniform_from_word(philox_word(seed, b, i, v)));
+  return -std::log(-std::log(u));
+}
+
+// The verifier's resampling noise (counter domain 2).
+double gumbel_d(uint64_t seed, int32_t b, int32_t i, int64_t v) {
+  const double u = static_cast<double>(uniform_from_word(philox_word(seed, b, i, v, 2u)));
   return -std::log(-std::log(u));
 }
 
@@ -398,6 +406,105 @@ int32_t oracle_walk(const oracle_walk_args* a) {
     }
   }
   return status;
+}
+
+// ---------------------------------------------------------------- verification
+//
+// Speculative sampling verification of K drafted tokens (Leviathan, Kalman, Matias,
+// "Fast Inference from Transformers via Speculative Decoding", ICML 2023, Algorithm 1;
+// Chen et al., "Accelerating Large Language Model Decoding with Speculative Sampling",
+// 2023), consuming the draft_logits the walk kept (vLLM PR #62958, "Details": the bf16
+// draft logits are the distribution the draft tokens were sampled from).
+//   q_i = softmax(draft[b, i, :] / T), p_i = softmax(target[b, i, :] / T);
+//   for i = 0 .. K-1: u_i uniform (domain 1); accept d_i iff u_i q_i(d_i) < p_i(d_i);
+//     at the first rejection emit a sample of norm(max(0, p_i - q_i)) and stop;
+//   all accepted: emit a sample of p_K.
+// Samples by Gumbel-max with domain-2 noise: residual scores log(p - q) + g where
+// p > q (if p > q nowhere, the scores of p: target / T + g), bonus target / T + g.
+struct oracle_verify_args {
+  const uint16_t* target;    // [bs, K+1, V] bf16 target logits
+  const uint16_t* draft;     // [bs, K, V] bf16 draft logits
+  const int32_t* dtok;       // [bs, K] draft tokens
+  const uint64_t* seeds;     // [bs]
+  const int32_t* slot;       // [bs] batch slot b in the Philox counter, or null (= row)
+  int64_t V;
+  int32_t bs, K;
+  float temperature;
+  int32_t* accepted;         // [bs] accepted draft tokens
+  int32_t* out_tokens;       // [bs, K+1] accepted drafts, the emitted sample, then -1
+  double* p_out;             // optional [bs, K+1, V] target probabilities
+  double* q_out;             // optional [bs, K, V] draft probabilities
+  double* u_out;             // optional [bs, K] acceptance uniforms
+  double* ratio_out;         // optional [bs, K] p_i(d_i) and q_i(d_i): ratio_out = p, qd_out = q
+  double* qd_out;            // optional [bs, K]
+  int32_t* y_out;            // optional [bs, K+1] the sample of every position (residual / bonus)
+  double* gap_out;           // optional [bs, K+1] its top-2 score gap
+  double* score_out;         // optional [bs, K+1, V] the sampling scores
+};
+
+int32_t oracle_verify(const oracle_verify_args* a) {
+  if (!a || !a->target || !a->draft || !a->dtok || !a->seeds || !a->accepted || !a->out_tokens)
+    return ORACLE_INVALID_ARG;
+  if (a->V <= 0 || a->bs <= 0 || a->K <= 0 || !(a->temperature > 0.0f) || !std::isfinite(a->temperature))
+    return ORACLE_INVALID_ARG;
+  const int64_t V = a->V;
+  const int32_t K = a->K;
+  const double T = static_cast<double>(a->temperature);
+  const double ninf = -std::numeric_limits<double>::infinity();
+  std::vector<double> p(V), q(V), s(V);
+  // softmax of a bf16 row divided by T (all zero when the row is -inf everywhere)
+  auto softmax = [&](const uint16_t* row, std::vector<double>& out) {
+    double m = ninf;
+    for (int64_t v = 0; v < V; ++v) m = std::max(m, bf16_bits_to_double(row[v]) / T);
+    double z = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+      out[v] = m == ninf ? 0.0 : std::exp(bf16_bits_to_double(row[v]) / T - m);
+      z += out[v];
+    }
+    for (int64_t v = 0; v < V; ++v) out[v] = z > 0.0 ? out[v] / z : 0.0;
+  };
+  for (int32_t r = 0; r < a->bs; ++r) {
+    const int32_t b = a->slot ? a->slot[r] : r;
+    const uint64_t seed = a->seeds[r];
+    int32_t n_acc = -1;  // first rejected position, -1 while all accepted
+    for (int32_t i = 0; i <= K; ++i) {
+      const uint16_t* trow = a->target + (static_cast<size_t>(r) * (K + 1) + i) * V;
+      softmax(trow, p);
+      if (a->p_out) std::copy(p.begin(), p.end(), a->p_out + (static_cast<size_t>(r) * (K + 1) + i) * V);
+      bool residual = false;
+      if (i < K) {
+        softmax(a->draft + (static_cast<size_t>(r) * K + i) * V, q);
+        if (a->q_out) std::copy(q.begin(), q.end(), a->q_out + (static_cast<size_t>(r) * K + i) * V);
+        const int32_t d = a->dtok[static_cast<size_t>(r) * K + i];
+        const double u = static_cast<double>(uniform_from_word(philox_word(seed, b, i, 0, 1u)));
+        const double pd = (d >= 0 && d < V) ? p[d] : 0.0, qd = (d >= 0 && d < V) ? q[d] : 0.0;
+        if (a->u_out) a->u_out[static_cast<size_t>(r) * K + i] = u;
+        if (a->ratio_out) a->ratio_out[static_cast<size_t>(r) * K + i] = pd;
+        if (a->qd_out) a->qd_out[static_cast<size_t>(r) * K + i] = qd;
+        if (n_acc < 0 && !(u * qd < pd)) n_acc = i;
+        for (int64_t v = 0; v < V; ++v) {
+          const double rv = p[v] - q[v];
+          s[v] = rv > 0.0 ? std::log(rv) + gumbel_d(seed, b, i, v) : ninf;
+          residual = residual || rv > 0.0;
+        }
+      }
+      if (!residual)  // bonus position, or p > q nowhere: a sample of p
+        for (int64_t v = 0; v < V; ++v) s[v] = bf16_bits_to_double(trow[v]) / T + gumbel_d(seed, b, i, v);
+      const int64_t y = argmax_first(s);
+      if (a->y_out) a->y_out[static_cast<size_t>(r) * (K + 1) + i] = static_cast<int32_t>(y);
+      if (a->gap_out) a->gap_out[static_cast<size_t>(r) * (K + 1) + i] = top2_gap(s, y);
+      if (a->score_out) std::copy(s.begin(), s.end(), a->score_out + (static_cast<size_t>(r) * (K + 1) + i) * V);
+      const int32_t n = n_acc < 0 ? K : n_acc;
+      if (i == n) {  // the emitted sample (first rejection, or the bonus)
+        int32_t* out = a->out_tokens + static_cast<size_t>(r) * (K + 1);
+        for (int32_t j = 0; j < n; ++j) out[j] = a->dtok[static_cast<size_t>(r) * K + j];
+        out[n] = static_cast<int32_t>(y);
+        for (int32_t j = n + 1; j <= K; ++j) out[j] = -1;
+        a->accepted[r] = n;
+      }
+    }
+  }
+  return ORACLE_OK;
 }
 
 }  // extern "C"

@@ -179,3 +179,54 @@ def walk(base_bits, w1_bits, prev, K: int, *, w2_bits=None, w2q=None, scales=Non
         _ptr(cand))
     st = lib().oracle_walk(C.byref(args))
     return WalkResult(int(st), tokens, gap, best, fcls, logits, lbf, scores, cand)
+
+
+class _VerifyArgs(C.Structure):
+    _fields_ = [
+        ("target", C.c_void_p), ("draft", C.c_void_p), ("dtok", C.c_void_p), ("seeds", C.c_void_p),
+        ("slot", C.c_void_p), ("V", C.c_int64), ("bs", C.c_int32), ("K", C.c_int32),
+        ("temperature", C.c_float), ("accepted", C.c_void_p), ("out_tokens", C.c_void_p),
+        ("p_out", C.c_void_p), ("q_out", C.c_void_p), ("u_out", C.c_void_p),
+        ("ratio_out", C.c_void_p), ("qd_out", C.c_void_p), ("y_out", C.c_void_p),
+        ("gap_out", C.c_void_p), ("score_out", C.c_void_p),
+    ]
+
+
+@dataclass
+class VerifyResult:
+    status: int
+    accepted: np.ndarray      # [bs]
+    out_tokens: np.ndarray    # [bs, K+1]
+    u: np.ndarray             # [bs, K] acceptance uniforms
+    p_d: np.ndarray           # [bs, K] target probability of each draft token
+    q_d: np.ndarray           # [bs, K] draft probability of each draft token
+    y: np.ndarray             # [bs, K+1] sample of every position (residual, or bonus at K)
+    gap: np.ndarray           # [bs, K+1] its top-2 score gap
+    p: np.ndarray | None      # [bs, K+1, V]
+    q: np.ndarray | None      # [bs, K, V]
+    scores: np.ndarray | None  # [bs, K+1, V]
+
+
+def verify(target_bits, draft_bits, dtok, seeds, temperature: float, *, slot=None,
+           want_probs: bool = False) -> VerifyResult:
+    """Speculative-sampling verification of the draft tokens (see oracle_verify)."""
+    t = _c(target_bits, np.uint16)
+    d = _c(draft_bits, np.uint16)
+    tk = _c(dtok, np.int32)
+    sd = _c(seeds, np.uint64)
+    sl = _c(slot, np.int32)
+    bs, K1, V = t.shape
+    K = K1 - 1
+    assert d.shape == (bs, K, V) and tk.shape == (bs, K)
+    acc = np.zeros(bs, np.int32)
+    out = np.zeros((bs, K + 1), np.int32)
+    u = np.zeros((bs, K)); pd = np.zeros((bs, K)); qd = np.zeros((bs, K))
+    y = np.zeros((bs, K + 1), np.int32); gap = np.zeros((bs, K + 1))
+    p = np.zeros((bs, K + 1, V)) if want_probs else None
+    q = np.zeros((bs, K, V)) if want_probs else None
+    sc = np.zeros((bs, K + 1, V)) if want_probs else None
+    a = _VerifyArgs(_ptr(t), _ptr(d), _ptr(tk), _ptr(sd), _ptr(sl), V, bs, K, temperature,
+                    _ptr(acc), _ptr(out), _ptr(p), _ptr(q), _ptr(u), _ptr(pd), _ptr(qd), _ptr(y),
+                    _ptr(gap), _ptr(sc))
+    st = lib().oracle_verify(C.byref(a))
+    return VerifyResult(int(st), acc, out, u, pd, qd, y, gap, p, q, sc)
