@@ -297,6 +297,44 @@ def time_graph(args, steps, flush):
     return [s.elapsed_time(e) for s, e in evs]
 
 
+def time_verify(dev, flush, peaks, steps, V=151936, K=7, bs=64, T=1.0):
+    """Speculative-sampling verification of K drafted tokens per row (dspark_verify) on
+    synthetic bf16 logits: draft logits N(0, 3^2), target logits the draft logits plus
+    N(0, 0.3^2) noise (so that acceptances and rejections both occur), an independent
+    bonus row, draft tokens drawn from softmax(draft / T). Per-call CUDA-event times
+    with the L2 flushed before each call; the floor is one read of both logit tensors."""
+    from dspark_markov_draft_gb300 import capi
+    g = torch.Generator(device=dev).manual_seed(7)
+    drf = (torch.randn(bs, K, V, generator=g, device=dev) * 3).to(torch.bfloat16)
+    tgt = (torch.cat([drf.float(), torch.randn(bs, 1, V, generator=g, device=dev) * 3], 1)
+           + torch.randn(bs, K + 1, V, generator=g, device=dev) * 0.3).to(torch.bfloat16)
+    q = torch.softmax(drf.float() / T, -1)
+    dtok = torch.stack([torch.multinomial(q[:, i], 1, generator=g)[:, 0] for i in range(K)], 1).to(torch.int32)
+    del q
+    seeds = torch.arange(bs, device=dev, dtype=torch.int64) * 3 + 1
+    acc = torch.empty(bs, dtype=torch.int32, device=dev)
+    out = torch.empty((bs, K + 1), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        flush.zero_()
+        capi.verify(tgt, drf, dtok, seeds, T, accepted=acc, out_tokens=out, stream=stream)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s, e in evs:
+        flush.zero_()
+        s.record(stream)
+        capi.verify(tgt, drf, dtok, seeds, T, accepted=acc, out_tokens=out, stream=stream)
+        e.record(stream)
+    torch.cuda.synchronize()
+    us = 1000 * statistics.median([s.elapsed_time(e) for s, e in evs])
+    nbytes = (tgt.numel() + drf.numel()) * 2
+    floor_us = nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+    return {"workload": f"verify v{V} k{K} bs{bs} T={T}", "us_per_call": us, "calls": steps,
+            "hbm_bytes": nbytes, "floor_us": floor_us, "frac_of_floor": floor_us / us,
+            "mean_accepted": float(acc.float().mean()), "kernels_per_call": 3,
+            "l2": "flushed before every call"}
+
+
 def time_e2e(cfg, t, args, steps, dev):
     """Walk through dspark_walk_from_host: per-step H2D of base/prev/seeds from pinned
     host memory, the walk, D2H of the tokens; timed with events around all of it."""
@@ -466,6 +504,7 @@ def main():
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-verify", action="store_true")
     ap.add_argument("--workload", default=MAIN["name"],
                     help="run this workload as the main line (one of the built-in names)")
     a = ap.parse_args()
@@ -517,6 +556,7 @@ def main():
 
     e2e_ms, h2d, d2h = (float("nan"), 0, 0) if a.no_e2e else time_e2e(cfg, t, args, max(3, a.steps // 2), dev)
     graph_times = time_graph(args, max(5, a.steps), flush)  # outside the timed region
+    verify = None if a.no_verify else time_verify(dev, flush, peaks, max(5, a.steps))
     fl, res_rows = floors_of(cfg)
     us = 1000 * ms
     roof = roofline(cfg, peaks, fl, us, sms)
@@ -569,6 +609,7 @@ def main():
                       "l2": "flushed before every replay"},
             "roofline": roof,
             "floors": floor_rec,
+            "verify": verify,
             "cpu_baseline": cpu,
             "e2e": {"value": world * toks / (e2e_ms * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -48,6 +48,14 @@ class WalkArgs(C.Structure):
     ]
 
 
+class VerifyArgs(C.Structure):
+    _fields_ = [
+        ("target_logits", C.c_void_p), ("draft_logits", C.c_void_p), ("draft_tokens", C.c_void_p),
+        ("seeds", C.c_void_p), ("V", C.c_int64), ("bs", C.c_int32), ("K", C.c_int32),
+        ("temperature", C.c_float), ("accepted", C.c_void_p), ("out_tokens", C.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -70,6 +78,7 @@ def lib():
         L.dspark_query_capacity.argtypes = [i32, i64, i32, i32, C.POINTER(C.c_int32),
                                             C.POINTER(C.c_int64)]
         L.dspark_gumbel_noise.argtypes = [vp, i32, i32, i64, vp, vp, vp]
+        L.dspark_verify.argtypes = [C.POINTER(VerifyArgs), vp]
         L.dspark_status_string.argtypes = [i32]
         L.dspark_status_string.restype = C.c_char_p
         L.dspark_last_cuda_error.argtypes = []
@@ -192,6 +201,24 @@ def walk_from_host(args: WalkArgs, base_host, prev_host, seeds_host, tokens_host
     _check(lib().dspark_walk_from_host(C.byref(args), _ptr(base_host), _ptr(prev_host),
                                        _ptr(seeds_host), _ptr(tokens_host), _ptr(logits_host),
                                        _stream(stream)), "dspark_walk_from_host")
+
+
+def verify(target_logits, draft_logits, draft_tokens, seeds, temperature=1.0, *, accepted=None,
+           out_tokens=None, stream=None):
+    """dspark_verify: speculative-sampling verification. target_logits bf16 [bs, K+1, V],
+    draft_logits bf16 [bs, K, V], draft_tokens int32 [bs, K], seeds [bs].
+    Returns (accepted int32 [bs], out_tokens int32 [bs, K+1])."""
+    bs, K1, V = target_logits.shape
+    dev = target_logits.device
+    if accepted is None:
+        accepted = torch.empty(bs, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((bs, K1), dtype=torch.int32, device=dev)
+    a = VerifyArgs(_dev_ptr(target_logits), _dev_ptr(draft_logits), _dev_ptr(draft_tokens),
+                   _dev_ptr(seeds), V, bs, K1 - 1, temperature, _dev_ptr(accepted),
+                   _dev_ptr(out_tokens))
+    _check(lib().dspark_verify(C.byref(a), _stream(stream)), "dspark_verify")
+    return accepted, out_tokens
 
 
 def gumbel_noise(seeds: torch.Tensor, K: int, V: int, stream=None):

@@ -206,6 +206,37 @@ int32_t dspark_gumbel_noise(const uint64_t* seeds, int32_t bs, int32_t K, int64_
  */
 int32_t dspark_walk_noalloc(const dspark_walk_args* args, dspark_stream_t stream);
 
+/*
+ * Speculative-sampling verification of drafted tokens (Leviathan, Kalman, Matias, ICML
+ * 2023, Algorithm 1), consuming the walk's draft_logits, which are the distribution the
+ * draft tokens were sampled from (vLLM PR #62958, "Details"). With
+ * q_i = softmax(draft_logits[b, i, :] / T) and p_i = softmax(target_logits[b, i, :] / T):
+ * draft i is accepted iff u_i q_i(d_i) < p_i(d_i); at the first rejection a sample of
+ * norm(max(0, p_i - q_i)) is emitted and the row stops; if all K are accepted a sample
+ * of p_K is emitted. u_i and the Gumbel-max noise of the samples come from the walk's
+ * Philox4x32-10 keyed by the row's seed, counter (v >> 2, i, b, 1) for u_i (v = 0) and
+ * (v >> 2, i, b, 2) for the noise, so the verification is reproducible.
+ *   target_logits bf16 [bs, K+1, V]; draft_logits bf16 [bs, K, V]; draft_tokens int32
+ *   [bs, K]; seeds uint64 [bs]; out: accepted int32 [bs] (0..K), out_tokens int32
+ *   [bs, K+1] (the accepted drafts, the emitted sample, then -1). All device memory
+ *   owned by the caller; asynchronous on `stream`. A draft token outside [0, V) is
+ *   rejected. Returns DSPARK_ERR_INVALID_ARG for null pointers, V <= 0, bs outside
+ *   1..DSPARK_MAX_BS, K outside 1..DSPARK_MAX_K, or T not > 0 and finite.
+ */
+typedef struct dspark_verify_args {
+  const uint16_t* target_logits;
+  const uint16_t* draft_logits;
+  const int32_t* draft_tokens;
+  const uint64_t* seeds;
+  int64_t V;
+  int32_t bs;
+  int32_t K;
+  float temperature;
+  int32_t* accepted;
+  int32_t* out_tokens;
+} dspark_verify_args;
+int32_t dspark_verify(const dspark_verify_args* args, dspark_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* dspark_status_string(int32_t status);
 

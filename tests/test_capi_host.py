@@ -81,3 +81,14 @@ def test_invalid_arguments_rejected_on_host(L):
     assert L.dspark_quantize_w2(None, 10, 256, None, None, None, None) == 1
     assert L.dspark_quantize_w2(fake, 10, 255, fake, fake, None, None) == 1
     assert L.dspark_gumbel_noise(None, 1, 1, 10, None, None, None) == 1
+    v = capi.VerifyArgs()
+    assert L.dspark_verify(C.byref(v), None) == 1                     # null pointers
+    for bad in (dict(V=0), dict(bs=0), dict(bs=65), dict(K=0), dict(K=33), dict(temperature=0.0),
+                dict(temperature=float("nan"))):
+        d = dict(target_logits=fake, draft_logits=fake, draft_tokens=fake, seeds=fake, V=100,
+                 bs=2, K=3, temperature=1.0, accepted=fake, out_tokens=fake)
+        d.update(bad)
+        x = capi.VerifyArgs()
+        for k, val in d.items():
+            setattr(x, k, val)
+        assert L.dspark_verify(C.byref(x), None) == 1, bad
