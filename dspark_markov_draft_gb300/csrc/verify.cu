@@ -41,15 +41,17 @@ __device__ __forceinline__ uint4 philox_block_d(uint64_t seed, int b, int i, uin
                        static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
 }
 
-// Hardware base-2 exponential (relative error about 2^-22; 2^-inf = 0).
+// Hardware base-2 exponential (relative error about 2^-22; 2^-inf = 0; results below
+// 2^-126 flush to 0, which no normaliser or acceptance test here can notice).
 __device__ __forceinline__ float ex2(float x) {
   float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Hardware reciprocal (about 1 ulp); used on arguments in [6e-8, 17].
 __device__ __forceinline__ float rcp_approx(float x) {
   float y;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -257,27 +259,48 @@ __global__ void __cluster_dims__(kEmitCtas, 1, 1) __launch_bounds__(kVerifyThrea
   auto sample = [&](bool res, int round) {
     uint64_t best = 0ull;
     int any = 0;
-    for (int64_t m = v0 / 4 + tid; 4 * m < v1; m += kVerifyThreads) {
-      const uint4 w4 = philox_block_d(seed, b, n, static_cast<uint32_t>(m), 2u);
+    // 8-byte loads of a group's four entries when both rows allow them (V a multiple of
+    // 4 makes every group of the slice whole); indices fit 32 bits (V < 2^31)
+    const bool vec = (V & 3) == 0 &&
+                     ((reinterpret_cast<uintptr_t>(trow) | (res ? reinterpret_cast<uintptr_t>(drow) : 0u)) & 7u) == 0;
+    const uint32_t e1 = static_cast<uint32_t>(v1);
+    for (uint32_t m = static_cast<uint32_t>(v0) / 4 + tid; 4 * m < e1; m += kVerifyThreads) {
+      const uint4 w4 = philox_block_d(seed, b, n, m, 2u);
       const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+      float xt[4], xd[4] = {0.f, 0.f, 0.f, 0.f};
+      if (vec) {
+        const uint2 a = __ldg(reinterpret_cast<const uint2*>(trow) + m);
+        xt[0] = bf16_lo(a.x); xt[1] = bf16_hi(a.x); xt[2] = bf16_lo(a.y); xt[3] = bf16_hi(a.y);
+        if (res) {
+          const uint2 d = __ldg(reinterpret_cast<const uint2*>(drow) + m);
+          xd[0] = bf16_lo(d.x); xd[1] = bf16_hi(d.x); xd[2] = bf16_lo(d.y); xd[3] = bf16_hi(d.y);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t v = 4 * m + e;
+          xt[e] = v < e1 ? bf16_to_f32(__ldg(trow + v)) : 0.f;
+          if (res) xd[e] = v < e1 ? bf16_to_f32(__ldg(drow + v)) : 0.f;
+        }
+      }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int64_t v = 4 * m + e;
-        if (v >= v1) break;
-        const float xt = bf16_to_f32(__ldg(trow + v));
-        float sc;
+        const uint32_t v = 4 * m + e;
+        if (v >= e1) break;
+        uint32_t key;
         if (res) {
-          const float pv = __fmul_rn(ex2(__fmaf_rn(xt, c, nmt)), zt);
-          const float qv = __fmul_rn(ex2(__fmaf_rn(bf16_to_f32(__ldg(drow + v)), c, nmd)), zd);
-          const float rr = __fsub_rn(pv, qv);
+          // (p - q) / E >= 0 is finite: its bits order like the value; entries with
+          // p <= q take key 0, below every candidate (if all are, the p round follows)
+          const float rr = __fsub_rn(__fmul_rn(ex2(__fmaf_rn(xt[e], c, nmt)), zt),
+                                     __fmul_rn(ex2(__fmaf_rn(xd[e], c, nmd)), zd));
           const float f = __uint_as_float(0x3F800000u | (ws[e] >> 9));
           const float u = __fadd_rn(__fsub_rn(f, 1.0f), 5.9604644775390625e-08f);
-          sc = rr > 0.f ? __fmul_rn(rr, rcp_approx(neg_log_unit(u))) : -INFINITY;
+          key = rr > 0.f ? (__float_as_uint(__fmul_rn(rr, rcp_approx(neg_log_unit(u)))) | 0x80000000u) : 0u;
           any |= rr > 0.f ? 1 : 0;
         } else {
-          sc = __fadd_rn(__fmul_rn(xt, p.inv_t), gumbel_from_word(ws[e]));
+          key = order_key(__fadd_rn(__fmul_rn(xt[e], p.inv_t), gumbel_from_word(ws[e])));
         }
-        best = umax64(best, pack_best(order_key(sc), static_cast<uint32_t>(v)));
+        best = umax64(best, pack_best(key, v));
       }
     }
     best = block_reduce(best, [](uint64_t a, uint64_t q) { return umax64(a, q); }, shu);
