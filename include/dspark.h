@@ -213,15 +213,21 @@ int32_t dspark_walk_noalloc(const dspark_walk_args* args, dspark_stream_t stream
  * q_i = softmax(draft_logits[b, i, :] / T) and p_i = softmax(target_logits[b, i, :] / T):
  * draft i is accepted iff u_i q_i(d_i) < p_i(d_i); at the first rejection a sample of
  * norm(max(0, p_i - q_i)) is emitted and the row stops; if all K are accepted a sample
- * of p_K is emitted. u_i and the Gumbel-max noise of the samples come from the walk's
- * Philox4x32-10 keyed by the row's seed, counter (v >> 2, i, b, 1) for u_i (v = 0) and
- * (v >> 2, i, b, 2) for the noise, so the verification is reproducible.
+ * of p_K is emitted. Samples are Gumbel-max draws: the argmax over v of
+ * log(p(v) - q(v)) + g_v where p > q (if p > q nowhere after rounding, the scores of
+ * p), and of target[b, K, v] / T + g_v for the bonus token. u_i = (2 (w >> 9) + 1) 2^-24
+ * and g_v = -log(-log u_v) come from the walk's Philox4x32-10 keyed by the row's seed,
+ * counter (0, i, b, 1), word 0, for u_i, and (v >> 2, n, b, 2), word v & 3, for the
+ * noise at the emitting position n (the walk uses counter word 3 = 0), so the
+ * verification is reproducible and never reuses the drafter's noise.
  *   target_logits bf16 [bs, K+1, V]; draft_logits bf16 [bs, K, V]; draft_tokens int32
  *   [bs, K]; seeds uint64 [bs]; out: accepted int32 [bs] (0..K), out_tokens int32
  *   [bs, K+1] (the accepted drafts, the emitted sample, then -1). All device memory
  *   owned by the caller; asynchronous on `stream`. A draft token outside [0, V) is
- *   rejected. Returns DSPARK_ERR_INVALID_ARG for null pointers, V <= 0, bs outside
- *   1..DSPARK_MAX_BS, K outside 1..DSPARK_MAX_K, or T not > 0 and finite.
+ *   rejected. No alignment is required (16- and 8-byte loads are used where the rows
+ *   allow them). Returns DSPARK_ERR_INVALID_ARG for null pointers, V outside
+ *   1..DSPARK_MAX_V, bs outside 1..DSPARK_MAX_BS, K outside 1..DSPARK_MAX_K, or T not
+ *   > 0 and finite; DSPARK_ERR_CUDA if a launch fails.
  */
 typedef struct dspark_verify_args {
   const uint16_t* target_logits;
