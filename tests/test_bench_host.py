@@ -1,0 +1,51 @@
+"""Host-side arithmetic of bench.py's report: the algorithmic bytes of a walk counted by
+hand, and the roofline object's choice of the slowest floor and its fraction."""
+from __future__ import annotations
+
+import pytest
+
+import bench
+
+
+def test_hbm_bytes_of_the_main_workload_by_hand():
+    V, K, bs = 151936, 7, 64
+    w2 = V * 256 + 4 * V           # int8 codes + one fp32 scale per row, read once
+    base = bs * K * V * 2          # every bf16 base logit once
+    emb = bs * K * 256 * 2         # one W1 row per request and position
+    tokens = bs * K * 4
+    assert bench.hbm_bytes(bench.MAIN) == w2 + base + emb + tokens
+
+
+def test_hbm_bytes_count_draft_logits_and_top_k_candidates():
+    cfg = dict(bench.MAIN, logits=True)
+    assert bench.hbm_bytes(cfg) - bench.hbm_bytes(bench.MAIN) == 64 * 7 * 151936 * 2
+    tk = dict(bench.MAIN, top_k=512, int8=False)
+    # the candidate walk reads one bf16 W2 row per candidate instead of W2 once
+    assert bench.hbm_bytes(tk) == 64 * 7 * 512 * 256 * 2 + 64 * 7 * 151936 * 2 + 64 * 7 * 256 * 2 + 64 * 7 * 4
+
+
+PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, sm_mhz=2000.0, src="fallback")
+
+
+def test_roofline_takes_the_slowest_floor_and_its_fraction():
+    cfg = bench.MAIN
+    fl = bench.floors(cfg, PEAKS, sms=152, resident_rows=100_000, l2_gbs=20_000.0)
+    assert set(fl) == {"hbm_us", "smem_us", "l2_us", "tensor_us"}
+    slowest = max(fl, key=fl.get)
+    us = 4 * fl[slowest]
+    r = bench.roofline(cfg, PEAKS, fl, us, sms=152)
+    assert r["frac"] == pytest.approx(fl[slowest] / us)  # a quarter of the floor's speed
+    if slowest == "hbm_us":
+        assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+        assert r["achieved"] * 1e9 * us * 1e-6 == pytest.approx(bench.hbm_bytes(cfg))
+
+
+def test_small_batches_are_bound_by_dp4a_issue():
+    cfg = dict(bench.MAIN, bs=1)
+    fl = bench.floors(cfg, PEAKS, sms=152, resident_rows=150_000, l2_gbs=20_000.0)
+    assert "alu_us" in fl and "tensor_us" not in fl
+    ops, lanes = bench.alu_ops(cfg)
+    assert ops == 3 * 151936 * 256 * 7 / 4 and lanes == 64
+    assert fl["alu_us"] == pytest.approx(ops / (lanes * 152 * 2000e6) * 1e6)
+    r = bench.roofline(cfg, PEAKS, {"alu_us": fl["alu_us"]}, 2 * fl["alu_us"], sms=152)
+    assert r["bound"] == "alu" and r["frac"] == pytest.approx(0.5)
