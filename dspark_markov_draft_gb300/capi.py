@@ -84,7 +84,8 @@ def lib():
         L.dspark_last_cuda_error.argtypes = []
         L.dspark_last_cuda_error.restype = C.c_char_p
         for f in ("dspark_quantize_w2", "dspark_walk", "dspark_walk_topk", "dspark_walk_noalloc",
-                  "dspark_walk_from_host", "dspark_query_capacity", "dspark_gumbel_noise"):
+                  "dspark_walk_from_host", "dspark_query_capacity", "dspark_gumbel_noise",
+                  "dspark_verify"):
             getattr(L, f).restype = C.c_int32
         _lib = L
     return _lib
@@ -102,6 +103,16 @@ def _dev_ptr(t: torch.Tensor | None):
     if t is not None and not t.is_cuda:
         raise ValueError("expected a CUDA tensor")
     return _ptr(t)
+
+
+def _expect(t: torch.Tensor, shape, dtypes, name: str, device):
+    """A contiguous tensor of this shape and one of these dtypes on `device`."""
+    if tuple(t.shape) != tuple(shape) or t.dtype not in dtypes or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous {'/'.join(map(str, dtypes))} tensor of shape "
+                         f"{tuple(shape)}, got {t.dtype} {tuple(t.shape)}"
+                         f"{'' if t.is_contiguous() else ' (not contiguous)'}")
+    if t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
 
 
 def _stream(stream) -> int | None:
@@ -210,10 +221,18 @@ def verify(target_logits, draft_logits, draft_tokens, seeds, temperature=1.0, *,
     Returns (accepted int32 [bs], out_tokens int32 [bs, K+1])."""
     bs, K1, V = target_logits.shape
     dev = target_logits.device
+    # the kernels index these buffers by (bs, K, V): refuse a mismatch here rather than
+    # read past a buffer on the device
+    _expect(target_logits, (bs, K1, V), (torch.bfloat16,), "target_logits", dev)
+    _expect(draft_logits, (bs, K1 - 1, V), (torch.bfloat16,), "draft_logits", dev)
+    _expect(draft_tokens, (bs, K1 - 1), (torch.int32,), "draft_tokens", dev)
+    _expect(seeds, (bs,), (torch.int64, getattr(torch, "uint64", torch.int64)), "seeds", dev)
     if accepted is None:
         accepted = torch.empty(bs, dtype=torch.int32, device=dev)
     if out_tokens is None:
         out_tokens = torch.empty((bs, K1), dtype=torch.int32, device=dev)
+    _expect(accepted, (bs,), (torch.int32,), "accepted", dev)
+    _expect(out_tokens, (bs, K1), (torch.int32,), "out_tokens", dev)
     a = VerifyArgs(_dev_ptr(target_logits), _dev_ptr(draft_logits), _dev_ptr(draft_tokens),
                    _dev_ptr(seeds), V, bs, K1 - 1, temperature, _dev_ptr(accepted),
                    _dev_ptr(out_tokens))

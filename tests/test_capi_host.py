@@ -92,3 +92,25 @@ def test_invalid_arguments_rejected_on_host(L):
         for k, val in d.items():
             setattr(x, k, val)
         assert L.dspark_verify(C.byref(x), None) == 1, bad
+
+
+def test_verify_binding_refuses_mismatched_buffers():
+    """The binding checks shapes, dtypes and contiguity before any pointer reaches the
+    kernels (which index the buffers by bs, K and V): CPU tensors suffice to see it."""
+    import torch
+    from dspark_markov_draft_gb300 import capi
+    bs, K, V = 3, 2, 10
+    good = dict(t=torch.zeros(bs, K + 1, V, dtype=torch.bfloat16), d=torch.zeros(bs, K, V, dtype=torch.bfloat16),
+                k=torch.zeros(bs, K, dtype=torch.int32), s=torch.zeros(bs, dtype=torch.int64))
+    bad = [dict(d=torch.zeros(bs, K + 1, V, dtype=torch.bfloat16)),          # K mismatch
+           dict(d=torch.zeros(bs, K, V, dtype=torch.float32)),               # dtype
+           dict(k=torch.zeros(bs, K, dtype=torch.int64)),
+           dict(s=torch.zeros(bs + 1, dtype=torch.int64)),
+           dict(t=torch.zeros(bs, V, K + 1, dtype=torch.bfloat16).transpose(1, 2))]  # not contiguous
+    for over in bad:
+        a = dict(good, **over)
+        with pytest.raises(ValueError, match="expected a contiguous"):
+            capi.verify(a["t"], a["d"], a["k"], a["s"], 1.0)
+    with pytest.raises(ValueError, match="CUDA tensor"):  # well-formed, but on the host
+        capi.verify(good["t"], good["d"], good["k"], good["s"], 1.0,
+                    accepted=torch.zeros(bs, dtype=torch.int32), out_tokens=torch.zeros(bs, K + 1, dtype=torch.int32))
