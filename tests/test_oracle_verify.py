@@ -89,3 +89,43 @@ def test_special_cases(oracle):
     dz[0, 0, 1] = 0xFF80
     res = O.verify(tb, dz, dtok, np.array([5], np.uint64), T)
     assert res.accepted[0] >= 1 and res.out_tokens[0, 0] == 1
+
+
+def test_random_draws_follow_the_documented_counters(oracle):
+    """The verifier's randomness, recomputed from the Philox core (itself pinned against
+    an independent implementation) and the documented layout: u_i from counter
+    (0, i, b, 1), word 0; the sample noise of position n from counter (v >> 2, n, b, 2),
+    word v & 3, g = -log(-log u). The bonus scores are target / T + g, the residual
+    scores log(p - q) + g where p > q; the probabilities are softmax(row / T)."""
+    bs, K, V, T = 3, 2, 37, 0.8
+    g = torch.Generator().manual_seed(11)
+    tgt = torch.randn(bs, K + 1, V, generator=g) * 2
+    drf = torch.randn(bs, K, V, generator=g) * 2
+    tb, db = _bits(tgt), _bits(drf)
+    dtok = np.array([[1, 5], [36, 0], [7, 7]], np.int32)
+    seeds = np.array([5, 2**40 + 3, 2**64 - 7], np.uint64)
+    res = O.verify(tb, db, dtok, seeds, T, want_probs=True)
+    assert res.status == 0
+    T = float(np.float32(T))  # the temperature is an fp32 argument
+
+    def u_of(w):
+        return (2.0 * (int(w) >> 9) + 1.0) * 2.0**-24
+
+    for r in range(bs):
+        key = [int(seeds[r]) & 0xFFFFFFFF, int(seeds[r]) >> 32]
+        for i in range(K):
+            w = O.philox4x32_10([0, i, r, 1], key)[0]
+            assert res.u[r, i] == u_of(w)
+        for n in range(K + 1):
+            p = _probs(tb[r, n], T)
+            np.testing.assert_allclose(res.p[r, n], p, rtol=1e-12, atol=1e-300)
+            x = torch.from_numpy(tb[r, n].view(np.int16)).view(torch.bfloat16).double().numpy()
+            noise = np.array([-np.log(-np.log(u_of(O.philox4x32_10([v >> 2, n, r, 2], key)[v & 3])))
+                              for v in range(V)])
+            if n == K:
+                want = x / T + noise
+            else:
+                rv = p - _probs(db[r, n], T)
+                want = np.where(rv > 0, np.log(np.where(rv > 0, rv, 1.0)) + noise, -np.inf)
+            np.testing.assert_allclose(res.scores[r, n], want, rtol=1e-9, atol=1e-9)
+            assert res.y[r, n] == int(np.argmax(want))
