@@ -27,6 +27,33 @@ cudaError_t launch_quantize_w2(const uint16_t* w2, int64_t V, int8_t* q, float* 
 cudaError_t launch_gumbel_noise(const uint64_t* seeds, int bs, int K, int64_t V, uint32_t* words,
                                 float* gumbel, cudaStream_t stream);
 
+// Checks of a walk's arguments other than its workspace, made before any CUDA call.
+int32_t check_walk_inputs(const dspark_walk_args* a) {
+  if (!a) return DSPARK_ERR_INVALID_ARG;
+  if (!a->base_logits || !a->w1 || !a->prev_tokens || !a->draft_tokens) return DSPARK_ERR_INVALID_ARG;
+  if (a->rank != DSPARK_RANK) return DSPARK_ERR_INVALID_ARG;
+  if (a->V <= 0 || a->V > DSPARK_MAX_V) return DSPARK_ERR_INVALID_ARG;
+  if (a->bs < 1 || a->bs > DSPARK_MAX_BS || a->K < 1 || a->K > DSPARK_MAX_K) return DSPARK_ERR_INVALID_ARG;
+  if (a->mode != DSPARK_GREEDY && a->mode != DSPARK_PROBABILISTIC) return DSPARK_ERR_INVALID_ARG;
+  // with per-row modes any row may be sampled; per-row temperatures are checked on the
+  // device (a bad one invalidates its row only)
+  if (a->mode == DSPARK_PROBABILISTIC || a->row_modes) {
+    if (!a->seeds) return DSPARK_ERR_INVALID_ARG;
+    if (!a->temperatures && (!(a->temperature > 0.f) || !(a->temperature < 3.4e38f)))
+      return DSPARK_ERR_INVALID_ARG;
+  }
+  const bool have_bf16 = a->w2 != nullptr;
+  const bool have_int8 = a->w2q != nullptr;
+  if (have_bf16 == have_int8) return DSPARK_ERR_INVALID_ARG;
+  if (have_int8 && !a->w2_scales) return DSPARK_ERR_INVALID_ARG;
+  if (a->top_k < 0 || a->top_k > a->V) return DSPARK_ERR_INVALID_ARG;
+  // 16-byte vector loads of W1 / W2 rows
+  if ((reinterpret_cast<uintptr_t>(a->w1) | reinterpret_cast<uintptr_t>(a->w2) |
+       reinterpret_cast<uintptr_t>(a->w2q)) & 15u)
+    return DSPARK_ERR_INVALID_ARG;
+  return DSPARK_OK;
+}
+
 namespace {
 
 thread_local char g_last_error[256] = "";
@@ -141,31 +168,11 @@ bool tc_fits(const DeviceCaps& caps, int64_t V) {
 }
 
 int32_t check_common(const dspark_walk_args* a) {
-  if (!a) return DSPARK_ERR_INVALID_ARG;
-  if (!a->base_logits || !a->w1 || !a->prev_tokens || !a->draft_tokens) return DSPARK_ERR_INVALID_ARG;
-  if (a->rank != DSPARK_RANK) return DSPARK_ERR_INVALID_ARG;
-  if (a->V <= 0 || a->V > DSPARK_MAX_V) return DSPARK_ERR_INVALID_ARG;
-  if (a->bs < 1 || a->bs > DSPARK_MAX_BS || a->K < 1 || a->K > DSPARK_MAX_K) return DSPARK_ERR_INVALID_ARG;
-  if (a->mode != DSPARK_GREEDY && a->mode != DSPARK_PROBABILISTIC) return DSPARK_ERR_INVALID_ARG;
-  // with per-row modes any row may be sampled; per-row temperatures are checked on the
-  // device (a bad one invalidates its row only)
-  if (a->mode == DSPARK_PROBABILISTIC || a->row_modes) {
-    if (!a->seeds) return DSPARK_ERR_INVALID_ARG;
-    if (!a->temperatures && (!(a->temperature > 0.f) || !(a->temperature < 3.4e38f)))
-      return DSPARK_ERR_INVALID_ARG;
-  }
-  const bool have_bf16 = a->w2 != nullptr;
-  const bool have_int8 = a->w2q != nullptr;
-  if (have_bf16 == have_int8) return DSPARK_ERR_INVALID_ARG;
-  if (have_int8 && !a->w2_scales) return DSPARK_ERR_INVALID_ARG;
-  if (a->top_k < 0 || a->top_k > a->V) return DSPARK_ERR_INVALID_ARG;
+  const int32_t st = check_walk_inputs(a);
+  if (st != DSPARK_OK) return st;
   if (!a->workspace) return DSPARK_ERR_WORKSPACE;
   if (a->workspace_bytes < ws_total(a->K, a->bs, a->top_k)) return DSPARK_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return DSPARK_ERR_WORKSPACE;
-  // 16-byte vector loads of W1 / W2 rows
-  if ((reinterpret_cast<uintptr_t>(a->w1) | reinterpret_cast<uintptr_t>(a->w2) |
-       reinterpret_cast<uintptr_t>(a->w2q)) & 15u)
-    return DSPARK_ERR_INVALID_ARG;
   return DSPARK_OK;
 }
 

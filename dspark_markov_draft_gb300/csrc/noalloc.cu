@@ -11,6 +11,9 @@
 #include "common.cuh"
 
 namespace dspark {
+
+int32_t check_walk_inputs(const dspark_walk_args* a);
+
 namespace {
 
 // Stated maximum of the static scratch: enough for every walk the dense entry point
@@ -30,7 +33,9 @@ extern "C" int32_t dspark_walk_noalloc(const dspark_walk_args* a, dspark_stream_
   using namespace dspark;
   if (!a) return DSPARK_ERR_INVALID_ARG;
   if (a->top_k != 0) return DSPARK_ERR_UNSUPPORTED;  // the top-k lists do not fit
-  if (a->bs < 1 || a->bs > DSPARK_MAX_BS || a->K < 1 || a->K > DSPARK_MAX_K) return DSPARK_ERR_INVALID_ARG;
+  // every argument check before the first CUDA call, as in the other entry points
+  const int32_t st = check_walk_inputs(a);
+  if (st != DSPARK_OK) return st;
   const size_t need = ws_total(a->K, a->bs, 0);
   if (need > kStaticScratchBytes) return DSPARK_ERR_WORKSPACE;
 

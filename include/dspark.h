@@ -193,6 +193,7 @@ int32_t dspark_gumbel_noise(const uint64_t* seeds, int32_t bs, int32_t K, int64_
  * decode path would fail or synchronise). The pages have no counterpart of this call.
  *   - Takes the same arguments as dspark_walk; `workspace` and `workspace_bytes` are
  *     ignored. Full-vocabulary walk only: top_k > 0 returns DSPARK_ERR_UNSUPPORTED.
+ *     Invalid arguments return DSPARK_ERR_INVALID_ARG before any CUDA call.
  *   - Scratch comes from one static device array of 24,576 bytes inside the library,
  *     held by every GPU that loads the library until the process exits. A shape whose
  *     scratch would not fit returns DSPARK_ERR_WORKSPACE (every shape dspark_walk

@@ -76,8 +76,23 @@ def test_invalid_arguments_rejected_on_host(L):
                 dict(row_modes=fake, seeds=None),                      # per-row modes need seeds
                 dict(row_modes=fake, seeds=fake, temperature=0.0)):    # ... and a valid scalar T
         assert L.dspark_walk(C.byref(args(**bad)), None) == 1, bad
+    for bad in (dict(w2q=fake, w2=None),                       # int8 W2 without its scales
+                dict(w1=fake + 8), dict(w2=fake + 4),            # rows not 16-byte aligned
+                dict(V=(1 << 31)), dict(top_k=-1),
+                dict(mode=1, seeds=fake, temperature=float("inf")),
+                dict(mode=1, seeds=fake, temperature=float("nan"))):
+        assert L.dspark_walk(C.byref(args(**bad)), None) == 1, bad
+    # the top-k and allocation-free entry points apply the same checks first (the latter
+    # before it looks up its scratch on the device, so here, with no GPU, too)
+    for f in (L.dspark_walk_topk, L.dspark_walk_noalloc):
+        assert f(None, None) == 1
+        for bad in (dict(rank=128), dict(bs=65), dict(K=33), dict(mode=1, seeds=None)):
+            assert f(C.byref(args(**bad)), None) == 1, (f, bad)
+    assert L.dspark_walk_topk(C.byref(args(top_k=0)), None) == 1      # k >= 1 required
+    assert L.dspark_walk_noalloc(C.byref(args(top_k=5)), None) == 2   # full vocabulary only
     assert L.dspark_walk(C.byref(args(workspace_bytes=16)), None) == 8
     assert L.dspark_walk(C.byref(args(workspace=None)), None) == 8
+    assert L.dspark_walk(C.byref(args(workspace=fake + 128)), None) == 8   # not 256-byte aligned
     assert L.dspark_quantize_w2(None, 10, 256, None, None, None, None) == 1
     assert L.dspark_quantize_w2(fake, 10, 255, fake, fake, None, None) == 1
     assert L.dspark_gumbel_noise(None, 1, 1, 10, None, None, None) == 1
