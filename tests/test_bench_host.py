@@ -49,3 +49,24 @@ def test_small_batches_are_bound_by_dp4a_issue():
     assert fl["alu_us"] == pytest.approx(ops / (lanes * 152 * 2000e6) * 1e6)
     r = bench.roofline(cfg, PEAKS, {"alu_us": fl["alu_us"]}, 2 * fl["alu_us"], sms=152)
     assert r["bound"] == "alu" and r["frac"] == pytest.approx(0.5)
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` times the oracle on the host cores (no GPU) and prints
+    one JSON line with the keys the two arms share, plus its sample description."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    p = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "1"],
+                       cwd=root, capture_output=True, text=True, timeout=600)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["n_gpus"] == 1
+    assert d["config"]["workload"] == bench.MAIN["name"]
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
