@@ -55,18 +55,22 @@ int32_t check_walk_inputs(const dspark_walk_args* a) {
 }
 
 namespace {
-
 thread_local char g_last_error[256] = "";
+}  // namespace
 
+// Records the failing call for dspark_last_cuda_error and returns DSPARK_ERR_CUDA.
 int32_t cuda_fail(cudaError_t e, const char* where) {
   std::snprintf(g_last_error, sizeof g_last_error, "%s: %s", where, cudaGetErrorString(e));
   return DSPARK_ERR_CUDA;
 }
 
+namespace {
+
 struct DeviceCaps {
   bool valid = false;
   int sms = 0;
   int smem_optin = 0;
+  int smem_per_sm = 0;
   int coop = 0;
 };
 
@@ -84,6 +88,8 @@ int32_t get_caps(int device, DeviceCaps* out) {
       return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
     if ((e = cudaDeviceGetAttribute(&c.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device)) != cudaSuccess)
       return cuda_fail(e, "cudaDeviceGetAttribute(smem opt-in)");
+    if ((e = cudaDeviceGetAttribute(&c.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(smem per SM)");
     if ((e = cudaDeviceGetAttribute(&c.coop, cudaDevAttrCooperativeLaunch, device)) != cudaSuccess)
       return cuda_fail(e, "cudaDeviceGetAttribute(cooperative launch)");
     c.valid = true;
@@ -138,8 +144,9 @@ struct TcPlan {
 };
 
 // Tensor-core walk: B operand (N x 512 bytes), the slice's scales, bookkeeping, and as
-// many resident W2 rows as the remaining shared memory holds.
-TcPlan plan_tc(const DeviceCaps& caps, int64_t V, bool int8, bool prob, int bs, int cap_rows) {
+// many resident W2 rows (whole 32-row blocks) as the remaining shared memory holds.
+TcPlan plan_tc(const DeviceCaps& caps, int64_t V, bool int8, bool prob, int bs, int cap_rows, bool base_tma) {
+  (void)prob;
   TcPlan pl{};
   pl.grid = caps.sms;
   const int N = bs <= 16 ? 16 : bs <= 32 ? 32 : 64;
@@ -147,9 +154,8 @@ TcPlan plan_tc(const DeviceCaps& caps, int64_t V, bool int8, bool prob, int bs, 
   const int64_t per_cta = (V + pl.grid - 1) / pl.grid + 32;
   pl.slice_cap = static_cast<int>((per_cta + 31) & ~31LL);
   const int row_bytes = int8 ? kRank : 2 * kRank;
-  const size_t fixed = 1024 + static_cast<size_t>(N) * 512 + walk_tc_stage_bytes(N) +
-                       (int8 ? static_cast<size_t>(pl.slice_cap) * 4 : 0) +
-                       walk_tc_misc_smem();
+  const size_t fixed = 1024 + static_cast<size_t>(N) * 512 + (base_tma ? tc_stage_ring_bytes(N) : 0) +
+                       (int8 ? static_cast<size_t>(pl.slice_cap) * 4 : 0) + walk_tc_misc_smem();
   int64_t rows = caps.smem_optin > static_cast<int>(fixed)
                      ? (static_cast<int64_t>(caps.smem_optin) - static_cast<int64_t>(fixed)) / row_bytes
                      : 0;
@@ -231,35 +237,97 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Tensor map over a [bs][K][V] bf16 tensor (base logits or draft_logits) for the
-// tensor-core epilogue: box of 32 vocabulary rows x 1 position x N/2 requests. False
-// (and the kernel uses per-thread copies) when the layout cannot be described: V not a
-// multiple of 8, or a pointer not 16-byte aligned.
-bool make_bsk_map(const dspark_walk_args* a, const uint16_t* ptr, int N, CUtensorMap* m) {
-  if (!ptr || (a->V & 7) != 0 || (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return false;
+// Tensor map over the W2 rows for the tensor-core walk's resident copies: [V][256] int8
+// or bf16, box of 32 rows x 128 bytes, 128-byte swizzle. False when the driver entry
+// point is missing (the walk then keeps no rows resident).
+bool make_w2_map(const dspark_walk_args* a, CUtensorMap* m) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const bool int8 = a->w2q != nullptr;
+  void* ptr = int8 ? const_cast<int8_t*>(a->w2q) : static_cast<void*>(const_cast<uint16_t*>(a->w2));
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kRank), static_cast<cuuint64_t>(a->V)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRank) * (int8 ? 1 : 2)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(int8 ? 128 : 64), 32};
+  const cuuint32_t elem[2] = {1, 1};
+  const CUresult r = enc(m, int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr,
+                         dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// The tensor-core walk's warpgroups rebalance their registers with setmaxnreg on the
+// assumption that the kernel was compiled for kTcLaunchRegs registers per thread; with
+// any other count a request for more registers could wait forever, so the walk is not
+// launched. Checked once per kernel instance.
+int32_t check_tc_registers(const void* fn) {
+  constexpr int kSlots = 64;
+  static const void* checked[kSlots] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  for (int k = 0; k < kSlots && checked[k]; ++k)
+    if (checked[k] == fn) return DSPARK_OK;
+  cudaFuncAttributes attr{};
+  const cudaError_t e = cudaFuncGetAttributes(&attr, fn);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(walk_tc_kernel)");
+  if (attr.numRegs != kTcLaunchRegs) {
+    std::snprintf(g_last_error, sizeof g_last_error,
+                  "walk_tc_kernel compiled for %d registers per thread, its register split assumes %d",
+                  attr.numRegs, kTcLaunchRegs);
+    return DSPARK_ERR_UNSUPPORTED;
+  }
+  for (int k = 0; k < kSlots; ++k)
+    if (!checked[k]) { checked[k] = fn; break; }
+  return DSPARK_OK;
+}
+
+// Tensor map over the base logits [bs][K][V] bf16 for the tensor-core walk's stages:
+// box of 128 vocabulary rows x 1 position x N requests. False (the walk then loads the
+// base logits per thread) when the layout cannot be described: V not a multiple of 8
+// (row strides must be multiples of 16 bytes) or a pointer not 16-byte aligned.
+bool make_base_map(const dspark_walk_args* a, int N, CUtensorMap* m) {
+  if ((a->V & 7) != 0 || (reinterpret_cast<uintptr_t>(a->base_logits) & 15u) != 0) return false;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a->V), static_cast<cuuint64_t>(a->K),
                               static_cast<cuuint64_t>(a->bs)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a->V) * 2,
                                  static_cast<cuuint64_t>(a->V) * 2 * static_cast<cuuint64_t>(a->K)};
-  const cuuint32_t box[3] = {32, 1, static_cast<cuuint32_t>(N / 2)};
+  const cuuint32_t box[3] = {128, 1, static_cast<cuuint32_t>(N)};
   const cuuint32_t elem[3] = {1, 1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(ptr),
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(a->base_logits),
                          dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-int32_t launch_coop(const void* fn, int grid, int threads, size_t smem, WalkParams& p, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-  if (per_sm < 1) return DSPARK_ERR_COOP_TOO_LARGE;
+// Dynamic shared memory that keeps a kernel at one CTA per SM: more than half of the
+// SM's shared memory (capped at the per-block opt-in). Kernels that allocate all 512
+// tensor-memory columns need this: a second CTA on the same SM would wait in
+// tcgen05.alloc until the first one exits, which a grid-wide barrier never allows.
+size_t exclusive_smem(size_t smem, int smem_per_sm, int smem_optin) {
+  const size_t half = static_cast<size_t>(smem_per_sm) / 2 + 1024;
+  if (smem >= half) return smem;
+  return half < static_cast<size_t>(smem_optin) ? half : static_cast<size_t>(smem_optin);
+}
+
+// Cooperative launch of a persistent walk kernel. tmem_exclusive: the kernel takes all
+// of tensor memory, so exactly one CTA may be resident per SM.
+int32_t launch_coop(const void* fn, int grid, int threads, size_t smem, WalkParams& p, cudaStream_t stream,
+                    const DeviceCaps& caps, bool tmem_exclusive) {
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    if (per_sm < 1) return DSPARK_ERR_COOP_TOO_LARGE;
+    if (!tmem_exclusive || per_sm == 1) break;
+    const size_t more = exclusive_smem(smem, caps.smem_per_sm, caps.smem_optin);
+    if (attempt == 1 || more == smem) return DSPARK_ERR_COOP_TOO_LARGE;
+    smem = more;
+  }
   void* args[] = {&p};
-  e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(threads), args, smem, stream);
+  cudaError_t e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(threads), args, smem, stream);
   if (e == cudaErrorCooperativeLaunchTooLarge) {
     cudaGetLastError();
     return DSPARK_ERR_COOP_TOO_LARGE;
@@ -308,7 +376,7 @@ int32_t dspark_query_capacity(int32_t device, int64_t V, int32_t w2_is_int8, int
   const bool tc = bs >= kTcMinBs && tc_fits(caps, V);
   int grid, per_cta;
   if (tc) {
-    const TcPlan pl = plan_tc(caps, V, w2_is_int8 != 0, false, bs, -1);
+    const TcPlan pl = plan_tc(caps, V, w2_is_int8 != 0, false, bs, -1, V % 8 == 0);
     grid = pl.grid;
     per_cta = pl.resident_rows;
   } else {
@@ -356,7 +424,7 @@ int32_t dspark_walk_topk(const dspark_walk_args* a, dspark_stream_t stream) {
   const size_t smem = topk_walk_smem(a->bs);
   const bool prob = a->mode == DSPARK_PROBABILISTIC || a->row_modes, lg = a->draft_logits != nullptr;
   const void* fn = topk_walk_kernel_ptr(a->w2q != nullptr, prob, lg);
-  return launch_coop(fn, caps.sms, kWalkThreads, smem, p, s);
+  return launch_coop(fn, caps.sms, kWalkThreads, smem, p, s, caps, false);
 }
 
 int32_t dspark_walk(const dspark_walk_args* a, dspark_stream_t stream) {
@@ -373,18 +441,29 @@ int32_t dspark_walk(const dspark_walk_args* a, dspark_stream_t stream) {
                       (a->bs >= kTcMinBs || (a->flags & DSPARK_FLAG_FORCE_TENSOR_CORES)) &&
                       tc_fits(caps, a->V);
   if (use_tc) {
-    const TcPlan pl = plan_tc(caps, a->V, int8, prob, a->bs, a->resident_rows_cap);
-    WalkParams p = make_params(a, pl.grid, pl.resident_rows, pl.slice_cap);
-    p.base_tma = make_bsk_map(a, a->base_logits, pl.nq * 4, &p.base_map) ? 1 : 0;
-    p.logits_tma = make_bsk_map(a, a->draft_logits, pl.nq * 4, &p.logits_map) ? 1 : 0;
+    CUtensorMap base_map;
+    const int N = a->bs <= 16 ? 16 : a->bs <= 32 ? 32 : 64;
+    const bool base_tma = make_base_map(a, N, &base_map);
+    const TcPlan pl = plan_tc(caps, a->V, int8, prob, a->bs, a->resident_rows_cap, base_tma);
+    int resident = pl.resident_rows;
+    size_t smem = pl.smem;
+    WalkParams p = make_params(a, pl.grid, resident, pl.slice_cap);
+    p.base_tma = base_tma ? 1 : 0;
+    if (base_tma) p.base_map = base_map;
+    p.w2_tma = make_w2_map(a, &p.w2_map) ? 1 : 0;
+    if (!p.w2_tma) {  // no tensor map: every row streamed
+      smem -= static_cast<size_t>(resident) * (int8 ? kRank : 2 * kRank);
+      p.resident_rows = 0;
+    }
     const bool rows = prob && (a->temperatures || a->row_modes);  // per-row settings
-    return launch_coop(walk_tc_kernel_ptr(int8, prob, lg, pl.nq, rows), pl.grid, walk_tc_threads(pl.nq * 4), pl.smem, p,
-                       reinterpret_cast<cudaStream_t>(stream));
+    const void* fn = walk_tc_kernel_ptr(int8, prob, lg, pl.nq, rows);
+    if ((st = check_tc_registers(fn)) != DSPARK_OK) return st;
+    return launch_coop(fn, pl.grid, kTcThreads, smem, p, reinterpret_cast<cudaStream_t>(stream), caps, true);
   }
   const Plan pl = plan_dense(caps, a->V, int8, a->bs, a->resident_rows_cap);
   WalkParams p = make_params(a, pl.grid, pl.resident_rows, pl.slice_cap);
   const void* fn = walk_cc_kernel_ptr(int8, prob, lg);
-  return launch_coop(fn, pl.grid, kWalkThreads, pl.smem, p, reinterpret_cast<cudaStream_t>(stream));
+  return launch_coop(fn, pl.grid, kWalkThreads, pl.smem, p, reinterpret_cast<cudaStream_t>(stream), caps, true);
 }
 
 int32_t dspark_verify(const dspark_verify_args* a, dspark_stream_t stream) {

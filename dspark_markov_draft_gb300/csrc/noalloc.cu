@@ -13,6 +13,7 @@
 namespace dspark {
 
 int32_t check_walk_inputs(const dspark_walk_args* a);
+int32_t cuda_fail(cudaError_t e, const char* where);
 
 namespace {
 
@@ -31,17 +32,17 @@ std::mutex g_scratch_mu;
 
 extern "C" int32_t dspark_walk_noalloc(const dspark_walk_args* a, dspark_stream_t stream) {
   using namespace dspark;
-  if (!a) return DSPARK_ERR_INVALID_ARG;
-  if (a->top_k != 0) return DSPARK_ERR_UNSUPPORTED;  // the top-k lists do not fit
   // every argument check before the first CUDA call, as in the other entry points
   const int32_t st = check_walk_inputs(a);
   if (st != DSPARK_OK) return st;
+  if (a->top_k != 0) return DSPARK_ERR_UNSUPPORTED;  // the top-k lists do not fit
   const size_t need = ws_total(a->K, a->bs, 0);
   if (need > kStaticScratchBytes) return DSPARK_ERR_WORKSPACE;
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DSPARK_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice, "dspark_walk_noalloc device index");
   void* scratch = nullptr;
   {
     // Once per device, with that device current: the array's device address. In host
@@ -50,7 +51,8 @@ extern "C" int32_t dspark_walk_noalloc(const dspark_walk_args* a, dspark_stream_
     if (!g_scratch_ptr[dev]) {
       void* p = nullptr;
       e = cudaGetSymbolAddress(&p, g_walk_scratch);
-      if (e != cudaSuccess || !p) return DSPARK_ERR_CUDA;
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static walk scratch)");
+      if (!p) return cuda_fail(cudaErrorInvalidSymbol, "cudaGetSymbolAddress(static walk scratch)");
       g_scratch_ptr[dev] = p;
     }
     scratch = g_scratch_ptr[dev];
@@ -59,7 +61,7 @@ extern "C" int32_t dspark_walk_noalloc(const dspark_walk_args* a, dspark_stream_
   // The array keeps the previous call's contents (a timed-out call leaves it dirty):
   // clear the part this walk uses. Calls that overlap on the GPU race on the array.
   e = cudaMemsetAsync(scratch, 0, need, s);
-  if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static walk scratch)");
   dspark_walk_args b = *a;
   b.workspace = scratch;
   b.workspace_bytes = kStaticScratchBytes;

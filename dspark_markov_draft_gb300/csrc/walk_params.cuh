@@ -25,18 +25,19 @@ struct WalkParams {
   int32_t temp_is_one;
   int32_t resident_rows;     // W2 rows per CTA kept in shared memory (multiple of 32)
   int32_t slice_cap;         // upper bound of the rows of one CTA's vocabulary slice
+  int32_t w2_tma;            // w2_map is valid (tensor-core walk)
   int32_t base_tma;          // base_map is valid (tensor-core walk)
-  int32_t logits_tma;        // logits_map is valid (tensor-core walk)
   float inv_temperature;     // 1 / temperature, rounded to fp32 (tensor-core walk)
   const float* temps;        // [bs] per-row temperatures, or null (then `temperature`)
   const int32_t* modes;      // [bs] per-row modes, or null (then the kernel's mode)
   StepSync sync;
-  // Tensor map over base [bs][K][V] (bf16), box {32 rows, 1 position, N/2 requests}:
-  // one tile copy brings an epilogue warp's base logits of one 128-row tile.
-  CUtensorMap base_map;      // 128-byte aligned type
-  // The same geometry over draft_logits: an epilogue warp's tile of bf16 logits goes
-  // back to global memory in one tile copy.
-  CUtensorMap logits_map;
+  // Tensor map over the W2 rows (int8 [V][256] or bf16 [V][256]), box of 32 rows x 128
+  // bytes with the 128-byte swizzle: the tensor-core walk copies its shared-memory
+  // resident rows with it, 32 rows and one 128-byte part of the row per copy.
+  CUtensorMap w2_map;        // 128-byte aligned type
+  // Tensor map over the base logits [bs][K][V] (bf16), box of 128 vocabulary rows x 1
+  // position x N requests: one copy stages a tile's base logits for every request.
+  CUtensorMap base_map;
 };
 
 // Per-row sampling settings. A PROB kernel serves batches with at least one sampled
@@ -91,19 +92,36 @@ __host__ __device__ inline int64_t slice_start(int c, int G, int64_t V) {
   return (static_cast<int64_t>(c) * V / G) & ~static_cast<int64_t>(31);
 }
 
-// Tensor-core walk: threads per CTA for N padded request rows. N = 16 adds two warps
-// that only issue MMAs (18 warps, 96 registers per thread); N = 32 and 64 keep 16
-// warps, the issuing done by two producer warps, so that the epilogue keeps 128
-// registers per thread.
-__host__ __device__ constexpr int walk_tc_threads(int N) { return N <= 16 ? 576 : 512; }
-
-// Tensor-core walk epilogue: base logits staged per epilogue warp (8), two
-// tiles of 32 rows x N/2 request rows, bf16. The epilogue keeps tile numbers in 8-bit
-// fields, so a CTA's vocabulary slice holds at most kTcMaxTiles tiles of 128 rows.
+// Tensor-core walk: six warpgroups -- 4 producer warps, 16 epilogue warps, and a last
+// warpgroup whose first warp issues the MMAs. The kernel is compiled for kTcLaunchRegs
+// registers per thread (the most that 6 warps per SM sub-partition allow); the
+// warpgroups then rebalance them with setmaxnreg: producers kTcProducerRegs, epilogue
+// kTcEpilogueRegs, the issuing warpgroup kTcIssuerRegs. The shares add up to exactly
+// the launch's total, so no request waits for registers that are not there.
+constexpr int kTcProducerWarps = 4;
+constexpr int kTcEpilogueWarps = 16;
+constexpr int kTcThreads = (kTcProducerWarps + kTcEpilogueWarps + 4) * 32;
+constexpr int kTcLaunchRegs = 80;
+constexpr int kTcProducerRegs = 80;
+constexpr int kTcEpilogueRegs = 88;
+constexpr int kTcIssuerRegs = 48;
+static_assert(kTcProducerWarps * 32 * kTcProducerRegs + kTcEpilogueWarps * 32 * kTcEpilogueRegs +
+                      4 * 32 * kTcIssuerRegs ==
+                  kTcThreads * kTcLaunchRegs,
+              "the warpgroups' register shares must add up to the launch's registers");
+// The epilogue keeps tile numbers in 8-bit fields, so a CTA's vocabulary slice holds at
+// most kTcMaxTiles tiles of 128 rows.
 constexpr int kTcMaxTiles = 255;
-__host__ __device__ constexpr int walk_tc_stage_bytes(int N) { return 8 * 2 * (N / 2) * 32 * 2; }
 
-// Tensor-core walk: shared memory besides the B operand and the resident rows.
+// Tensor-core walk: stages of base logits staged by tensor-map copies (128 rows x N
+// requests, bf16, each).
+__host__ __device__ constexpr int tc_base_stages(int N) { return N >= 64 ? 3 : 4; }
+__host__ __device__ constexpr size_t tc_stage_ring_bytes(int N) {
+  return static_cast<size_t>(tc_base_stages(N)) * 128 * N * 2;
+}
+
+// Tensor-core walk: shared memory besides the B operand, the base-logit stages, the
+// slice's scales and the resident rows.
 __host__ __device__ inline size_t walk_tc_misc_smem() {
   return 64 * 4          // prev tokens
          + 64 * 8        // seeds
@@ -111,7 +129,7 @@ __host__ __device__ inline size_t walk_tc_misc_smem() {
          + 4 * 64 * 8    // per-quadrant argmax words
          + 2 * 8         // 2^-s as two factors
          + 64 * 4 + 8    // 1/T per row, greedy-row mask
-         + 30 * 8 + 16;  // mbarriers, TMEM base, flag, batch |e| maximum
+         + 24 * 8 + 32;  // mbarriers, TMEM base, flags, batch |e| maximum
 }
 
 }  // namespace dspark

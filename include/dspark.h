@@ -192,14 +192,18 @@ int32_t dspark_gumbel_noise(const uint64_t* seeds, int32_t bs, int32_t K, int64_
  * whose device memory is all pre-reserved by a caching allocator; cudaMalloc on the
  * decode path would fail or synchronise). The pages have no counterpart of this call.
  *   - Takes the same arguments as dspark_walk; `workspace` and `workspace_bytes` are
- *     ignored. Full-vocabulary walk only: top_k > 0 returns DSPARK_ERR_UNSUPPORTED.
- *     Invalid arguments return DSPARK_ERR_INVALID_ARG before any CUDA call.
+ *     ignored. Invalid arguments return DSPARK_ERR_INVALID_ARG before any CUDA call
+ *     (the same checks as dspark_walk); then, full-vocabulary walk only: a valid
+ *     top_k > 0 returns DSPARK_ERR_UNSUPPORTED.
  *   - Scratch comes from one static device array of 24,576 bytes inside the library,
  *     held by every GPU that loads the library until the process exits. A shape whose
  *     scratch would not fit returns DSPARK_ERR_WORKSPACE (every shape dspark_walk
  *     accepts fits).
  *   - The first call on a device looks up the array's device address with that device
- *     current; make that first call before any stream capture.
+ *     current. With CUDA's lazy module loading (the default) that lookup also loads
+ *     this part of the library onto the device, which creates the array's storage
+ *     then: make the first call on each device at start-up, before the caller hands
+ *     its device memory to a caching allocator and before any stream capture.
  *   - Each call clears the part of the array it uses with cudaMemsetAsync on `stream`,
  *     then launches the walk; it calls no allocating routine. All calls share the
  *     array, so calls whose kernels overlap on the GPU (different streams, no ordering)

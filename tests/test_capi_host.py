@@ -90,6 +90,7 @@ def test_invalid_arguments_rejected_on_host(L):
             assert f(C.byref(args(**bad)), None) == 1, (f, bad)
     assert L.dspark_walk_topk(C.byref(args(top_k=0)), None) == 1      # k >= 1 required
     assert L.dspark_walk_noalloc(C.byref(args(top_k=5)), None) == 2   # full vocabulary only
+    assert L.dspark_walk_noalloc(C.byref(args(top_k=-1)), None) == 1  # invalid before unsupported
     assert L.dspark_walk(C.byref(args(workspace_bytes=16)), None) == 8
     assert L.dspark_walk(C.byref(args(workspace=None)), None) == 8
     assert L.dspark_walk(C.byref(args(workspace=fake + 128)), None) == 8   # not 256-byte aligned

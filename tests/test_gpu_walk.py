@@ -244,6 +244,23 @@ def test_vocabulary_smaller_than_grid(oracle, bs):
         check_walk(oracle, inp, tokens, mode=mode, q=q_ref, sc=sc_ref, gpu_logits=lg)
 
 
+@pytest.mark.parametrize("flags", [capi.FLAG_FORCE_CUDA_CORES, capi.FLAG_FORCE_TENSOR_CORES])
+def test_small_shared_memory_plan_keeps_one_cta_per_sm(oracle, flags):
+    """Both walks allocate all of tensor memory, so a second CTA on an SM would wait in
+    the allocation until the first exits. With a tiny vocabulary and no resident rows the
+    shared-memory request alone would allow several CTAs per SM; the launch raises it so
+    that one fits, and the walk completes correctly."""
+    V, K, bs = 64, 3, 2
+    inp = synth.make(V, bs, K, seed=66)
+    w1, w2, base, prev, seeds = to_dev(inp)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    tokens, _ = capi.walk(base, w1, prev, w2=w2, resident_rows_cap=0, flags=flags,
+                          status=status, timeout_us=200000)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    check_walk(oracle, inp, tokens, mode=capi.GREEDY)
+
+
 @pytest.mark.parametrize("bs", [1, 8])
 def test_timeout_returns_status_and_context_survives(bs):
     """CTA 0 skips its first arrival: every wait gives up after 20 ms and reports

@@ -3,11 +3,11 @@
 The allocation-free entry point serves callers that cannot call cudaMalloc (a plugin
 enqueue hook, or a server whose device memory is all pre-reserved): its scratch is a
 static device array inside the library instead of a caller-provided workspace. Here it
-runs through the C ABI twice in a row on the same inputs -- so the second call finds
-the array holding the first call's contents -- and each result must match the regular
+runs through the C ABI twice in a row on the same inputs, and each result must match the regular
 entry point's within the parity tolerances (tokens identical, logits within
-2e-2 + 1e-2 |x|). This file is collected last so that a failure here cannot stop the
-rest of the suite.
+2e-2 + 1e-2 |x|). A call after one whose wait timed out (leaving the array dirty) must
+match as well. This file is collected last so that a failure here cannot stop the rest
+of the suite.
 """
 import ctypes as C
 
@@ -61,6 +61,33 @@ def test_noalloc_matches_walk_twice(int8, mode, T, bs, K):
         fin = np.isfinite(r)
         assert np.array_equal(np.isfinite(g), fin)
         assert np.all(np.abs(g[fin] - r[fin]) <= 2e-2 + 1e-2 * np.abs(r[fin]))
+
+
+def test_noalloc_recovers_after_a_timed_out_call():
+    """A call whose grid barrier gives up (CTA 0 skips its first arrival, a 20 ms limit)
+    leaves the static array dirty; the next call clears it first and must then match the
+    regular entry point."""
+    V, bs, K = 6007, 2, 3
+    inp = synth.make(V, bs, K, seed=43)
+    dev = "cuda"
+    w1, w2 = inp.w1.to(dev), inp.w2.to(dev)
+    base, prev = inp.base.to(dev), inp.prev.to(dev)
+    ref_tok, _ = capi.walk(base, w1, prev, w2=w2)
+    torch.cuda.synchronize()
+    unused_ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    tok = torch.full((bs, K), -7, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    args = capi.make_args(base, w1, prev, tok, unused_ws, w2=w2, status=status,
+                          flags=capi.FLAG_SKIP_ARRIVAL_CTA0, timeout_us=20000)
+    assert capi.walk_noalloc(args) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 5  # TIMEOUT
+    status.zero_()
+    args = capi.make_args(base, w1, prev, tok, unused_ws, w2=w2, status=status)
+    assert capi.walk_noalloc(args) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(tok, ref_tok)
 
 
 def test_noalloc_rejects_topk():
