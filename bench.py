@@ -7,9 +7,8 @@ in the pages' own kernel benchmark. Inputs are seeded synthetic tensors of the
 workload's shapes and distributions, resident in HBM before timing starts.
 
 Default workload: V=151936, rank 256, K=7, bs=64, int8 W2 (per-row fp32 scales),
-greedy, base logits N(0, 3^2) with one +8 peak per row and position. Further lines of
-the same configuration family (bs 1 and 16, probabilistic T=1) are reported under
-"variants".
+greedy, base logits N(0, 3^2) with one +8 peak per row and position. Every other
+configuration of the workload family is timed too and reported under "variants".
 
 Usage:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -39,26 +38,32 @@ R = 256
 
 MAIN = dict(name="v151936_k7_bs64_int8_greedy", V=151936, K=7, bs=64, int8=True, mode=0, T=1.0,
             top_k=0, peak=8.0, logits=False)
+
+
+def _cfg(name, V, K, bs, int8, mode, T, top_k=0, peak=None, logits=False):
+    return dict(name=name, V=V, K=K, bs=bs, int8=int8, mode=mode, T=T, top_k=top_k, peak=peak, logits=logits)
+
+
+# Every configuration of the workload family, timed as "variants" beside the main line:
+# V=129280 K=5 bs=1 bf16 greedy; V=151936 K=7 int8 at bs 1/16/64, greedy and sampled at
+# T=1 with a +8 peak; V=151936 K=16 bf16 sampled at T=0.7 writing draft_logits, bs 1/64;
+# V=248320 K=16 int8 greedy at bs 1/16/64; the top-k walk at V=151936 K=7 bs=64, k 512 and
+# 4096, sampled at T=1.
 VARIANTS = [
-    dict(name="v151936_k7_bs1_int8_greedy", V=151936, K=7, bs=1, int8=True, mode=0, T=1.0, top_k=0, peak=8.0, logits=False),
-    dict(name="v151936_k7_bs1_int8_prob", V=151936, K=7, bs=1, int8=True, mode=1, T=1.0, top_k=0, peak=8.0, logits=False),
-    dict(name="v151936_k7_bs16_int8_greedy", V=151936, K=7, bs=16, int8=True, mode=0, T=1.0, top_k=0, peak=8.0, logits=False),
-    dict(name="v151936_k7_bs64_int8_prob", V=151936, K=7, bs=64, int8=True, mode=1, T=1.0, top_k=0, peak=8.0, logits=False),
+    _cfg("v129280_k5_bs1_bf16_greedy", 129280, 5, 1, False, 0, 1.0),
+    _cfg("v151936_k7_bs1_int8_greedy", 151936, 7, 1, True, 0, 1.0, peak=8.0),
+    _cfg("v151936_k7_bs1_int8_prob", 151936, 7, 1, True, 1, 1.0, peak=8.0),
+    _cfg("v151936_k7_bs16_int8_greedy", 151936, 7, 16, True, 0, 1.0, peak=8.0),
+    _cfg("v151936_k7_bs16_int8_prob", 151936, 7, 16, True, 1, 1.0, peak=8.0),
+    _cfg("v151936_k7_bs64_int8_prob", 151936, 7, 64, True, 1, 1.0, peak=8.0),
+    _cfg("v151936_k16_bs1_bf16_prob_logits", 151936, 16, 1, False, 1, 0.7, peak=8.0, logits=True),
+    _cfg("v151936_k16_bs64_bf16_prob_logits", 151936, 16, 64, False, 1, 0.7, peak=8.0, logits=True),
+    _cfg("v248320_k16_bs1_int8_greedy", 248320, 16, 1, True, 0, 1.0),
+    _cfg("v248320_k16_bs16_int8_greedy", 248320, 16, 16, True, 0, 1.0),
+    _cfg("v248320_k16_bs64_int8_greedy", 248320, 16, 64, True, 0, 1.0),
+    _cfg("v151936_k7_bs64_topk512_prob", 151936, 7, 64, False, 1, 1.0, top_k=512),
+    _cfg("v151936_k7_bs64_topk4096_prob", 151936, 7, 64, False, 1, 1.0, top_k=4096),
 ]
-
-
-# Further workloads that can be selected with --workload (parity cases, not bench lines).
-EXTRA = [
-    dict(name="v129280_k5_bs1_bf16_greedy", V=129280, K=5, bs=1, int8=False, mode=0, T=1.0, top_k=0, peak=None, logits=False),
-    dict(name="v151936_k16_bs1_bf16_prob_logits", V=151936, K=16, bs=1, int8=False, mode=1, T=0.7, top_k=0, peak=8.0, logits=True),
-    dict(name="v151936_k16_bs64_bf16_prob_logits", V=151936, K=16, bs=64, int8=False, mode=1, T=0.7, top_k=0, peak=8.0, logits=True),
-    dict(name="v248320_k16_bs1_int8_greedy", V=248320, K=16, bs=1, int8=True, mode=0, T=1.0, top_k=0, peak=None, logits=False),
-    dict(name="v248320_k16_bs64_int8_greedy", V=248320, K=16, bs=64, int8=True, mode=0, T=1.0, top_k=0, peak=None, logits=False),
-    dict(name="v151936_k7_bs64_topk512_prob", V=151936, K=7, bs=64, int8=False, mode=1, T=1.0, top_k=512, peak=None, logits=False),
-    dict(name="v151936_k7_bs64_topk4096_prob", V=151936, K=7, bs=64, int8=False, mode=1, T=1.0, top_k=4096, peak=None, logits=False),
-]
-
-
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -68,12 +73,16 @@ def load_peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, sm_mhz=2070.0, src="fallback")
 
 
-# Per-SM issue rates used for the on-chip floors (nominal Blackwell figures): 128 bytes
-# of shared memory per clock, 64 dp4a lanes per clock (half the fp32 lanes), 128 fp32
-# FMA lanes per clock.
-SMEM_B_PER_CLK = 128
-DP4A_PER_CLK = 64
+# Per-SM rates used for the on-chip floors: shared memory 512 bytes per clock (16-byte
+# loads without bank conflicts, measured on this GPU with a single-SM probe), 128 fp32
+# FMA lanes per clock, 16 multi-function-unit lanes per clock (logarithms).
+SMEM_B_PER_CLK = 512
 FFMA_PER_CLK = 128
+MUFU_PER_CLK = 16
+# Instructions per Gumbel draw on the integer/fp32 pipes besides the two logarithms:
+# a quarter of a Philox4x32-10 block (10 rounds of two 32x32 multiplies with high halves
+# and four xors, ~8 instructions per round) plus the uniform and the series.
+GUMBEL_ALU_PER_DRAW = 30
 
 
 def row_bytes(cfg) -> int:
@@ -82,62 +91,81 @@ def row_bytes(cfg) -> int:
 
 def hbm_bytes(cfg) -> float:
     """Algorithmic HBM bytes of one walk: W2 (+ scales) once, every base logit once, the
-    K embedding rows per request, the tokens, and draft_logits when written."""
+    K embedding rows per request, the tokens, and draft_logits when written. The top-k
+    walk reads each gathered bf16 W2 row from L2 (see floors); HBM sees W2 at most once."""
     V, K, bs = cfg["V"], cfg["K"], cfg["bs"]
     w2 = V * row_bytes(cfg) + (4 * V if cfg["int8"] else 0)
-    if cfg["top_k"]:
-        w2 = bs * K * cfg["top_k"] * R * 2
     base = bs * K * V * 2
     emb = bs * K * R * 2
     out = bs * K * 4 + (bs * K * V * 2 if cfg["logits"] else 0)
     return float(w2 + base + emb + out)
 
 
+def gathered_bytes(cfg) -> float:
+    """Bytes of the candidate rows the top-k walk gathers (from L2): one W2 row per
+    candidate, request row and position (int8 rows carry their fp32 scale)."""
+    k = cfg["top_k"]
+    return float(cfg["bs"] * cfg["K"] * k * (row_bytes(cfg) + (4 if cfg["int8"] else 0)))
+
+
 def uses_tensor_cores(cfg) -> bool:
     return cfg["top_k"] == 0 and cfg["bs"] >= 3
 
 
+def contraction_flops(cfg) -> float:
+    """The method's multiply-adds (2 flops each): every vocabulary row (top-k: every
+    candidate) against every request row's embedding, at every position."""
+    rows = cfg["top_k"] if cfg["top_k"] else cfg["V"]
+    return 2.0 * rows * R * cfg["bs"] * cfg["K"]
+
+
 def floors(cfg, peaks, sms: int, resident_rows: int, l2_gbs: float):
-    """Lower bounds (µs) of one walk, per resource. Memory: HBM (W2 once, base logits,
+    """Lower bounds (us) of one walk, per resource. Memory: HBM (W2 once, base logits,
     outputs), shared memory (the resident W2 rows read at every position), L2 (the
-    streamed W2 rows at positions 1..K-1). Contraction: 2 V 256 bs K flops on the
-    tensor cores (bs >= 3), or the dp4a / fp32 FMA instructions of the CUDA-core
-    contraction (bs <= 2). The roofline is the slowest of them."""
+    streamed W2 rows at positions 1..K-1; top-k: every gathered candidate row).
+    Contraction: the method's flops on the tensor cores (tensor-core walk, bs >= 3) or on
+    the fp32 FMA pipe (CUDA-core and top-k walks). The roofline is the slowest of them.
+    Sampled walks also get an informational floor for the Gumbel draws ("gumbel_us":
+    two logarithms per draw on the multi-function units, or the other instructions of a
+    draw at the fp32 issue rate), not part of the roofline."""
     V, K, bs = cfg["V"], cfg["K"], cfg["bs"]
     clk = peaks["sm_mhz"] * 1e6
     out = {"hbm_us": hbm_bytes(cfg) / (peaks["hbm_gbs"] * 1e9) * 1e6}
     if cfg["top_k"]:
-        return out
-    rb = row_bytes(cfg)
-    res_b = resident_rows * rb
-    out["smem_us"] = K * res_b / (SMEM_B_PER_CLK * sms * clk) * 1e6
-    out["l2_us"] = (K - 1) * (V - resident_rows) * rb / (l2_gbs * 1e9) * 1e6
-    if uses_tensor_cores(cfg):
-        out["tensor_us"] = 2.0 * V * R * bs * K / (peaks["bf16_tflops"] * 1e12) * 1e6
+        out["l2_us"] = gathered_bytes(cfg) / (l2_gbs * 1e9) * 1e6
+        out["fma_us"] = contraction_flops(cfg) / (2 * FFMA_PER_CLK * sms * clk) * 1e6
     else:
-        ops, lanes = alu_ops(cfg)  # int8: 3 byte limbs of the embedding, one dp4a per 4 codes each
-        out["alu_us"] = ops / (lanes * sms * clk) * 1e6
+        rb = row_bytes(cfg)
+        out["smem_us"] = K * resident_rows * rb / (SMEM_B_PER_CLK * sms * clk) * 1e6
+        out["l2_us"] = (K - 1) * (V - resident_rows) * rb / (l2_gbs * 1e9) * 1e6
+        if uses_tensor_cores(cfg):
+            out["tensor_us"] = contraction_flops(cfg) / (peaks["bf16_tflops"] * 1e12) * 1e6
+        else:
+            out["fma_us"] = contraction_flops(cfg) / (2 * FFMA_PER_CLK * sms * clk) * 1e6
     return out
 
 
-def alu_ops(cfg) -> tuple[float, int]:
-    """(instructions per walk, lanes per clock per SM) of the CUDA-core contraction."""
-    n = float(cfg["V"]) * R * cfg["bs"] * cfg["K"]
-    return (3.0 * n / 4, DP4A_PER_CLK) if cfg["int8"] else (n, FFMA_PER_CLK)
+def gumbel_floor_us(cfg, peaks, sms: int) -> float | None:
+    """Informational floor of the Gumbel draws of a sampled walk (None when greedy)."""
+    if cfg["mode"] != 1:
+        return None
+    draws = float(cfg["bs"] * cfg["K"] * (cfg["top_k"] or cfg["V"]))
+    clk = peaks["sm_mhz"] * 1e6
+    return max(2 * draws / (MUFU_PER_CLK * sms * clk), GUMBEL_ALU_PER_DRAW * draws / (FFMA_PER_CLK * sms * clk)) * 1e6
 
 
 def roofline(cfg, peaks, fl, us, sms: int):
     """The roofline object for the slowest floor: achieved = that resource's algorithmic
     work per walk / measured walk time, against its peak."""
     key = max(fl, key=fl.get)
+    clk = peaks["sm_mhz"] * 1e6
     if key == "tensor_us":
-        ach = 2.0 * cfg["V"] * R * cfg["bs"] * cfg["K"] / (us * 1e-6) / 1e12
+        ach = contraction_flops(cfg) / (us * 1e-6) / 1e12
         r = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
-    elif key == "alu_us":
-        ops, lanes = alu_ops(cfg)
-        peak = lanes * sms * peaks["sm_mhz"] * 1e6 / 1e9
-        r = {"bound": "alu", "achieved": ops / (us * 1e-6) / 1e9, "peak": peak,
-             "unit": "G dp4a/s" if cfg["int8"] else "G FMA/s"}
+    elif key == "fma_us":
+        peak = 2 * FFMA_PER_CLK * sms * clk / 1e12
+        r = {"bound": "fma", "achieved": contraction_flops(cfg) / (us * 1e-6) / 1e12, "peak": peak,
+             "unit": "TFLOP/s (fp32 FMA)"}
     elif key == "smem_us":
         r = {"bound": "smem", "achieved": fl[key] / us, "peak": 1.0, "unit": "fraction"}
     elif key == "l2_us":
@@ -403,6 +431,20 @@ class OracleRunner:
         self.prev = inp.prev.numpy()
         self.seeds = inp.seeds.numpy().astype(np.uint64)
 
+    def parity(self, gpu_tokens, nthreads: int) -> dict:
+        """Teacher-forced check of the GPU's tokens of these inputs (every row): at each
+        step the GPU token is the oracle's, a near tie (within 1e-3 of the best score),
+        a bf16-boundary case, or rejected."""
+        c = self.cfg
+        follow = np.ascontiguousarray(gpu_tokens, dtype=np.int32)
+        r = self.O.walk(self.base, self.w1, self.prev, c["K"], seeds=self.seeds, mode=c["mode"],
+                        temperature=c["T"], top_k=c["top_k"], follow=follow, nthreads=nthreads, **self.kw)
+        cls = r.follow_class
+        return {"steps": int(cls.size), "same": int((cls == self.O.CLASS_SAME).sum()),
+                "near_tie": int((cls == self.O.CLASS_NEAR_TIE).sum()),
+                "bf16_boundary": int((cls == self.O.CLASS_BF16_BOUNDARY).sum()),
+                "rejected": int((cls == self.O.CLASS_REJECTED).sum()), "tie_tol": 1e-3, "bf16_eps": 1e-4}
+
     def run(self, rows: int, nthreads: int) -> float:
         """Seconds for a walk of the first `rows` rows."""
         c = self.cfg
@@ -416,9 +458,12 @@ class OracleRunner:
         return dt
 
 
-def cpu_baseline(cfg, target_s: float = 12.0):
-    """Oracle throughput on a bounded sample of the workload: enough request rows (all
-    K positions) for about `target_s` seconds of CPU work, capped at the whole batch."""
+def cpu_baseline(cfg, gpu_tokens=None, target_s: float = 10.0, single_s: float = 3.0):
+    """The oracle on the host cores, on a bounded sample of the workload: all cores
+    (OpenMP over the vocabulary) on whole request rows (all K positions) for about
+    `target_s` seconds, and one core on single rows for about `single_s` seconds. When
+    the GPU's tokens of the same inputs are given, the same leg also checks them against
+    the oracle, teacher-forced over every row (the parity counts)."""
     cores = host_cores()
     runner = OracleRunner(cfg, cfg["bs"])
     t1 = runner.run(1, cores)
@@ -426,9 +471,17 @@ def cpu_baseline(cfg, target_s: float = 12.0):
     reps = 1 if rows < cfg["bs"] else int(min(20, max(1, target_s / max(rows * t1, 1e-6))))
     dt = sum(runner.run(rows, cores) for _ in range(reps))
     toks = reps * rows * cfg["K"]
-    return {"value": toks / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{reps} x {rows} of {cfg['bs']} request rows, all {cfg['K']} positions, "
-                      f"{dt:.1f} s of oracle time"}
+    out = {"value": toks / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": f"{reps} x {rows} of {cfg['bs']} request rows, all {cfg['K']} positions, "
+                     f"{dt:.1f} s of oracle time"}
+    s1 = runner.run(1, 1)
+    reps1 = int(max(1, min(20, single_s / max(s1, 1e-6)))) - 1
+    s1 += sum(runner.run(1, 1) for _ in range(reps1))
+    out["single_thread"] = {"value": (reps1 + 1) * cfg["K"] / s1, "unit": UNIT, "cores": 1,
+                            "sample": f"{reps1 + 1} x 1 request row, all {cfg['K']} positions, {s1:.1f} s"}
+    if gpu_tokens is not None:
+        out["parity"] = runner.parity(gpu_tokens, cores)
+    return out
 
 
 def reference_arm(a, rank, world):
@@ -528,7 +581,7 @@ def main():
     peaks = load_peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 129 MB L2
-    by_name = {c["name"]: c for c in [MAIN] + VARIANTS + EXTRA}
+    by_name = {c["name"]: c for c in [MAIN] + VARIANTS}
     cfg = by_name[a.workload]
 
     def floors_of(c):
@@ -537,6 +590,9 @@ def main():
             _, res = capi.query_capacity(local, c["V"], c["int8"], c["bs"])
         fl = floors(c, peaks, sms, res, l2_gbs)
         return fl, res
+
+    def kernels_per_walk(c):
+        return 2 if c["top_k"] else 1
 
     l2_gbs = measure_l2_gbs(dev)
     # untimed warm-up of the whole path, then the timed walks
@@ -567,26 +623,31 @@ def main():
     floor_rec = {k: round(v, 3) for k, v in fl.items()}
     floor_rec.update({"floor_us": round(floor_us, 3), "frac_of_floor": floor_us / us,
                       "resident_w2_rows": res_rows, "l2_gbs_live": round(l2_gbs, 1),
-                      "hbm_bytes": hbm_bytes(cfg)})
+                      "hbm_bytes": hbm_bytes(cfg), "gumbel_us_informational": gumbel_floor_us(cfg, peaks, sms)})
 
     variants = []
     if not a.no_variants:
         for vc in VARIANTS:
-            vt, _, _ = time_walks(vc, max(5, a.steps // 2), 3, dev, flush)
+            if vc["name"] == cfg["name"]:
+                continue
+            vt, vtens, _ = time_walks(vc, max(5, a.steps // 2), 3, dev, flush)
+            del vtens
+            torch.cuda.empty_cache()
             vus = 1000 * statistics.mean(vt)
             vfl, vres = floors_of(vc)
             vfloor = max(vfl.values())
             vr = roofline(vc, peaks, vfl, vus, sms)
             variants.append({"workload": vc["name"], "us_per_walk": vus,
                              "draft_tokens_per_s": vc["bs"] * vc["K"] / (vus * 1e-6),
-                             "kernel": kernel_name(vc), "floor_us": vfloor,
-                             "frac_of_floor": vfloor / vus,
+                             "kernel": kernel_name(vc), "kernels_per_walk": kernels_per_walk(vc),
+                             "floor_us": vfloor, "frac_of_floor": vfloor / vus,
                              "bound": vr["bound"], "frac": vr["frac"],
-                             "floors_us": {k: round(v, 3) for k, v in vfl.items()}})
+                             "floors_us": {k: round(v, 3) for k, v in vfl.items()},
+                             "gumbel_us_informational": gumbel_floor_us(vc, peaks, sms)})
 
     cpu = None
     if rank == 0 and not a.no_cpu_baseline:
-        cpu = cpu_baseline(cfg)
+        cpu = cpu_baseline(cfg, gpu_tokens=t["tokens"].cpu().numpy())
 
     if rank == 0:
         tc = uses_tensor_cores(cfg)
@@ -594,6 +655,9 @@ def main():
                   else "bf16 x bf16, fp32 accumulate (tcgen05)") if tc else
                  ("int8 x 24-bit integer embedding (dp4a), fp32 epilogue" if cfg["int8"]
                   else "bf16 x bf16, fp32 FMA"))
+        parity = (cpu or {}).get("parity")
+        if cpu and "parity" in cpu:
+            cpu = {k: v for k, v in cpu.items() if k != "parity"}
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -613,7 +677,8 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": world * toks / (e2e_ms * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": a.steps * (2 if cfg["top_k"] else 1),
+            "parity": parity,
+            "gpu_launches": a.steps * kernels_per_walk(cfg),
             "clocks": clk.summary(),
             "wall_s_timed": wall,
             "variants": variants,

@@ -52,27 +52,33 @@ class _WalkArgs(C.Structure):
 _lib = None
 
 
+def bind(L):
+    """Declare the C signatures of an oracle library handle (also used by the tests
+    that build copies of the oracle with planted mistakes)."""
+    L.oracle_bf16_to_double.restype = C.c_double
+    L.oracle_bf16_to_double.argtypes = [C.c_uint16]
+    L.oracle_round_bf16.restype = C.c_uint16
+    L.oracle_round_bf16.argtypes = [C.c_double]
+    L.oracle_philox4x32_10.restype = None
+    L.oracle_philox4x32_10.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p]
+    L.oracle_gumbel_block.restype = None
+    L.oracle_gumbel_block.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_int64,
+                                      C.c_void_p, C.c_void_p, C.c_void_p]
+    L.oracle_quantize_w2.restype = C.c_int32
+    L.oracle_quantize_w2.argtypes = [C.c_void_p, C.c_int64, C.c_int32, C.c_void_p,
+                                     C.c_void_p]
+    L.oracle_topk_select.restype = C.c_int32
+    L.oracle_topk_select.argtypes = [C.c_void_p, C.c_int32, C.c_int64, C.c_int32,
+                                     C.c_void_p]
+    L.oracle_walk.restype = C.c_int32
+    L.oracle_walk.argtypes = [C.POINTER(_WalkArgs)]
+    return L
+
+
 def lib():
     global _lib
     if _lib is None:
-        _lib = C.CDLL(build())
-        _lib.oracle_bf16_to_double.restype = C.c_double
-        _lib.oracle_bf16_to_double.argtypes = [C.c_uint16]
-        _lib.oracle_round_bf16.restype = C.c_uint16
-        _lib.oracle_round_bf16.argtypes = [C.c_double]
-        _lib.oracle_philox4x32_10.restype = None
-        _lib.oracle_philox4x32_10.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p]
-        _lib.oracle_gumbel_block.restype = None
-        _lib.oracle_gumbel_block.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_int64,
-                                             C.c_void_p, C.c_void_p, C.c_void_p]
-        _lib.oracle_quantize_w2.restype = C.c_int32
-        _lib.oracle_quantize_w2.argtypes = [C.c_void_p, C.c_int64, C.c_int32, C.c_void_p,
-                                            C.c_void_p]
-        _lib.oracle_topk_select.restype = C.c_int32
-        _lib.oracle_topk_select.argtypes = [C.c_void_p, C.c_int32, C.c_int64, C.c_int32,
-                                            C.c_void_p]
-        _lib.oracle_walk.restype = C.c_int32
-        _lib.oracle_walk.argtypes = [C.POINTER(_WalkArgs)]
+        _lib = bind(C.CDLL(build()))
     return _lib
 
 

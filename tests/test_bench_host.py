@@ -20,8 +20,9 @@ def test_hbm_bytes_count_draft_logits_and_top_k_candidates():
     cfg = dict(bench.MAIN, logits=True)
     assert bench.hbm_bytes(cfg) - bench.hbm_bytes(bench.MAIN) == 64 * 7 * 151936 * 2
     tk = dict(bench.MAIN, top_k=512, int8=False)
-    # the candidate walk reads one bf16 W2 row per candidate instead of W2 once
-    assert bench.hbm_bytes(tk) == 64 * 7 * 512 * 256 * 2 + 64 * 7 * 151936 * 2 + 64 * 7 * 256 * 2 + 64 * 7 * 4
+    # HBM: bf16 W2 at most once and the base logits; the gathered candidate rows are L2 work
+    assert bench.hbm_bytes(tk) == 151936 * 512 + 64 * 7 * 151936 * 2 + 64 * 7 * 256 * 2 + 64 * 7 * 4
+    assert bench.gathered_bytes(tk) == 64 * 7 * 512 * 512
 
 
 PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, sm_mhz=2000.0, src="fallback")
@@ -40,15 +41,37 @@ def test_roofline_takes_the_slowest_floor_and_its_fraction():
         assert r["achieved"] * 1e9 * us * 1e-6 == pytest.approx(bench.hbm_bytes(cfg))
 
 
-def test_small_batches_are_bound_by_dp4a_issue():
+def test_small_batches_take_the_fp32_contraction_floor():
+    """bs <= 2: the method's multiply-adds at the fp32 FMA pipe's peak (128 lanes per SM
+    and clock, two flops each) -- not the implementation's byte limbs."""
     cfg = dict(bench.MAIN, bs=1)
     fl = bench.floors(cfg, PEAKS, sms=152, resident_rows=150_000, l2_gbs=20_000.0)
-    assert "alu_us" in fl and "tensor_us" not in fl
-    ops, lanes = bench.alu_ops(cfg)
-    assert ops == 3 * 151936 * 256 * 7 / 4 and lanes == 64
-    assert fl["alu_us"] == pytest.approx(ops / (lanes * 152 * 2000e6) * 1e6)
-    r = bench.roofline(cfg, PEAKS, {"alu_us": fl["alu_us"]}, 2 * fl["alu_us"], sms=152)
-    assert r["bound"] == "alu" and r["frac"] == pytest.approx(0.5)
+    assert "fma_us" in fl and "tensor_us" not in fl
+    flops = 2.0 * 151936 * 256 * 7
+    assert bench.contraction_flops(cfg) == flops
+    assert fl["fma_us"] == pytest.approx(flops / (2 * 128 * 152 * 2000e6) * 1e6)
+    r = bench.roofline(cfg, PEAKS, {"fma_us": fl["fma_us"]}, 2 * fl["fma_us"], sms=152)
+    assert r["bound"] == "fma" and r["frac"] == pytest.approx(0.5)
+
+
+def test_top_k_floors_put_gathered_rows_on_l2():
+    tk = dict(bench.MAIN, top_k=4096, int8=False, mode=1)
+    fl = bench.floors(tk, PEAKS, sms=152, resident_rows=0, l2_gbs=8_000.0)
+    assert fl["l2_us"] == pytest.approx(64 * 7 * 4096 * 512 / 8e12 * 1e6)
+    assert fl["hbm_us"] == pytest.approx(bench.hbm_bytes(tk) / 6.8e12 * 1e6)
+    assert bench.gumbel_floor_us(tk, PEAKS, 152) > 0
+    assert bench.gumbel_floor_us(bench.MAIN, PEAKS, 152) is None
+
+
+def test_variants_cover_every_configuration():
+    names = {c["name"] for c in bench.VARIANTS} | {bench.MAIN["name"]}
+    assert len(names) == len(bench.VARIANTS) + 1
+    vs = [bench.MAIN] + bench.VARIANTS
+    assert any(c["V"] == 129280 and c["K"] == 5 and c["bs"] == 1 and not c["int8"] for c in vs)
+    assert {c["bs"] for c in vs if c["V"] == 151936 and c["K"] == 7 and c["int8"]} == {1, 16, 64}
+    assert {c["bs"] for c in vs if c["V"] == 151936 and c["K"] == 16 and c["logits"]} == {1, 64}
+    assert {c["bs"] for c in vs if c["V"] == 248320} == {1, 16, 64}
+    assert {c["top_k"] for c in vs if c["top_k"]} == {512, 4096}
 
 
 def test_reference_arm_prints_one_contract_line():

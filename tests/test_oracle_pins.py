@@ -424,6 +424,144 @@ def test_follow_classification(oracle):
     assert res.follow_class[0, 0] == oracle.CLASS_REJECTED
 
 
+# The bf16-boundary class: in probabilistic mode a GPU token that differs from the
+# oracle's is accepted when one logit lies within bf16_eps (1e-4, in logit units) of a
+# bf16 rounding midpoint and rounding it the other way makes the GPU token come within
+# tie_tol of the best score. The cases below are built exactly: V = 6, R = 4, the
+# embedding W1[0] = e_0, so the bias of entry v is its W2 entry x_v and the fp64 logit
+# is base_v + x_v (bf16 values summed exactly in fp64; x_v = a_v + b_v over two
+# embedding components where x_v itself needs more than 8 significant bits). The Gumbel noise g comes
+# from the separately pinned Philox generator. T = 0.5 makes logit units and score
+# units differ by a factor of 2, so a window applied in score units fails case A.
+_BF16_MID = 4.015625          # midpoint between the bf16 values 4.0 and 4.03125
+_STEP = 2.0 ** -14            # bf16 spacing of the W2 entries near 2^-6
+
+
+def _boundary_row(oracle, follow_logit_x, tok_logit, tok_x=0.0, follow_base=4.0, seed=None):
+    """Walk one probabilistic step over V = 6 and return (oracle token, follow class) of
+    the follow token 0, for the first seed whose noise admits the construction."""
+    V, R, T = 6, 4, 0.5
+    w1 = np.zeros((V, R), np.uint16)
+    w1[0] = bf16_bits([1.0, 1.0, 0, 0])
+    seeds = [seed] if seed is not None else range(200)
+    for sd in seeds:
+        _, _, g = oracle.gumbel_block(np.array([sd], np.uint64), 1, V)
+        g = g[0, 0]
+        base = np.full(V, -30.0)
+        base[0] = follow_base
+        b1 = tok_logit(g)  # the oracle's token (entry 1): a bf16 base value, or None
+        if b1 is None:
+            continue
+        base[1] = b1
+        xa, xb = np.zeros(V), np.zeros(V)  # x_v = xa_v + xb_v, each bf16-exact
+        xa[0], xb[0] = follow_logit_x if isinstance(follow_logit_x, tuple) else (follow_logit_x, 0.0)
+        xa[1], xb[1] = tok_x if isinstance(tok_x, tuple) else (tok_x, 0.0)
+        w2 = np.zeros((V, R), np.uint16)
+        w2[:, 0] = bf16_bits(xa)
+        w2[:, 1] = bf16_bits(xb)
+        assert np.array_equal(bf16_bits(xa).view(np.int16), torch.tensor(xa, dtype=torch.float64)
+                              .to(torch.bfloat16).view(torch.int16).numpy()), "bias parts must be bf16-exact"
+        res = oracle.walk(bf16_bits(base).reshape(1, 1, V), w1, np.array([0], np.int32), 1, w2_bits=w2,
+                          seeds=np.array([sd], np.uint64), mode=oracle.PROBABILISTIC, temperature=T,
+                          follow=np.array([[0]], np.int32), want_logits=True, want_scores=True)
+        return sd, res
+    raise AssertionError("no seed admits the construction")
+
+
+def _tok_for_up_case(g):
+    """bf16 base logit b1 of entry 1 with 2 b1 + g_1 between the follow token's score under
+    round-to-nearest (2 * 4.0 + g_0) and under the upward rounding (2 * 4.03125 + g_0),
+    each with a margin beyond tie_tol = 1e-3."""
+    lo, hi = 8.0 + g[0] + 0.004, 8.0625 + g[0] - 0.004
+    target = 0.5 * ((lo + hi) / 2 - g[1])
+    b1 = float(torch.tensor(target, dtype=torch.float32).to(torch.bfloat16).float())
+    s1 = 2 * b1 + g[1]
+    return b1 if lo < s1 < hi else None
+
+
+def test_bf16_boundary_class_upward_rounding(oracle):
+    """Case A: the follow token's logit lies 2^-14 (6.1e-5 < 1e-4) below the midpoint, so
+    rounding it up gives it the best score: CLASS_BF16_BOUNDARY. Case B: 2^-13 (1.2e-4)
+    below, outside the window: CLASS_REJECTED. Both with the oracle's token kept by
+    round-to-nearest (no near tie)."""
+    for x0, want in ((0.015625 - _STEP, oracle.CLASS_BF16_BOUNDARY),
+                     (0.015625 - 2 * _STEP, oracle.CLASS_REJECTED)):
+        sd, res = _boundary_row(oracle, x0, _tok_for_up_case)
+        assert res.status == 0
+        assert abs(res.logits[0, 0, 0] - _BF16_MID) in (_STEP, 2 * _STEP)
+        assert res.tokens[0, 0] == 1, (sd, res.tokens)
+        assert res.scores[0, 0, 1] - res.scores[0, 0, 0] > 1e-3  # not a near tie
+        assert res.follow_class[0, 0] == want, (x0, sd, res.follow_class)
+
+
+def test_bf16_boundary_class_downward_rounding(oracle):
+    """Case C: the oracle's token's logit lies 2^-14 ABOVE a midpoint (rounded up by
+    round-to-nearest); rounding it down instead lets the follow token (bf16-exact logit)
+    come within tie_tol: CLASS_BF16_BOUNDARY. The same token 2^-13 above: rejected."""
+    # entry 1's logit = 4.0 + 0.015625 + x1: bf16 4.03125 by round-to-nearest, 4.0 when
+    # rounded down; entry 0 (bf16-exact base b0, no bias) scores between the two.
+    for x1, want in ((_STEP, oracle.CLASS_BF16_BOUNDARY), (2 * _STEP, oracle.CLASS_REJECTED)):
+        V = 6
+        found = None
+        for sd in range(400):
+            _, _, g = oracle.gumbel_block(np.array([sd], np.uint64), 1, V)
+            g = g[0, 0]
+            lo, hi = 8.0 + g[1] - 1e-3 + 0.004, 8.0625 + g[1] - 1e-3 - 0.004  # s0 window
+            target = 0.5 * ((lo + hi) / 2 - g[0])
+            b0 = float(torch.tensor(target, dtype=torch.float32).to(torch.bfloat16).float())
+            if lo < 2 * b0 + g[0] < hi:
+                found = (sd, b0)
+                break
+        assert found is not None
+        sd, b0 = found
+        _, res = _boundary_row(oracle, 0.0, lambda g: 4.0, tok_x=(0.015625, x1), follow_base=b0, seed=sd)
+        assert res.status == 0
+        assert res.logits[0, 0, 1] - _BF16_MID == x1
+        assert res.tokens[0, 0] == 1, (sd, res.tokens)
+        assert res.scores[0, 0, 1] - res.scores[0, 0, 0] > 1e-3
+        assert res.follow_class[0, 0] == want, (x1, sd, res.follow_class)
+
+
+def _mutated_oracle(tmp_path, edits):
+    """A copy of the oracle with planted mistakes (each an (old, new) source edit), built
+    into tmp_path on the CPU and bound like the real one."""
+    import ctypes as C
+    from oracle import oracle as O
+    src = open(O.SRC).read()
+    for old, new in edits:
+        assert old in src
+        src = src.replace(old, new)
+    path = tmp_path / "mutant.cpp"
+    path.write_text(src)
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["g++", "-std=c++17", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC",
+                    "-shared", str(path), "-o", str(so)], check=True)
+    return O.bind(C.CDLL(str(so)))
+
+
+@pytest.mark.parametrize("edits", [
+    # the up / down choices of the alternative rounding swapped
+    [("const double pick = up ? std::max(lb, hi) : std::min(lb, lo);",
+      "const double pick = up ? std::min(lb, lo) : std::max(lb, hi);")],
+    # the window applied in score units (logit units times T) instead of logit units
+    [("const double lo = bf16_bits_to_double(round_to_bf16(l[v] - a->bf16_eps));",
+      "const double lo = bf16_bits_to_double(round_to_bf16(l[v] - a->bf16_eps * T));"),
+     ("const double hi = bf16_bits_to_double(round_to_bf16(l[v] + a->bf16_eps));",
+      "const double hi = bf16_bits_to_double(round_to_bf16(l[v] + a->bf16_eps * T));")],
+], ids=["up_down_swapped", "window_in_score_units"])
+def test_bf16_boundary_pins_catch_planted_mistakes(oracle, tmp_path, monkeypatch, edits):
+    """Each planted mistake in the bf16-boundary classification makes one of the pins
+    above fail."""
+    monkeypatch.setattr(oracle, "_lib", _mutated_oracle(tmp_path, edits))
+    failed = 0
+    for pin in (test_bf16_boundary_class_upward_rounding, test_bf16_boundary_class_downward_rounding):
+        try:
+            pin(oracle)
+        except AssertionError:
+            failed += 1
+    assert failed >= 1
+
+
 def test_prob_score_uses_bf16_logit(oracle):
     """The sampled score is bf16(l)/T + g: subtracting the (separately pinned) Gumbel
     noise and undoing T leaves exactly the bf16-rounded logit, not the fp64 one."""
