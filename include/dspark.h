@@ -164,10 +164,15 @@ int32_t dspark_walk_from_host(const dspark_walk_args* args, const uint16_t* base
                               dspark_stream_t stream);
 
 /* Bytes of scratch workspace a walk of this shape needs (argmax slots, barrier
- * counters, status words, top-k candidate lists). */
+ * counters, status words, top-k candidate lists). Part of the walk's C interface
+ * specified with dspark_walk (caller-owned workspace, no allocation in the library);
+ * the pages have no counterpart. Returns 0 for bs < 1, K < 1 or top_k < 0. */
 size_t dspark_walk_workspace_size(int64_t V, int32_t bs, int32_t K, int32_t top_k);
 
 /*
+ * Part of the walk's C interface specified with dspark_walk (the shared-memory capacity
+ * behind "most of W2 stays in shared memory", vLLM PR #62958, "Overview", queried at
+ * run time).
  * Launch plan dspark_walk takes by default on `device` for this batch size (CUDA-core
  * contraction at bs <= 2, tensor cores from bs = 3): cooperative grid size (CTAs) and
  * the number of W2 rows kept resident in shared memory over the whole grid (greedy
@@ -180,8 +185,11 @@ int32_t dspark_query_capacity(int32_t device, int64_t V, int32_t w2_is_int8, int
                               int32_t* grid_ctas, int64_t* resident_rows);
 
 /*
- * The Philox words and Gumbel values the walk draws, for checking: words uint32 and
- * gumbel fp32 [bs, K, V] (either may be NULL). Same generator code as the walk.
+ * TEST HOOK (not needed to use the walk): the Philox words and Gumbel values the walk
+ * draws, for checking them bit for bit against an independent implementation: words
+ * uint32 and gumbel fp32 [bs, K, V] (either may be NULL). Same generator code as the
+ * walk (vLLM PR #62958, "Details": Philox noise keyed by the request seed and the draft
+ * position). Returns DSPARK_ERR_INVALID_ARG for null seeds, bs < 1, K < 1 or V <= 0.
  */
 int32_t dspark_gumbel_noise(const uint64_t* seeds, int32_t bs, int32_t K, int64_t V,
                             uint32_t* words, float* gumbel, dspark_stream_t stream);
@@ -248,10 +256,13 @@ typedef struct dspark_verify_args {
 } dspark_verify_args;
 int32_t dspark_verify(const dspark_verify_args* args, dspark_stream_t stream);
 
-/* Human-readable name of a status code (static storage). */
+/* Human-readable name of a status code (static storage). Part of the C interface's
+ * error reporting; the pages have no counterpart. */
 const char* dspark_status_string(int32_t status);
 
-/* The last CUDA error string seen by this thread's calls into the library. */
+/* The last CUDA error string seen by this thread's calls into the library (for
+ * DSPARK_ERR_CUDA, and the reason of a DSPARK_ERR_UNSUPPORTED launch refusal). Part of
+ * the C interface's error reporting; the pages have no counterpart. */
 const char* dspark_last_cuda_error(void);
 
 #ifdef __cplusplus

@@ -23,7 +23,7 @@
 //   * Philox4x32-10: J. K. Salmon, M. A. Moraes, R. O. Dror, D. E. Shaw, "Parallel
 //     Random Numbers: As Easy as 1, 2, 3", SC'11.
 //
-// Readings where the pages are silent (each is listed in the design notes):
+// Readings where the pages are silent:
 //   * quantizer: scale = max|w| / 127 in fp32; q = round-half-even(w / scale) in fp32,
 //     clamped to [-127, 127]; an all-zero row has scale 0 and q = 0.
 //   * the probabilistic score is bf16(l) / T + g with g = -log(-log(u)); greedy uses l.
@@ -203,6 +203,8 @@ struct oracle_walk_args {
   uint16_t* logits_bf16;     // [bs, K, V] bf16(l)
   double* scores;            // [bs, K, V] scores the argmax ran over
   int32_t* cand;             // [bs, K, top_k] candidates in ascending vocabulary order
+  const double* base_f64;    // optional [bs, K, V] base logits in fp64 (unrounded), used
+                             // instead of `base` when given (the drafter's LM-head output)
 };
 
 double oracle_bf16_to_double(uint16_t h) { return bf16_bits_to_double(h); }
@@ -262,6 +264,45 @@ int32_t oracle_quantize_w2(const uint16_t* w2, int64_t V, int32_t R, int8_t* q, 
   return status;
 }
 
+// Top-k candidate set of one fp64 row (the same order: NaN first, then larger value,
+// then smaller index), ascending vocabulary order.
+void topk_select_f64(const double* row, int64_t V, int32_t k, int32_t* cand) {
+  std::vector<int64_t> order(V);
+  for (int64_t v = 0; v < V; ++v) order[v] = v;
+  std::partial_sort(order.begin(), order.begin() + k, order.end(),
+                    [&](int64_t a, int64_t b) { return topk_before(row[a], a, row[b], b); });
+  std::vector<int64_t> chosen(order.begin(), order.begin() + k);
+  std::sort(chosen.begin(), chosen.end());
+  for (int32_t j = 0; j < k; ++j) cand[j] = static_cast<int32_t>(chosen[j]);
+}
+
+// The drafter's LM head (vLLM PR #49969, "Purpose": the base logits of every draft
+// position come from the dense LM-head output): logits[m, v] = sum_k hidden[m, k] *
+// lm_head[v, k] in fp64, sequential k order, unrounded.
+int32_t oracle_lmhead_logits(const uint16_t* hidden, const uint16_t* lm_head, int32_t M, int32_t d,
+                             int64_t V, double* out, int32_t nthreads) {
+  if (!hidden || !lm_head || !out || M <= 0 || d <= 0 || V <= 0) return ORACLE_INVALID_ARG;
+#ifdef _OPENMP
+  const int nt = nthreads > 0 ? nthreads : 1;
+#else
+  (void)nthreads;
+#endif
+  for (int32_t m = 0; m < M; ++m) {
+    std::vector<double> h(d);
+    for (int32_t k = 0; k < d; ++k) h[k] = bf16_bits_to_double(hidden[static_cast<int64_t>(m) * d + k]);
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(nt) schedule(static)
+#endif
+    for (int64_t v = 0; v < V; ++v) {
+      const uint16_t* w = lm_head + v * d;
+      double acc = 0.0;
+      for (int32_t k = 0; k < d; ++k) acc += h[k] * bf16_bits_to_double(w[k]);
+      out[static_cast<int64_t>(m) * V + v] = acc;
+    }
+  }
+  return ORACLE_OK;
+}
+
 // Top-k candidate set of every (b, i) row of the base logits, ascending vocab order.
 int32_t oracle_topk_select(const uint16_t* base, int32_t rows, int64_t V, int32_t k,
                            int32_t* cand) {
@@ -284,7 +325,7 @@ int32_t oracle_topk_select(const uint16_t* base, int32_t rows, int64_t V, int32_
 
 // The K-step walk of every row, in the order the method defines it.
 int32_t oracle_walk(const oracle_walk_args* a) {
-  if (!a || !a->base || !a->w1 || !a->prev || !a->tokens) return ORACLE_INVALID_ARG;
+  if (!a || (!a->base && !a->base_f64) || !a->w1 || !a->prev || !a->tokens) return ORACLE_INVALID_ARG;
   if (a->V <= 0 || a->R <= 0 || a->bs <= 0 || a->K <= 0) return ORACLE_INVALID_ARG;
   if (a->mode != 0 && a->mode != 1) return ORACLE_INVALID_ARG;
   const bool int8_w2 = a->w2 == nullptr;
@@ -321,14 +362,17 @@ int32_t oracle_walk(const oracle_walk_args* a) {
     }
     for (int32_t i = 0; i < K; ++i) {
       const int64_t ri = static_cast<int64_t>(row) * K + i;
-      const uint16_t* base_row = a->base + ri * V;
+      const uint16_t* base_row = a->base ? a->base + ri * V : nullptr;
+      const double* base_row64 = a->base_f64 ? a->base_f64 + ri * V : nullptr;
+      auto base_at = [&](int64_t v) { return base_row64 ? base_row64[v] : bf16_bits_to_double(base_row[v]); };
 
       // The Markov embedding of the previous token.
       for (int32_t k = 0; k < R; ++k) e[k] = bf16_bits_to_double(a->w1[prev * R + k]);
 
       // Top-k: candidates chosen once per position from the unbiased base logits.
       if (a->top_k > 0) {
-        oracle_topk_select(base_row, 1, V, a->top_k, cand_row.data());
+        if (base_row64) topk_select_f64(base_row64, V, a->top_k, cand_row.data());
+        else oracle_topk_select(base_row, 1, V, a->top_k, cand_row.data());
         is_cand.assign(V, 0);
         for (int32_t j = 0; j < a->top_k; ++j) is_cand[cand_row[j]] = 1;
         if (a->cand)
@@ -354,7 +398,7 @@ int32_t oracle_walk(const oracle_walk_args* a) {
             const uint16_t* wrow = a->w2 + v * R;
             for (int32_t k = 0; k < R; ++k) bias += bf16_bits_to_double(wrow[k]) * e[k];
           }
-          lv = bf16_bits_to_double(base_row[v]) + bias;
+          lv = base_at(v) + bias;
         }
         l[v] = lv;
         if (a->mode == 0) {

@@ -45,7 +45,7 @@ class _WalkArgs(C.Structure):
         ("nthreads", C.c_int32),
         ("tokens", C.c_void_p), ("gap", C.c_void_p), ("best_score", C.c_void_p),
         ("follow_class", C.c_void_p), ("logits", C.c_void_p), ("logits_bf16", C.c_void_p),
-        ("scores", C.c_void_p), ("cand", C.c_void_p),
+        ("scores", C.c_void_p), ("cand", C.c_void_p), ("base_f64", C.c_void_p),
     ]
 
 
@@ -72,6 +72,9 @@ def bind(L):
                                      C.c_void_p]
     L.oracle_walk.restype = C.c_int32
     L.oracle_walk.argtypes = [C.POINTER(_WalkArgs)]
+    L.oracle_lmhead_logits.restype = C.c_int32
+    L.oracle_lmhead_logits.argtypes = [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int64,
+                                       C.c_void_p, C.c_int32]
     return L
 
 
@@ -152,12 +155,28 @@ class WalkResult:
     cand: np.ndarray | None
 
 
+def lmhead_logits(hidden_bits, lm_head_bits, nthreads: int = 1) -> np.ndarray:
+    """fp64 LM-head logits [M, V] of bf16 hidden states [M, d] and LM head [V, d]."""
+    h = _c(hidden_bits, np.uint16)
+    w = _c(lm_head_bits, np.uint16)
+    M, d = h.shape
+    V = w.shape[0]
+    assert w.shape[1] == d
+    out = np.zeros((M, V), dtype=np.float64)
+    st = lib().oracle_lmhead_logits(_ptr(h), _ptr(w), M, d, V, _ptr(out), nthreads)
+    assert st == 0, st
+    return out
+
+
 def walk(base_bits, w1_bits, prev, K: int, *, w2_bits=None, w2q=None, scales=None, seeds=None,
          slot=None, mode: int = GREEDY, temperature: float = 1.0, top_k: int = 0, follow=None,
          tie_tol: float = 1e-3, bf16_eps: float = 1e-4, nthreads: int = 1,
          want_logits: bool = False, want_logits_bf16: bool = False, want_scores: bool = False,
-         want_cand: bool = False) -> WalkResult:
-    base = _c(base_bits, np.uint16)
+         want_cand: bool = False, base_f64=None) -> WalkResult:
+    """base_bits: bf16 [bs, K, V] base logits, or None with base_f64: fp64 [bs, K, V]
+    unrounded base logits (the LM-head output)."""
+    b64 = _c(base_f64, np.float64)
+    base = _c(base_bits, np.uint16) if base_bits is not None else None
     w1 = _c(w1_bits, np.uint16)
     w2 = _c(w2_bits, np.uint16)
     q = _c(w2q, np.int8)
@@ -167,9 +186,9 @@ def walk(base_bits, w1_bits, prev, K: int, *, w2_bits=None, w2q=None, scales=Non
     sl = _c(slot, np.int32)
     fo = _c(follow, np.int32)
     bs = pv.shape[0]
-    V = base.shape[-1]
+    V = (base if base is not None else b64).shape[-1]
     R = w1.shape[1]
-    assert base.shape == (bs, K, V), (base.shape, bs, K, V)
+    assert (base if base is not None else b64).shape == (bs, K, V), (bs, K, V)
     tokens = np.zeros((bs, K), dtype=np.int32)
     gap = np.zeros((bs, K), dtype=np.float64)
     best = np.zeros((bs, K), dtype=np.float64)
@@ -182,7 +201,7 @@ def walk(base_bits, w1_bits, prev, K: int, *, w2_bits=None, w2q=None, scales=Non
         _ptr(base), _ptr(w1), _ptr(w2), _ptr(q), _ptr(sc), _ptr(pv), _ptr(sd), _ptr(sl),
         V, R, bs, K, mode, temperature, top_k, _ptr(fo), tie_tol, bf16_eps, nthreads,
         _ptr(tokens), _ptr(gap), _ptr(best), _ptr(fcls), _ptr(logits), _ptr(lbf), _ptr(scores),
-        _ptr(cand))
+        _ptr(cand), _ptr(b64))
     st = lib().oracle_walk(C.byref(args))
     return WalkResult(int(st), tokens, gap, best, fcls, logits, lbf, scores, cand)
 

@@ -578,3 +578,49 @@ def test_prob_score_uses_bf16_logit(oracle):
     np.testing.assert_allclose((res.scores - g) * np.float64(np.float32(T)), lb, rtol=0, atol=1e-12)
     # and that rounding did change some logits (the inputs are not bf16-exact)
     assert np.mean(lb != res.logits) > 0.9
+
+
+# ---------------------------------------------------------------- the drafter's LM head
+
+def test_lmhead_logits_exact_on_integer_inputs(oracle):
+    """Small-integer hidden states and LM-head weights: every product and sum is exact,
+    so the fp64 logits equal the integer matrix product (numpy int64)."""
+    g = np.random.default_rng(9)
+    M, d, V = 5, 96, 301
+    h = g.integers(-6, 7, size=(M, d))
+    w = g.integers(-9, 10, size=(V, d))
+    out = oracle.lmhead_logits(bf16_bits(h.ravel()).reshape(M, d), bf16_bits(w.ravel()).reshape(V, d))
+    np.testing.assert_array_equal(out, (h.astype(np.int64) @ w.T.astype(np.int64)).astype(np.float64))
+
+
+def test_lmhead_one_hot_hidden_selects_a_column(oracle):
+    """A one-hot hidden state e_j gives, for every vocabulary entry, the LM head's entry
+    in column j (bf16 values, exact)."""
+    g = np.random.default_rng(10)
+    d, V = 64, 257
+    w = bf16_bits(g.normal(0, 1, V * d)).reshape(V, d)
+    for j in (0, 17, 63):
+        h = np.zeros((1, d), np.uint16)
+        h[0, j] = bf16_bits([1.0])[0]
+        out = oracle.lmhead_logits(h, w)
+        col = torch.from_numpy(w[:, j].view(np.int16)).view(torch.bfloat16).double().numpy()
+        np.testing.assert_array_equal(out[0], col)
+
+
+def test_walk_on_fp64_base_equals_walk_on_the_same_bf16_values(oracle):
+    """The walk fed unrounded fp64 base logits that happen to be bf16 values behaves like
+    the walk fed those bf16 values (dense and top-k)."""
+    V, R, K, bs = 120, 8, 3, 2
+    g = torch.Generator().manual_seed(11)
+    base = (torch.randn(bs, K, V, generator=g) * 3).to(torch.bfloat16)
+    w1 = torch.randn(V, R, generator=g).to(torch.bfloat16)
+    w2 = (torch.randn(V, R, generator=g) / 3).to(torch.bfloat16)
+    bb = base.view(torch.int16).numpy().view(np.uint16)
+    kw = dict(w2_bits=w2.view(torch.int16).numpy().view(np.uint16), seeds=np.array([3, 4], np.uint64),
+              mode=oracle.PROBABILISTIC, temperature=0.8, want_logits=True)
+    w1b = w1.view(torch.int16).numpy().view(np.uint16)
+    for top_k in (0, 7):
+        a = oracle.walk(bb, w1b, np.array([5, 9], np.int32), K, top_k=top_k, **kw)
+        b = oracle.walk(None, w1b, np.array([5, 9], np.int32), K, top_k=top_k, base_f64=base.double().numpy(), **kw)
+        np.testing.assert_array_equal(a.tokens, b.tokens)
+        np.testing.assert_array_equal(a.logits, b.logits)
