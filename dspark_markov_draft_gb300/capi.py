@@ -45,7 +45,20 @@ class WalkArgs(C.Structure):
         ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t),
         ("status_dev", C.c_void_p), ("flags", C.c_uint32), ("resident_rows_cap", C.c_int32),
         ("timeout_us", C.c_uint32), ("temperatures", C.c_void_p), ("row_modes", C.c_void_p),
+        ("topk_cand", C.c_void_p), ("topk_base", C.c_void_p),
     ]
+
+
+class LmheadArgs(C.Structure):
+    _fields_ = [
+        ("hidden", C.c_void_p), ("lm_head", C.c_void_p), ("V", C.c_int64), ("M", C.c_int32),
+        ("d", C.c_int32), ("top_k", C.c_int32), ("cand", C.c_void_p), ("cand_base", C.c_void_p),
+        ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t), ("status_dev", C.c_void_p),
+        ("stats_dev", C.c_void_p), ("flags", C.c_uint32), ("timeout_us", C.c_uint32),
+    ]
+
+
+LMHEAD_FLAG_EXACT = 0x1
 
 
 class VerifyArgs(C.Structure):
@@ -79,13 +92,16 @@ def lib():
                                             C.POINTER(C.c_int64)]
         L.dspark_gumbel_noise.argtypes = [vp, i32, i32, i64, vp, vp, vp]
         L.dspark_verify.argtypes = [C.POINTER(VerifyArgs), vp]
+        L.dspark_lmhead_topk.argtypes = [C.POINTER(LmheadArgs), vp]
+        L.dspark_lmhead_workspace_size.argtypes = [i32, i64, i32]
+        L.dspark_lmhead_workspace_size.restype = C.c_size_t
         L.dspark_status_string.argtypes = [i32]
         L.dspark_status_string.restype = C.c_char_p
         L.dspark_last_cuda_error.argtypes = []
         L.dspark_last_cuda_error.restype = C.c_char_p
         for f in ("dspark_quantize_w2", "dspark_walk", "dspark_walk_topk", "dspark_walk_noalloc",
                   "dspark_walk_from_host", "dspark_query_capacity", "dspark_gumbel_noise",
-                  "dspark_verify"):
+                  "dspark_verify", "dspark_lmhead_topk"):
             getattr(L, f).restype = C.c_int32
         _lib = L
     return _lib
@@ -163,25 +179,42 @@ def quantize_w2(w2: torch.Tensor, q: torch.Tensor | None = None, scales: torch.T
 
 def make_args(base, w1, prev, tokens, workspace, *, w2=None, w2q=None, scales=None, seeds=None,
               mode=GREEDY, temperature=1.0, top_k=0, logits=None, status=None, flags=0,
-              resident_rows_cap=-1, timeout_us=0, temperatures=None, row_modes=None) -> WalkArgs:
+              resident_rows_cap=-1, timeout_us=0, temperatures=None, row_modes=None,
+              topk_cand=None, topk_base=None, V=None) -> WalkArgs:
     """temperatures (fp32 [bs]) and row_modes (int32 [bs]), device tensors, override the
-    scalar temperature and mode row by row."""
-    bs, K, V = base.shape
+    scalar temperature and mode row by row. topk_cand (int32 [bs, K, top_k]) and
+    topk_base (fp32, same shape): candidates chosen elsewhere (base may then be None,
+    with V given)."""
+    if base is not None:
+        bs, K, V = base.shape
+    else:
+        bs, K = tokens.shape
+        if V is None or topk_cand is None:
+            raise ValueError("without base logits: topk_cand, topk_base and V are required")
+    for t, name, dt in ((topk_cand, "topk_cand", torch.int32), (topk_base, "topk_base", torch.float32)):
+        if t is not None:
+            _expect(t, (bs, K, top_k), (dt,), name, tokens.device)
     wsp, wsn = _ws_view(workspace)
     return WalkArgs(
         _dev_ptr(base), _dev_ptr(w1), _dev_ptr(w2), _dev_ptr(w2q), _dev_ptr(scales),
         _dev_ptr(prev), _dev_ptr(seeds), V, w1.shape[1], bs, K, mode, temperature, top_k,
         _dev_ptr(tokens), _dev_ptr(logits), wsp, wsn, _dev_ptr(status), flags,
-        resident_rows_cap, timeout_us, _dev_ptr(temperatures), _dev_ptr(row_modes))
+        resident_rows_cap, timeout_us, _dev_ptr(temperatures), _dev_ptr(row_modes),
+        _dev_ptr(topk_cand), _dev_ptr(topk_base))
 
 
 def walk(base, w1, prev, *, w2=None, w2q=None, scales=None, seeds=None, mode=GREEDY,
          temperature=1.0, top_k=0, tokens=None, logits=None, want_logits=False, workspace=None,
          status=None, flags=0, resident_rows_cap=-1, timeout_us=0, stream=None,
-         temperatures=None, row_modes=None):
-    """Run dspark_walk (or dspark_walk_topk when top_k > 0). Returns (tokens, logits)."""
-    bs, K, V = base.shape
-    dev = base.device
+         temperatures=None, row_modes=None, topk_cand=None, topk_base=None, V=None):
+    """Run dspark_walk (or dspark_walk_topk when top_k > 0). Returns (tokens, logits).
+    With topk_cand / topk_base (e.g. from lmhead_topk) base may be None and V given."""
+    if base is not None:
+        bs, K, V = base.shape
+        dev = base.device
+    else:
+        bs, K = topk_cand.shape[:2]
+        dev = topk_cand.device
     if tokens is None:
         tokens = torch.empty((bs, K), dtype=torch.int32, device=dev)
     if want_logits and logits is None:
@@ -191,9 +224,42 @@ def walk(base, w1, prev, *, w2=None, w2q=None, scales=None, seeds=None, mode=GRE
     a = make_args(base, w1, prev, tokens, workspace, w2=w2, w2q=w2q, scales=scales,
                   seeds=seeds, mode=mode, temperature=temperature, top_k=top_k, logits=logits,
                   status=status, flags=flags, resident_rows_cap=resident_rows_cap,
-                  timeout_us=timeout_us, temperatures=temperatures, row_modes=row_modes)
+                  timeout_us=timeout_us, temperatures=temperatures, row_modes=row_modes,
+                  topk_cand=topk_cand, topk_base=topk_base, V=V)
     _check(lib().dspark_walk(C.byref(a), _stream(stream)), "dspark_walk")
     return tokens, logits
+
+
+def lmhead_workspace(M: int, V: int, top_k: int, device=None) -> torch.Tensor:
+    n = int(lib().dspark_lmhead_workspace_size(M, V, top_k))
+    if n == 0:
+        raise ValueError("invalid sizes for dspark_lmhead_workspace_size")
+    return torch.empty(n + 256, dtype=torch.uint8, device=device or "cuda")
+
+
+def lmhead_topk(hidden, lm_head, top_k: int, *, cand=None, cand_base=None, workspace=None, status=None,
+                stats=None, exact=False, timeout_us=0, stream=None):
+    """dspark_lmhead_topk: the top_k largest LM-head logits of every hidden row without the
+    dense logits. hidden bf16 [M, d], lm_head bf16 [V, d]. Returns (cand int32 [M, top_k],
+    cand_base fp32 [M, top_k])."""
+    M, d = hidden.shape
+    V = lm_head.shape[0]
+    dev = hidden.device
+    _expect(hidden, (M, d), (torch.bfloat16,), "hidden", dev)
+    _expect(lm_head, (V, d), (torch.bfloat16,), "lm_head", dev)
+    if cand is None:
+        cand = torch.empty((M, top_k), dtype=torch.int32, device=dev)
+    if cand_base is None:
+        cand_base = torch.empty((M, top_k), dtype=torch.float32, device=dev)
+    _expect(cand, (M, top_k), (torch.int32,), "cand", dev)
+    _expect(cand_base, (M, top_k), (torch.float32,), "cand_base", dev)
+    if workspace is None:
+        workspace = lmhead_workspace(M, V, top_k, device=dev)
+    wsp, wsn = _ws_view(workspace)
+    a = LmheadArgs(_dev_ptr(hidden), _dev_ptr(lm_head), V, M, d, top_k, _dev_ptr(cand), _dev_ptr(cand_base),
+                   wsp, wsn, _dev_ptr(status), _dev_ptr(stats), LMHEAD_FLAG_EXACT if exact else 0, timeout_us)
+    _check(lib().dspark_lmhead_topk(C.byref(a), _stream(stream)), "dspark_lmhead_topk")
+    return cand, cand_base
 
 
 def walk_args_call(args: WalkArgs, stream=None, topk: bool = False) -> int:

@@ -9,6 +9,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "lmhead.cuh"
 #include "walk_params.cuh"
 
 namespace dspark {
@@ -26,11 +27,16 @@ cudaError_t launch_quantize_w2(const uint16_t* w2, int64_t V, int8_t* q, float* 
                                int32_t* status_dev, cudaStream_t stream);
 cudaError_t launch_gumbel_noise(const uint64_t* seeds, int bs, int K, int64_t V, uint32_t* words,
                                 float* gumbel, cudaStream_t stream);
+cudaError_t launch_lmhead(LmParams& p, int sms, int pivot_rank, cudaStream_t stream);
+cudaError_t launch_fill_neg_inf(uint16_t* x, size_t n, cudaStream_t stream);
 
 // Checks of a walk's arguments other than its workspace, made before any CUDA call.
 int32_t check_walk_inputs(const dspark_walk_args* a) {
   if (!a) return DSPARK_ERR_INVALID_ARG;
-  if (!a->base_logits || !a->w1 || !a->prev_tokens || !a->draft_tokens) return DSPARK_ERR_INVALID_ARG;
+  // candidates given by the caller: both arrays, a top-k walk; base_logits not read then
+  const bool given = a->topk_cand != nullptr || a->topk_base != nullptr;
+  if (given && (!a->topk_cand || !a->topk_base || a->top_k < 1)) return DSPARK_ERR_INVALID_ARG;
+  if ((!a->base_logits && !given) || !a->w1 || !a->prev_tokens || !a->draft_tokens) return DSPARK_ERR_INVALID_ARG;
   if (a->rank != DSPARK_RANK) return DSPARK_ERR_INVALID_ARG;
   if (a->V <= 0 || a->V > DSPARK_MAX_V) return DSPARK_ERR_INVALID_ARG;
   if (a->bs < 1 || a->bs > DSPARK_MAX_BS || a->K < 1 || a->K > DSPARK_MAX_K) return DSPARK_ERR_INVALID_ARG;
@@ -418,9 +424,18 @@ int32_t dspark_walk_topk(const dspark_walk_args* a, dspark_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int rows = a->bs * a->K;
   WalkParams p = make_params(a, caps.sms, 0, 0);
-  cudaError_t e = launch_topk_select(a->base_logits, a->V, a->top_k, rows,
-                                     const_cast<int32_t*>(p.cand), a->draft_logits, s);
-  if (e != cudaSuccess) return cuda_fail(e, "topk_select_kernel launch");
+  if (a->topk_cand) {  // candidates and their base logits from the caller
+    p.cand = a->topk_cand;
+    p.cand_base = a->topk_base;
+    if (a->draft_logits) {
+      const cudaError_t e = launch_fill_neg_inf(a->draft_logits, static_cast<size_t>(rows) * a->V, s);
+      if (e != cudaSuccess) return cuda_fail(e, "fill_neg_inf_kernel launch");
+    }
+  } else {
+    const cudaError_t e = launch_topk_select(a->base_logits, a->V, a->top_k, rows,
+                                             const_cast<int32_t*>(p.cand), a->draft_logits, s);
+    if (e != cudaSuccess) return cuda_fail(e, "topk_select_kernel launch");
+  }
   const size_t smem = topk_walk_smem(a->bs);
   const bool prob = a->mode == DSPARK_PROBABILISTIC || a->row_modes, lg = a->draft_logits != nullptr;
   const void* fn = topk_walk_kernel_ptr(a->w2q != nullptr, prob, lg);
@@ -464,6 +479,69 @@ int32_t dspark_walk(const dspark_walk_args* a, dspark_stream_t stream) {
   WalkParams p = make_params(a, pl.grid, pl.resident_rows, pl.slice_cap);
   const void* fn = walk_cc_kernel_ptr(int8, prob, lg);
   return launch_coop(fn, pl.grid, kWalkThreads, pl.smem, p, reinterpret_cast<cudaStream_t>(stream), caps, true);
+}
+
+size_t dspark_lmhead_workspace_size(int32_t M, int64_t V, int32_t top_k) {
+  if (M < 1 || V < 1 || top_k < 1) return 0;
+  return lm_ws_total(M, V, top_k);
+}
+
+int32_t dspark_lmhead_topk(const dspark_lmhead_args* a, dspark_stream_t stream) {
+  if (!a || !a->hidden || !a->lm_head || !a->cand || !a->cand_base) return DSPARK_ERR_INVALID_ARG;
+  if (a->M < 1 || a->V < 1 || a->V > DSPARK_MAX_V || a->d < 64 || a->d > 16384 || (a->d % 64) != 0)
+    return DSPARK_ERR_INVALID_ARG;
+  if (a->top_k < 1 || a->top_k > a->V || a->top_k > 8192) return DSPARK_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(a->hidden) | reinterpret_cast<uintptr_t>(a->lm_head)) & 15u)
+    return DSPARK_ERR_INVALID_ARG;
+  if (!a->workspace || (reinterpret_cast<uintptr_t>(a->workspace) & 255u) ||
+      a->workspace_bytes < lm_ws_total(a->M, a->V, a->top_k))
+    return DSPARK_ERR_WORKSPACE;
+  DeviceCaps caps;
+  int32_t st;
+  if ((st = current_caps(&caps)) != DSPARK_OK) return st;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return DSPARK_ERR_UNSUPPORTED;
+  LmParams p{};
+  p.hidden = a->hidden;
+  p.lm_head = a->lm_head;
+  p.V = a->V;
+  p.M = a->M;
+  p.d = a->d;
+  p.k = a->top_k;
+  p.S = lm_samples(a->V);
+  p.cap = lm_cap(a->top_k);
+  char* ws = static_cast<char*>(a->workspace);
+  p.sample = reinterpret_cast<float*>(ws);
+  p.pivot = reinterpret_cast<uint32_t*>(ws + lm_ws_sample(a->M, a->V));
+  p.cnt = reinterpret_cast<uint32_t*>(ws + lm_ws_sample(a->M, a->V) + lm_align(4ull * a->M));
+  p.list = reinterpret_cast<uint64_t*>(ws + lm_ws_sample(a->M, a->V) + 2 * lm_align(4ull * a->M));
+  p.cand = a->cand;
+  p.cand_base = a->cand_base;
+  p.stats = a->stats_dev;
+  p.status_dev = a->status_dev;
+  p.flags = (a->flags & DSPARK_LMHEAD_FLAG_EXACT) ? kLmForceExact : 0;
+  p.timeout_ns = 1000ull * (a->timeout_us ? a->timeout_us : 1000000u);
+  auto map2d = [&](CUtensorMap* m, const void* ptr, cuuint64_t inner, cuuint64_t rows, cuuint64_t stride_bytes,
+                   cuuint32_t box_rows) {
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {stride_bytes};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t elem[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, elem,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  const cuuint64_t d = static_cast<cuuint64_t>(a->d);
+  if (!map2d(&p.w_map, a->lm_head, d, static_cast<cuuint64_t>(a->V), 2 * d, 128) ||
+      !map2d(&p.ws_map, a->lm_head, d, static_cast<cuuint64_t>(p.S), 2 * d * kLmSampleStride, 128) ||
+      !map2d(&p.h_map, a->hidden, d, static_cast<cuuint64_t>(a->M), 2 * d, 256))
+    return DSPARK_ERR_UNSUPPORTED;
+  // pivot rank: about 1.5 k times the sampling fraction, plus a margin
+  const double frac = static_cast<double>(p.S) / static_cast<double>(a->V);
+  int rank = static_cast<int>(1.5 * a->top_k * frac) + 32;
+  if (rank > p.S) rank = p.S;
+  const cudaError_t e = launch_lmhead(p, caps.sms, rank, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSPARK_OK : cuda_fail(e, "lmhead kernels launch");
 }
 
 int32_t dspark_verify(const dspark_verify_args* a, dspark_stream_t stream) {

@@ -438,7 +438,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
       const int64_t v = min(max(static_cast<int64_t>(p.cand[(static_cast<size_t>(b) * p.K + i) * p.top_k + j]),
                                 int64_t{0}), p.V - 1);
       it_v[e] = static_cast<int32_t>(v);
-      it_base[e] = bf16_to_f32(__ldg(p.base + (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v));
+      it_base[e] = p.cand_base ? __ldg(p.cand_base + (static_cast<size_t>(b) * p.K + i) * p.top_k + j)
+                               : bf16_to_f32(__ldg(p.base + (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v));
       float g = 0.f;
       if (row_sampled(p, PROB, b)) {
         const uint4 w = philox_block(p.seeds[b], b, i, static_cast<uint32_t>(v >> 2));

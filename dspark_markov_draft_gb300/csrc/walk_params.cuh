@@ -19,6 +19,7 @@ struct WalkParams {
   int32_t* tokens;           // [bs, K]
   uint16_t* logits;          // [bs, K, V] bf16 or null
   const int32_t* cand;       // top-k candidates [bs, K, top_k] (top-k walk)
+  const float* cand_base;    // their base logits [bs, K, top_k] fp32, or null (read from base)
   int64_t V;
   int32_t bs, K, top_k;
   float temperature;

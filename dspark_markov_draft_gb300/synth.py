@@ -103,3 +103,13 @@ WORKLOADS = {
     "v151936_k7_topk": dict(V=151936, K=7, bs=(64,), w2="bf16", mode="prob", T=1.0,
                             top_k=(512, 4096), peak=None, draft_logits=False),
 }
+
+
+def lmhead(M: int, d: int, V: int, seed: int = 0, std: float = 3.0):
+    """Synthetic drafter LM head: hidden states [M, d] ~ N(0, 1) and LM-head rows [V, d]
+    ~ N(0, std^2 / d), both bf16, so that the logits are about N(0, std^2) like the base
+    logits of the walk's workloads."""
+    g = torch.Generator().manual_seed(seed)
+    hidden = torch.randn(M, d, generator=g).to(torch.bfloat16)
+    head = (torch.randn(V, d, generator=g) * (std / d ** 0.5)).to(torch.bfloat16)
+    return hidden, head

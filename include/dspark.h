@@ -111,6 +111,12 @@ typedef struct dspark_walk_args {
   const int32_t* row_modes;  /* int32 [bs]: row b's dspark_mode, overriding `mode` (then
                                 `seeds` is required); a value other than 0 / 1 is
                                 reported like an invalid temperature */
+  /* Top-k walk on candidates chosen elsewhere (both optional, device memory, given
+     together, top_k > 0): the candidates of every (b, i) and their base logits, e.g. from
+     dspark_lmhead_topk. The walk then skips its own selection and base_logits may be
+     NULL. */
+  const int32_t* topk_cand;  /* int32 [bs, K, top_k] vocabulary ids in [0, V), any order */
+  const float* topk_base;    /* fp32 [bs, K, top_k] their base logits */
 } dspark_walk_args;
 
 /*
@@ -149,6 +155,47 @@ int32_t dspark_walk(const dspark_walk_args* args, dspark_stream_t stream);
  * product with the embedding).
  */
 int32_t dspark_walk_topk(const dspark_walk_args* args, dspark_stream_t stream);
+
+/*
+ * The drafter's LM head fused with the top-k selection (vLLM PR #49969, "Purpose": the
+ * base logits of all draft positions come from the dense LM-head output, and the top-k
+ * candidates are selected from them once, before the sequential walk). For every hidden
+ * row m (the (b, i) positions of a draft block, row m = b K + i) it finds the top_k
+ * largest logits hidden[m] . lm_head[v] over v in [0, V) -- order: NaN largest, then
+ * larger value, then smaller index -- without writing the dense [M, V] logits: a GEMM
+ * over a sample of the LM-head rows sets a conservative per-row pivot, a second GEMM
+ * keeps only the logits at or above it, and an exact per-row selection finishes (rows
+ * the pivot did not serve take an exact path over the whole row). Logits are fp32 dot
+ * products of bf16 inputs accumulated in fp32 on the tensor cores.
+ *   hidden bf16 [M, d]; lm_head bf16 [V, d] (d a multiple of 64, 64..16384, both
+ *   16-byte aligned); out: cand int32 [M, top_k] (any order), cand_base fp32 [M, top_k];
+ *   workspace >= dspark_lmhead_workspace_size(M, V, top_k), 256-byte aligned (needs no
+ *   zeroing); stats_dev optional int32 [2]: rows that took the exact path, rows whose
+ *   candidate list overflowed (both counted, never reset).
+ * Returns DSPARK_ERR_INVALID_ARG for null pointers, M < 1, V < 1, a bad d, top_k outside
+ * 1..min(V, 8192) or misaligned tensors; DSPARK_ERR_WORKSPACE for a missing or small
+ * workspace; DSPARK_ERR_CUDA if a launch fails. Device timeouts go to status_dev.
+ */
+typedef struct dspark_lmhead_args {
+  const uint16_t* hidden;
+  const uint16_t* lm_head;
+  int64_t V;
+  int32_t M;
+  int32_t d;
+  int32_t top_k;
+  int32_t* cand;
+  float* cand_base;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* status_dev;  /* optional device int32 */
+  int32_t* stats_dev;   /* optional device int32 [2] */
+  uint32_t flags;       /* DSPARK_LMHEAD_FLAG_EXACT: every row takes the exact path */
+  uint32_t timeout_us;  /* limit of every device-side wait; 0 = 1,000,000 us */
+} dspark_lmhead_args;
+#define DSPARK_LMHEAD_FLAG_EXACT 0x1u
+int32_t dspark_lmhead_topk(const dspark_lmhead_args* args, dspark_stream_t stream);
+/* Workspace bytes of dspark_lmhead_topk (0 for invalid sizes). */
+size_t dspark_lmhead_workspace_size(int32_t M, int64_t V, int32_t top_k);
 
 /*
  * End-to-end variant for callers whose per-call inputs live in host memory: copies

@@ -49,14 +49,21 @@ def nthreads() -> int:
 
 def check_walk(O, inp, gpu_tokens: torch.Tensor, *, mode: int, T: float = 1.0, top_k: int = 0,
                q=None, sc=None, gpu_logits: torch.Tensor | None = None, rows=None,
-               base_bits=None, label: str | None = "small and special cases") -> ParityStats:
-    """Validate GPU tokens (and optional bf16 logits) of the rows `rows` (default all)."""
+               base_bits=None, label: str | None = "small and special cases",
+               base_f64_all=None) -> ParityStats:
+    """Validate GPU tokens (and optional bf16 logits) of the rows `rows` (default all).
+    base_f64_all: fp64 [bs, K, V] base logits for the oracle (the LM-head output) instead
+    of the bf16 base logits of `inp`."""
     toks = gpu_tokens.detach().cpu().numpy().astype(np.int32)
     bs, K = toks.shape
     rows = np.arange(bs) if rows is None else np.asarray(rows)
-    base = bits(inp.base) if base_bits is None else base_bits
     kw = dict(w2q=q, scales=sc) if q is not None else dict(w2_bits=bits(inp.w2))
-    res = O.walk(base[rows], bits(inp.w1), inp.prev.numpy()[rows], K, slot=rows.astype(np.int32),
+    if base_f64_all is not None:
+        base_rows = None
+        kw["base_f64"] = np.ascontiguousarray(base_f64_all[rows])
+    else:
+        base_rows = (bits(inp.base) if base_bits is None else base_bits)[rows]
+    res = O.walk(base_rows, bits(inp.w1), inp.prev.numpy()[rows], K, slot=rows.astype(np.int32),
                  seeds=inp.seeds.numpy().astype(np.uint64)[rows], mode=mode, temperature=T,
                  top_k=top_k, follow=toks[rows], tie_tol=TIE_TOL, bf16_eps=BF16_EPS,
                  nthreads=nthreads(), want_logits=gpu_logits is not None, **kw)
@@ -98,13 +105,13 @@ def record(label: str, st: ParityStats) -> ParityStats:
     return st
 
 
-def check_walk_rows(O, inp, gpu_tokens, *, label: str, chunk: int = 8, **kw) -> ParityStats:
-    """check_walk over every row, a few rows at a time (bounded fp64 logit buffers), with
-    the summed counts recorded under `label`."""
-    bs = gpu_tokens.shape[0]
+def check_walk_rows(O, inp, gpu_tokens, *, label: str, chunk: int = 8, rows_subset=None, **kw) -> ParityStats:
+    """check_walk over every row (or the rows of `rows_subset`), a few rows at a time
+    (bounded fp64 logit buffers), with the summed counts recorded under `label`."""
+    all_rows = list(range(gpu_tokens.shape[0])) if rows_subset is None else list(rows_subset)
     tot = ParityStats(0, 0, 0, 0)
-    for r0 in range(0, bs, chunk):
-        st = check_walk(O, inp, gpu_tokens, rows=list(range(r0, min(bs, r0 + chunk))), label=None, **kw)
+    for r0 in range(0, len(all_rows), chunk):
+        st = check_walk(O, inp, gpu_tokens, rows=all_rows[r0:r0 + chunk], label=None, **kw)
         tot.steps += st.steps
         tot.same += st.same
         tot.near_tie += st.near_tie

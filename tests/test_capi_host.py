@@ -130,3 +130,32 @@ def test_verify_binding_refuses_mismatched_buffers():
     with pytest.raises(ValueError, match="CUDA tensor"):  # well-formed, but on the host
         capi.verify(good["t"], good["d"], good["k"], good["s"], 1.0,
                     accepted=torch.zeros(bs, dtype=torch.int32), out_tokens=torch.zeros(bs, K + 1, dtype=torch.int32))
+
+
+def test_lmhead_arguments_rejected_on_host(L):
+    """dspark_lmhead_topk refuses bad shapes, unaligned rows and a short workspace before
+    any CUDA call; the workspace size grows with every dimension."""
+    from dspark_markov_draft_gb300 import capi
+    fake = 1 << 20
+    ws = int(L.dspark_lmhead_workspace_size(448, 151936, 512))
+    assert ws > 0
+    assert int(L.dspark_lmhead_workspace_size(448, 151936, 4096)) > ws
+    assert int(L.dspark_lmhead_workspace_size(0, 151936, 512)) == 0
+    assert int(L.dspark_lmhead_workspace_size(448, 151936, 0)) == 0
+
+    def args(**kw):
+        d = dict(hidden=fake, lm_head=fake, V=151936, M=448, d=2048, top_k=512, cand=fake, cand_base=fake,
+                 workspace=fake, workspace_bytes=ws)
+        d.update(kw)
+        x = capi.LmheadArgs()
+        for k, v in d.items():
+            setattr(x, k, v)
+        return x
+    assert L.dspark_lmhead_topk(None, None) == 1
+    for bad in (dict(hidden=None), dict(lm_head=None), dict(cand=None), dict(cand_base=None),
+                dict(M=0), dict(V=0), dict(d=32), dict(d=2000), dict(d=16384 + 64),
+                dict(top_k=0), dict(top_k=8193), dict(V=100, top_k=101),
+                dict(hidden=fake + 8), dict(lm_head=fake + 2)):
+        assert L.dspark_lmhead_topk(C.byref(args(**bad)), None) == 1, bad
+    for bad in (dict(workspace=None), dict(workspace=fake + 64), dict(workspace_bytes=ws - 1)):
+        assert L.dspark_lmhead_topk(C.byref(args(**bad)), None) == 8, bad
