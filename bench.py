@@ -363,6 +363,70 @@ def time_verify(dev, flush, peaks, steps, V=151936, K=7, bs=64, T=1.0):
             "l2": "flushed before every call"}
 
 
+LMHEAD_CASES = [(2048, 512), (2048, 4096), (4096, 512)]
+
+
+def time_lmhead(dev, flush, peaks, steps, V=151936, K=7, bs=64, d=2048, k=512):
+    """The drafter's LM head fused with the top-k selection (dspark_lmhead_topk: sample
+    GEMM, pivot, filter GEMM, select) for bs*K hidden rows of width d, then the top-k walk
+    on its candidates (sampled, T=1). Per-call CUDA-event times with the L2 flushed before
+    each call. Roofline: the dense LM-head product's flops (2 M V d) on the tensor cores;
+    the HBM floor is one read of the LM head and the hidden rows."""
+    from dspark_markov_draft_gb300 import capi, synth
+    M = bs * K
+    hidden, head = synth.lmhead(M, d, V, seed=1)
+    hidden, head = hidden.to(dev), head.to(dev)
+    inp = synth.make(V, bs, K, seed=0)
+    w1, w2, prev, seeds = inp.w1.to(dev), inp.w2.to(dev), inp.prev.to(dev), inp.seeds.to(dev)
+    cand = torch.empty((M, k), dtype=torch.int32, device=dev)
+    cbase = torch.empty((M, k), dtype=torch.float32, device=dev)
+    ws = capi.lmhead_workspace(M, V, k, device=dev)
+    stats = torch.zeros(2, dtype=torch.int32, device=dev)
+    tokens = torch.empty((bs, K), dtype=torch.int32, device=dev)
+    wws = capi.alloc_workspace(V, bs, K, k, device=dev)
+    wargs = capi.make_args(None, w1, prev, tokens, wws, w2=w2, seeds=seeds, mode=capi.PROBABILISTIC,
+                           temperature=1.0, top_k=k, topk_cand=cand.view(bs, K, k),
+                           topk_base=cbase.view(bs, K, k), V=V)
+    stream = torch.cuda.current_stream()
+
+    def head_call():
+        capi.lmhead_topk(hidden, head, k, cand=cand, cand_base=cbase, workspace=ws, stats=stats, stream=stream)
+
+    def timed(fn, n):
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for s_, e_ in evs:
+            flush.zero_()
+            s_.record(stream)
+            fn()
+            e_.record(stream)
+        torch.cuda.synchronize()
+        return 1000 * statistics.median([s_.elapsed_time(e_) for s_, e_ in evs])
+
+    def both():
+        head_call()
+        st = capi.walk_args_call(wargs, stream, topk=True)
+        if st:
+            raise RuntimeError(f"top-k walk failed: {capi.STATUS.get(st, st)}")
+
+    us_head = timed(head_call, steps)
+    us_both = timed(both, steps)
+    flops = 2.0 * M * V * d
+    tflops = flops / (us_head * 1e-6) / 1e12
+    nbytes = 2.0 * (V * d + M * d)
+    return {"workload": f"lmhead d{d} v{V} k{K} bs{bs} top-k {k}", "hidden_rows": M,
+            "us_lmhead_topk": us_head, "us_lmhead_topk_plus_walk": us_both,
+            "tensor_floor_us": flops / (peaks["bf16_tflops"] * 1e12) * 1e6,
+            "hbm_floor_us": nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"]},
+            "rows_on_exact_path": int(stats[0].item()), "kernels_per_call": 4 + 2,
+            "l2": "flushed before every call"}
+
+
 def time_e2e(cfg, t, args, steps, dev):
     """Walk through dspark_walk_from_host: per-step H2D of base/prev/seeds from pinned
     host memory, the walk, D2H of the tokens; timed with events around all of it."""
@@ -558,6 +622,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-verify", action="store_true")
+    ap.add_argument("--no-lmhead", action="store_true")
     ap.add_argument("--workload", default=MAIN["name"],
                     help="run this workload as the main line (one of the built-in names)")
     a = ap.parse_args()
@@ -613,6 +678,8 @@ def main():
     e2e_ms, h2d, d2h = (float("nan"), 0, 0) if a.no_e2e else time_e2e(cfg, t, args, max(3, a.steps // 2), dev)
     graph_times = time_graph(args, max(5, a.steps), flush)  # outside the timed region
     verify = None if a.no_verify else time_verify(dev, flush, peaks, max(5, a.steps))
+    lmhead = [] if a.no_lmhead else [time_lmhead(dev, flush, peaks, max(5, a.steps), d=d_, k=k_)
+                                     for d_, k_ in LMHEAD_CASES]
     fl, res_rows = floors_of(cfg)
     us = 1000 * ms
     roof = roofline(cfg, peaks, fl, us, sms)
@@ -674,6 +741,7 @@ def main():
             "roofline": roof,
             "floors": floor_rec,
             "verify": verify,
+            "lmhead_topk": lmhead,
             "cpu_baseline": cpu,
             "e2e": {"value": world * toks / (e2e_ms * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

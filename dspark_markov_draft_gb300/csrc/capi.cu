@@ -520,6 +520,7 @@ int32_t dspark_lmhead_topk(const dspark_lmhead_args* a, dspark_stream_t stream) 
   p.stats = a->stats_dev;
   p.status_dev = a->status_dev;
   p.flags = (a->flags & DSPARK_LMHEAD_FLAG_EXACT) ? kLmForceExact : 0;
+  p.cluster = kLmCluster;
   p.timeout_ns = 1000ull * (a->timeout_us ? a->timeout_us : 1000000u);
   auto map2d = [&](CUtensorMap* m, const void* ptr, cuuint64_t inner, cuuint64_t rows, cuuint64_t stride_bytes,
                    cuuint32_t box_rows) {
@@ -534,11 +535,15 @@ int32_t dspark_lmhead_topk(const dspark_lmhead_args* a, dspark_stream_t stream) 
   const cuuint64_t d = static_cast<cuuint64_t>(a->d);
   if (!map2d(&p.w_map, a->lm_head, d, static_cast<cuuint64_t>(a->V), 2 * d, 128) ||
       !map2d(&p.ws_map, a->lm_head, d, static_cast<cuuint64_t>(p.S), 2 * d * kLmSampleStride, 128) ||
-      !map2d(&p.h_map, a->hidden, d, static_cast<cuuint64_t>(a->M), 2 * d, 256))
+      !map2d(&p.h_map0, a->hidden, d, static_cast<cuuint64_t>(a->M), 2 * d, static_cast<cuuint32_t>(lm_box0(a->M))) ||
+      (lm_box1(a->M) > 0 &&
+       !map2d(&p.h_map1, a->hidden, d, static_cast<cuuint64_t>(a->M), 2 * d, static_cast<cuuint32_t>(lm_box1(a->M)))))
     return DSPARK_ERR_UNSUPPORTED;
-  // pivot rank: about 1.5 k times the sampling fraction, plus a margin
+  // pivot rank: the sampled keys that stand for about 1.5 k + 512 of the V logits (the
+  // list then holds at least k and at most 3 k + 1024 entries with a wide margin)
   const double frac = static_cast<double>(p.S) / static_cast<double>(a->V);
-  int rank = static_cast<int>(1.5 * a->top_k * frac) + 32;
+  int rank = static_cast<int>((1.5 * a->top_k + 512.0) * frac + 0.5);
+  if (rank < 1) rank = 1;
   if (rank > p.S) rank = p.S;
   const cudaError_t e = launch_lmhead(p, caps.sms, rank, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DSPARK_OK : cuda_fail(e, "lmhead kernels launch");

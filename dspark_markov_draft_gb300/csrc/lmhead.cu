@@ -5,9 +5,10 @@
 //
 //   1. sample pass: the same GEMM over every kSampleStride-th LM-head row; the logits
 //      of those S rows are stored ([M, S] fp32, small);
-//   2. pivot: per hidden row m, the j-th largest sampled key, with j chosen so that far
-//      more than k of the V logits lie at or above it (keys: order-preserving uint32 of
-//      the fp32 logit, NaN largest, -0 equal to +0);
+//   2. pivot: per hidden row m, a key with at least j sampled keys at or above it (the
+//      j-th largest, resolved to its top bits), j chosen so that more than k of the V
+//      logits lie at or above it (keys: order-preserving uint32 of the fp32 logit, NaN
+//      largest, -0 equal to +0);
 //   3. filter pass: the GEMM over all V rows; the epilogue appends every logit whose key
 //      reaches the row's pivot to the row's list, as the packed word {key, 2^32-1-v}
 //      (the largest words are the top-k in the method's order: larger value first,
@@ -20,8 +21,11 @@
 // The GEMM: D[128 LM-head rows x up to 512 hidden rows] = A . B^T with A = 128 rows of
 // the LM head (bf16, K-major, 128-byte swizzle, staged by tensor-map copies) and B = the
 // hidden rows (two N parts of up to 256), accumulated in fp32 in tensor memory over
-// 64-wide chunks of d (tcgen05 kind::f16, bf16 inputs). Warp 0 copies, warp 1 issues
-// the MMAs, warps 2-5 run the epilogue; two stages of A and B.
+// 64-wide chunks of d (tcgen05 kind::f16, bf16 inputs). Warp 0 copies (and prefetches
+// the LM-head chunks a few stages ahead into L2), warp 1 issues the MMAs, sixteen warps
+// read the accumulator back; as many stages as shared memory holds (three at 448 hidden
+// rows). The epilogue is short next to a tile's MMAs: each of its warps reads 32 x 32
+// accumulators per step and tests them against per-column pivots broadcast by shuffles.
 #include <algorithm>
 #include <cstdint>
 
@@ -34,9 +38,6 @@ namespace {
 
 constexpr int kLmTile = 128;          // LM-head rows per tile (the MMA's M)
 constexpr int kLmChunk = 64;          // d elements per stage (128 bytes of bf16)
-constexpr int kLmStages = 2;
-constexpr int kLmBStageBytes = 2 * 256 * 128;   // two N parts of 256 hidden rows
-constexpr int kLmAStageBytes = kLmTile * 128;
 constexpr uint32_t kLmTmemCols = 512;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -82,6 +83,61 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, const
 __device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(mbar)) : "memory");
 }
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster (a launch without clusters is a cluster of one).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Tensor-map copy of one 2-D box into this CTA's shared memory (leader lane only).
+__device__ __forceinline__ void tma_2d_if(uint32_t leader, void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "{ .reg .pred q; setp.ne.b32 q, %5, 0; "
+      "@q cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4]; }"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "r"(leader)
+      : "memory");
+}
+// The same box written to the same offsets in every CTA of `mask`, each CTA's barrier at
+// `bar`'s offset receiving the bytes.
+__device__ __forceinline__ void tma_2d_mc_if(uint32_t leader, void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                             uint16_t mask) {
+  asm volatile(
+      "{ .reg .pred q; setp.ne.b32 q, %5, 0; "
+      "@q cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%2, %3}], [%4], %6; }"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "r"(leader),
+        "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_2d_if(uint32_t leader, const CUtensorMap* map, int x, int y) {
+  asm volatile("{ .reg .pred q; setp.ne.b32 q, %3, 0; @q cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}]; }"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(leader) : "memory");
+}
+// Arrive on `bar` once the MMAs issued so far complete: in this CTA only, or at the same
+// offset in every CTA of `mask`.
+__device__ __forceinline__ void mma_commit_if(uint32_t leader, uint64_t* bar) {
+  asm volatile("{ .reg .pred q; setp.ne.b32 q, %1, 0; "
+               "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0]; }"
+               ::"r"(smem_u32(bar)), "r"(leader) : "memory");
+}
+__device__ __forceinline__ void mma_commit_mc_if(uint32_t leader, uint64_t* bar, uint16_t mask) {
+  asm volatile("{ .reg .pred q; setp.ne.b32 q, %1, 0; "
+               "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %2; }"
+               ::"r"(smem_u32(bar)), "r"(leader), "h"(mask) : "memory");
+}
 
 // Inverse of order_key (the key of -0 is the key of +0: it returns +0).
 __device__ __forceinline__ float key_value(uint32_t key) {
@@ -89,35 +145,75 @@ __device__ __forceinline__ float key_value(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
+// A float threshold t with {x : !(x < t)} = {x : order_key(x) >= P} when P is the key of
+// a number; for a key in the range no number maps to (above +inf's key) it is +inf,
+// which selects {order_key(x) >= order_key(+inf)}: a larger set, still of the same form.
+// NaN logits always pass (their key is the largest).
+__device__ __forceinline__ float pivot_threshold(uint32_t P) {
+  const float t = key_value(P);
+  return (t != t && P >= 0x80000000u) ? __int_as_float(0x7f800000) : t;
+}
+
+// One unit of a GEMM pass: an LM-head tile, a chunk of up to 512 hidden rows, and a
+// range of 64-wide chunks of d (all of d unless the sample pass is split).
+struct LmUnit {
+  int tile, m0, mrows, kbeg, kend;
+};
+__device__ __forceinline__ LmUnit lm_unit(const LmParams& p, int u, int mchunks, int C, int crank, int nk) {
+  const int kp = u % p.ksplit, rest = u / p.ksplit;
+  LmUnit x;
+  x.m0 = (rest % mchunks) * 512;
+  x.tile = (rest / mchunks) * C + crank;
+  x.mrows = min(512, p.M - x.m0);
+  x.kbeg = kp * nk / p.ksplit;
+  x.kend = (kp + 1) * nk / p.ksplit;
+  return x;
+}
+
 }  // namespace
 
 // MODE 0: sample pass (rows r * stride of the LM head, logits stored); MODE 1: filter
 // pass (every row, logits at or above the row's pivot appended to its list).
+//
+// Clusters of p.cluster CTAs share the hidden-row chunks: CTA rank c of a cluster copies
+// the 32-row boxes b with b % cluster == c, multicast to every CTA of the cluster, and a
+// stage is refilled only after the MMAs of every CTA of the cluster have read it (each
+// CTA's commit arrives on the stage's empty barrier in all of them). The CTAs of a
+// cluster walk the same sequence of hidden-row chunks; each has its own LM-head tile.
 template <int MODE>
-__global__ void __launch_bounds__(192, 1) lmhead_gemm_kernel(const __grid_constant__ LmParams p) {
+__global__ void __launch_bounds__(kLmThreads, 1) lmhead_gemm_kernel(const __grid_constant__ LmParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  unsigned char* a_s = smem;                                         // [stages][128 x 128 B]
-  unsigned char* b_s = smem + kLmStages * kLmAStageBytes;            // [stages][2 x 256 x 128 B]
-  uint32_t* piv_s = reinterpret_cast<uint32_t*>(b_s + kLmStages * kLmBStageBytes);  // [4 warps][512]
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(piv_s + 4 * 512);
-  uint64_t* full = mbar;           // [stages] 1 arrival + bytes
-  uint64_t* empty = mbar + 2;      // [stages] 1 commit
-  uint64_t* dfull = mbar + 4;      // 1 commit
-  uint64_t* dempty = mbar + 5;     // 4 epilogue-warp arrivals
-  uint32_t* tbase_s = reinterpret_cast<uint32_t*>(mbar + 6);
+  const int NS = lm_stages(p.M);
+  const uint32_t stage_bytes = static_cast<uint32_t>(lm_stage_bytes(p.M));
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + NS * stage_bytes);
+  uint64_t* full = mbar;                     // [NS] 1 arrival + bytes
+  uint64_t* empty = mbar + NS;               // [NS] one commit from each CTA of the cluster
+  uint64_t* dfull = mbar + 2 * NS;           // 1 commit
+  uint64_t* dempty = mbar + 2 * NS + 1;      // kLmEpiWarps arrivals
+  uint32_t* tbase_s = reinterpret_cast<uint32_t*>(mbar + 2 * kLmMaxStages + 2);
   volatile int* fail = reinterpret_cast<volatile int*>(tbase_s + 1);
+  float* thr_s = reinterpret_cast<float*>(smem + NS * stage_bytes + 128);  // [epilogue warp][4 x 32]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int C = p.cluster;
+  const int crank = C > 1 ? static_cast<int>(cluster_rank()) : 0;
+  const int cid = C > 1 ? static_cast<int>(cluster_id()) : static_cast<int>(blockIdx.x);
+  const int ncl = C > 1 ? static_cast<int>(cluster_count()) : static_cast<int>(gridDim.x);
+  const uint16_t cmask = static_cast<uint16_t>((1u << C) - 1u);
   const int64_t rows = MODE == 0 ? p.S : p.V;                       // LM-head rows of this pass
   const int tiles = static_cast<int>((rows + kLmTile - 1) / kLmTile);
+  const int groups = (tiles + C - 1) / C;                           // tiles of one cluster step
   const int mchunks = (p.M + 511) / 512;
-  const int units = tiles * mchunks;
+  const int units = groups * mchunks * p.ksplit;                    // per cluster
   const int nk = p.d / kLmChunk;
 
   if (tid == 0) {
-    for (int b = 0; b < 6; ++b)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&mbar[b])), "r"(b == 5 ? 4u : 1u));
+    for (int b = 0; b < 2 * NS + 2; ++b) {
+      const uint32_t cnt = b == 2 * NS + 1 ? static_cast<uint32_t>(kLmEpiWarps)
+                                           : (b >= NS && b < 2 * NS ? static_cast<uint32_t>(C) : 1u);
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&mbar[b])), "r"(cnt));
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *fail = 0;
   }
@@ -128,72 +224,74 @@ __global__ void __launch_bounds__(192, 1) lmhead_gemm_kernel(const __grid_consta
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
+  cluster_sync();  // every CTA's barriers are initialised before any copy lands in it
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tbase_s;
   const CUtensorMap* amap = MODE == 0 ? &p.ws_map : &p.w_map;
 
   if (warp == 0) {
     // ------------------------------------------------------------ tensor-map copies
-    const bool leader = lane == 0;
+    const uint32_t leader = lane == 0;
     int g = 0;  // global chunk counter
-    for (int u = blockIdx.x; u < units && !__any_sync(kFull, *fail); u += gridDim.x) {
-      const int tile = u / mchunks, mc = u % mchunks;
-      const int m0 = mc * 512;
-      const int nparts = p.M - m0 > 256 ? 2 : 1;
-      const uint32_t bytes = kLmAStageBytes + nparts * 256 * 128;
+    for (int u = cid; u < units && !__any_sync(kFull, *fail); u += ncl) {
+      const LmUnit w = lm_unit(p, u, mchunks, C, crank, nk);
+      const int tile = w.tile, m0 = w.m0;
+      const uint32_t bytes = kLmAStageBytes + lm_b_rows(p.M) * 128;  // both boxes, rows past M filled
+      // the first chunks of this tile go to L2 now (the rest are prefetched as it runs)
+      const uint32_t pf = leader && static_cast<int64_t>(tile) * kLmTile < rows;  // tile holds rows
+      for (int kc = w.kbeg; kc < min(w.kend, w.kbeg + NS); ++kc) tma_prefetch_2d_if(pf, amap, kc * kLmChunk, tile * kLmTile);
       bool ok = true;
-      for (int kc = 0; kc < nk; ++kc, ++g) {
-        const int s = g % kLmStages;
-        if (g >= kLmStages && (ok = !__any_sync(kFull, !mbar_wait(&empty[s], ((g / kLmStages) - 1) & 1, p, fail))) == false) break;
+      for (int kc = w.kbeg; kc < w.kend; ++kc, ++g) {
+        const int s = g % NS;
+        if (g >= NS && (ok = !__any_sync(kFull, !mbar_wait(&empty[s], ((g / NS) - 1) & 1, p, fail))) == false) break;
+        if (kc + NS < w.kend) tma_prefetch_2d_if(pf, amap, (kc + NS) * kLmChunk, tile * kLmTile);
+        unsigned char* st = smem + s * stage_bytes;
         asm volatile(
             "{ .reg .pred q; setp.ne.b32 q, %2, 0; @q mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1; }"
-            ::"r"(smem_u32(&full[s])), "r"(bytes), "r"(static_cast<uint32_t>(leader)) : "memory");
-        asm volatile(
-            "{ .reg .pred q; setp.ne.b32 q, %5, 0; "
-            "@q cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4]; }"
-            ::"r"(smem_u32(a_s + s * kLmAStageBytes)), "l"(reinterpret_cast<uint64_t>(amap)),
-              "r"(kc * kLmChunk), "r"(tile * kLmTile), "r"(smem_u32(&full[s])), "r"(static_cast<uint32_t>(leader))
-            : "memory");
-        for (int part = 0; part < nparts; ++part)
-          asm volatile(
-              "{ .reg .pred q; setp.ne.b32 q, %5, 0; "
-              "@q cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4]; }"
-              ::"r"(smem_u32(b_s + s * kLmBStageBytes + part * 256 * 128)), "l"(reinterpret_cast<uint64_t>(&p.h_map)),
-                "r"(kc * kLmChunk), "r"(m0 + 256 * part), "r"(smem_u32(&full[s])), "r"(static_cast<uint32_t>(leader))
-              : "memory");
+            ::"r"(smem_u32(&full[s])), "r"(bytes), "r"(leader) : "memory");
+        tma_2d_if(leader, st, amap, kc * kLmChunk, tile * kLmTile, &full[s]);
+        // box 0 from cluster rank 0, box 1 from rank 1 (or 0 without a cluster)
+        const int nbox = lm_box1(p.M) > 0 ? 2 : 1;
+        for (int b = crank; b < nbox; b += C) {
+          unsigned char* dst = st + kLmAStageBytes + b * 256 * 128;
+          const CUtensorMap* hm = b == 0 ? &p.h_map0 : &p.h_map1;
+          if (C > 1)
+            tma_2d_mc_if(leader, dst, hm, kc * kLmChunk, m0 + 256 * b, &full[s], cmask);
+          else
+            tma_2d_if(leader, dst, hm, kc * kLmChunk, m0 + 256 * b, &full[s]);
+        }
       }
       if (!ok) break;
     }
     // copies still in flight land before the CTA leaves (bounded)
-    for (int s = 0; s < kLmStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       if (g - 1 - s < 0) continue;
       const int gl = g - 1 - s;
       const uint64_t t0 = globaltimer_ns();
-      while (!__all_sync(kFull, mbar_try(&full[gl % kLmStages], (gl / kLmStages) & 1)) &&
+      while (!__all_sync(kFull, mbar_try(&full[gl % NS], (gl / NS) & 1)) &&
              !__any_sync(kFull, globaltimer_ns() - t0 >= p.timeout_ns)) {}
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
-    const bool leader = lane == 0;
+    const uint32_t leader = lane == 0;
     int g = 0, un = 0, last = -1;
-    for (int u = blockIdx.x; u < units && !__any_sync(kFull, *fail); u += gridDim.x, ++un) {
-      const int mc = u % mchunks;
-      const int m0 = mc * 512;
-      const int mrows = min(512, p.M - m0);
+    for (int u = cid; u < units && !__any_sync(kFull, *fail); u += ncl, ++un) {
+      const LmUnit w = lm_unit(p, u, mchunks, C, crank, nk);
+      const int mrows = w.mrows;
       const int n0 = (min(256, mrows) + 15) & ~15;
       const int n1 = mrows > 256 ? ((mrows - 256 + 15) & ~15) : 0;
       if (un >= 1 && __any_sync(kFull, !mbar_wait(dempty, (un - 1) & 1, p, fail))) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       bool ok = true;
-      for (int kc = 0; kc < nk; ++kc, ++g) {
-        const int s = g % kLmStages;
-        if (__any_sync(kFull, !mbar_wait(&full[s], (g / kLmStages) & 1, p, fail))) { ok = false; break; }
+      for (int kc = w.kbeg; kc < w.kend; ++kc, ++g) {
+        const int s = g % NS;
+        if (__any_sync(kFull, !mbar_wait(&full[s], (g / NS) & 1, p, fail))) { ok = false; break; }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t a0 = smem_u32(a_s + s * kLmAStageBytes), b0 = smem_u32(b_s + s * kLmBStageBytes);
+        const uint32_t a0 = smem_u32(smem + s * stage_bytes), b0 = a0 + kLmAStageBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t ad = sw128_desc(a0 + kk * 32);
-          const uint32_t acc = (kc > 0 || kk > 0) ? 1u : 0u;
+          const uint32_t acc = (kc > w.kbeg || kk > 0) ? 1u : 0u;
           for (int part = 0; part < 2; ++part) {
             const int np = part == 0 ? n0 : n1;
             if (np == 0) continue;
@@ -201,45 +299,77 @@ __global__ void __launch_bounds__(192, 1) lmhead_gemm_kernel(const __grid_consta
             asm volatile(
                 "{ .reg .pred p, q; setp.ne.b32 p, %4, 0; setp.ne.b32 q, %5, 0; "
                 "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
-                ::"r"(tmem + part * 256), "l"(ad), "l"(bd), "r"(bf16_idesc(np)), "r"(acc),
-                  "r"(static_cast<uint32_t>(leader)) : "memory");
+                ::"r"(tmem + part * 256), "l"(ad), "l"(bd), "r"(bf16_idesc(np)), "r"(acc), "r"(leader)
+                : "memory");
           }
         }
-        asm volatile("{ .reg .pred q; setp.ne.b32 q, %1, 0; "
-                     "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0]; }"
-                     ::"r"(smem_u32(&empty[s])), "r"(static_cast<uint32_t>(leader)) : "memory");
+        if (C > 1)
+          mma_commit_mc_if(leader, &empty[s], cmask);
+        else
+          mma_commit_if(leader, &empty[s]);
       }
       if (!ok) break;
-      asm volatile("{ .reg .pred q; setp.ne.b32 q, %1, 0; "
-                   "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0]; }"
-                   ::"r"(smem_u32(dfull)), "r"(static_cast<uint32_t>(leader)) : "memory");
+      mma_commit_if(leader, dfull);
       last = un;
     }
-    if (last >= 0) {  // the last unit's MMAs complete before tensor memory goes (bounded)
-      const uint64_t t0 = globaltimer_ns();
+    // before tensor memory and the stages go (bounded): the last unit's MMAs are done,
+    // and every CTA of the cluster has released the stages (no arrival still to come)
+    const uint64_t t0 = globaltimer_ns();
+    if (last >= 0)
       while (!__all_sync(kFull, mbar_try(dfull, last & 1)) && !__any_sync(kFull, globaltimer_ns() - t0 >= p.timeout_ns)) {}
+    for (int s = 0; s < NS; ++s) {
+      if (g - 1 - s < 0) continue;
+      const int gl = g - 1 - s;
+      while (!__all_sync(kFull, mbar_try(&empty[gl % NS], (gl / NS) & 1)) &&
+             !__any_sync(kFull, globaltimer_ns() - t0 >= p.timeout_ns)) {}
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // tensor-memory lane quadrant (warps 2..5 -> 2, 3, 0, 1)
+    const int q = warp & 3;                    // tensor-memory lane quadrant
+    const int cg = (warp - 2) >> 2;            // column group: 32-column steps cg, cg + 4, ...
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
-    uint32_t* piv_w = piv_s + 512 * (warp - 2);  // this warp's copy of the chunk's pivots
     int un = 0;
-    for (int u = blockIdx.x; u < units && !__any_sync(kFull, *fail); u += gridDim.x, ++un) {
-      const int tile = u / mchunks, mc = u % mchunks;
-      const int m0 = mc * 512;
-      const int mrows = min(512, p.M - m0);
+    for (int u = cid; u < units && !__any_sync(kFull, *fail); u += ncl, ++un) {
+      const LmUnit w = lm_unit(p, u, mchunks, C, crank, nk);
+      const int tile = w.tile, m0 = w.m0, mrows = w.mrows;
+      // this warp's column thresholds (step i: columns 32 cg + 128 i + j at thr_w[32 i + j]),
+      // read before the accumulator is ready: a logit passes when !(x < threshold)
+      float* thr_w = thr_s + 128 * (warp - 2);
       if (MODE == 1) {
-        __syncwarp();  // the previous unit's pivots are read
-        for (int t = lane; t < mrows; t += 32) piv_w[t] = p.pivot[m0 + t];
+        __syncwarp();  // the previous unit's thresholds are read
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = 32 * cg + 128 * i + lane;
+          thr_w[32 * i + lane] = c < mrows ? pivot_threshold(__ldg(p.pivot + m0 + c)) : __int_as_float(0x7f800000);
+        }
         __syncwarp();
       }
       if (__any_sync(kFull, !mbar_wait(dfull, un & 1, p, fail))) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int64_t r = static_cast<int64_t>(tile) * kLmTile + 32 * q + lane;  // LM-head row of the pass
       const bool rvalid = r < rows;
-      for (int c0 = 0; c0 < mrows; c0 += 32) {
-        const uint32_t col = c0;  // hidden row 256 + j of part 1 sits in column 256 + j
+      // filter pass: appends wait in a four-entry queue {column, key} (the row r is this
+      // lane's) and are written after the accumulator is released
+      uint64_t q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+      int nq = 0;
+      auto flush = [&]() {
+        const uint64_t e[4] = {q0, q1, q2, q3};
+        uint32_t pos[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (i < nq) pos[i] = atomicAdd(p.cnt + m0 + static_cast<int>(e[i] >> 32), 1u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (i < nq && pos[i] < static_cast<uint32_t>(p.cap))
+            p.list[static_cast<size_t>(m0 + static_cast<int>(e[i] >> 32)) * p.cap + pos[i]] =
+                pack_best(static_cast<uint32_t>(e[i]), static_cast<uint32_t>(r));
+        nq = 0;
+      };
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c0 = 32 * cg + 128 * i;
+        if (c0 >= mrows) break;
+        // hidden row c0 + j sits in column c0 + j (part 1 starts at column 256)
         uint32_t v[32];
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
@@ -248,32 +378,58 @@ __global__ void __launch_bounds__(192, 1) lmhead_gemm_kernel(const __grid_consta
               "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
               "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
               "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-            : "r"(tmem + lane_off + col) : "memory");
+            : "r"(tmem + lane_off + static_cast<uint32_t>(c0)) : "memory");
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        const int ncol = min(32, mrows - c0);
+        if constexpr (MODE == 0) {
+          if (rvalid) {
+            float* dst = p.sample + static_cast<size_t>(m0 + c0) * p.S + r;
+            if (p.ksplit > 1) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int m = c0 + j;  // hidden row within the chunk
-          if (m >= mrows || !rvalid) continue;
-          const float x = __uint_as_float(v[j]);
-          if constexpr (MODE == 0) {
-            p.sample[static_cast<size_t>(m0 + m) * p.S + r] = x;
-          } else {
-            const uint32_t key = order_key(x);
-            if (key >= piv_w[m]) {
-              const uint32_t pos = atomicAdd(p.cnt + m0 + m, 1u);
-              if (pos < static_cast<uint32_t>(p.cap))
-                p.list[static_cast<size_t>(m0 + m) * p.cap + pos] = pack_best(key, static_cast<uint32_t>(r));
+              for (int j = 0; j < 32; ++j)
+                if (j < ncol) atomicAdd(dst + static_cast<size_t>(j) * p.S, __uint_as_float(v[j]));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < ncol) dst[static_cast<size_t>(j) * p.S] = __uint_as_float(v[j]);
             }
+          }
+        } else {
+          uint32_t pass = 0;
+          const float4* t4 = reinterpret_cast<const float4*>(thr_w + 32 * i);
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 t = t4[j4];
+            pass |= !(__uint_as_float(v[4 * j4 + 0]) < t.x) ? (1u << (4 * j4 + 0)) : 0u;
+            pass |= !(__uint_as_float(v[4 * j4 + 1]) < t.y) ? (1u << (4 * j4 + 1)) : 0u;
+            pass |= !(__uint_as_float(v[4 * j4 + 2]) < t.z) ? (1u << (4 * j4 + 2)) : 0u;
+            pass |= !(__uint_as_float(v[4 * j4 + 3]) < t.w) ? (1u << (4 * j4 + 3)) : 0u;
+          }
+          if (!rvalid) pass = 0;
+          pass &= ncol == 32 ? 0xFFFFFFFFu : ((1u << ncol) - 1u);
+          while (pass) {
+            const int j = __ffs(pass) - 1;
+            pass &= pass - 1;
+            uint32_t x = 0;
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj)
+              if (jj == j) x = v[jj];
+            if (nq == 4) flush();
+            q3 = q2; q2 = q1; q1 = q0;
+            q0 = (static_cast<uint64_t>(c0 + j) << 32) | order_key(__uint_as_float(x));
+            ++nq;
           }
         }
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(dempty);
+      if (MODE == 1 && nq > 0) flush();
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
+  cluster_sync();  // no CTA leaves while a peer may still write into it
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kLmTmemCols) : "memory");
@@ -283,17 +439,40 @@ namespace {
 
 constexpr int kSelThreads = 512;
 
-// Block-wide radix selection step: given a 256-bin histogram in shared memory and the
-// number of items strictly above the current prefix range, the bin holding the
-// `rank`-th largest item (1-based) and the count of items above that bin.
-__device__ __forceinline__ void pick_bin(const int* hist, int above, int rank, int* out_bin, int* out_above) {
-  int acc = above, bin = 0;
-  for (int h = 255; h >= 0; --h) {
-    if (acc + hist[h] >= rank) { bin = h; break; }
-    acc += hist[h];
+// One radix-selection step, run by warp 0 of the block: from a 256-bin histogram of
+// the items that share the current prefix, and the number of items above that prefix,
+// the bin holding the `rank`-th largest item (1-based), the items above that bin, and
+// whether the bin's items are exactly the ones still needed (then the selection ends:
+// every item at or above the bin's lower edge is taken). Lane l scans bins
+// 255 - 8l ... 248 - 8l after a warp prefix sum of the lanes' totals.
+__device__ __forceinline__ void pick_bin(const int* hist, int above, int rank, int* sel) {
+  const int lane = threadIdx.x & 31;
+  int c[8], tot = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    c[i] = hist[255 - 8 * lane - i];
+    tot += c[i];
   }
-  *out_bin = bin;
-  *out_above = acc;
+  int incl = tot;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(kFull, incl, off);
+    if (lane >= off) incl += y;
+  }
+  const int excl = incl - tot;
+  if (above + excl < rank && rank <= above + incl) {
+    int acc = above + excl;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (acc + c[i] >= rank) {
+        sel[0] = 255 - 8 * lane - i;
+        sel[1] = acc;
+        sel[2] = acc + c[i] == rank;
+        break;
+      }
+      acc += c[i];
+    }
+  }
 }
 
 // fp32 dot product of hidden row m and LM-head row v on CUDA cores (fixed order).
@@ -315,32 +494,60 @@ __device__ __forceinline__ float dot_row(const LmParams& p, int m, int64_t v) {
 
 }  // namespace
 
-// Per hidden row: the pivot key = the j-th largest key of the row's sampled logits (one
-// CTA per row, radix selection over four bytes), and the row's list counter zeroed.
+// Per hidden row: the pivot P, the largest key with at least j of the row's sampled keys
+// at or above it, resolved to its top kPivotBits bits (one CTA per row). Bitwise binary
+// search: starting from P = 0, each step sets the next bit when the sampled keys at or
+// above the candidate still number j or more (a count by every thread over its keys, a
+// warp sum and one shared-memory add per warp). At least j sampled keys are >= P; the
+// low bits left at zero let a few more through (those sharing P's top bits), which the
+// list capacity absorbs. The row's list counter is zeroed. Keys are staged in shared
+// memory when they fit (kPivotSmemKeys), else re-read from the sample rows.
+constexpr int kPivotSmemKeys = 40960;
+constexpr int kPivotBits = 20;
+
 __global__ void __launch_bounds__(kSelThreads) lmhead_pivot_kernel(const LmParams p, int j) {
-  __shared__ int hist[256];
-  __shared__ int sel[2];
+  extern __shared__ __align__(16) uint32_t keys_s[];
+  __shared__ int count[2];
   const int m = blockIdx.x;
   const float* x = p.sample + static_cast<size_t>(m) * p.S;
-  uint32_t prefix = 0;
-  int above = 0;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int sh = 24 - 8 * pass;
-    for (int t = threadIdx.x; t < 256; t += blockDim.x) hist[t] = 0;
-    __syncthreads();
-    for (int s = threadIdx.x; s < p.S; s += blockDim.x) {
-      const uint32_t key = order_key(x[s]);
-      if (pass == 0 || (key >> (sh + 8)) == prefix) atomicAdd(&hist[(key >> sh) & 0xFFu], 1);
+  const bool staged = p.S <= kPivotSmemKeys;
+  if (staged) {
+    for (int s0 = threadIdx.x; s0 < p.S; s0 += 8 * blockDim.x) {
+      float xv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int s = s0 + i * blockDim.x;
+        xv[i] = s < p.S ? x[s] : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int s = s0 + i * blockDim.x;
+        if (s < p.S) keys_s[s] = order_key(xv[i]);
+      }
     }
+  }
+  if (threadIdx.x < 2) count[threadIdx.x] = 0;
+  __syncthreads();
+  uint32_t P = 0;
+  for (int b = 31; b >= 32 - kPivotBits; --b) {
+    const uint32_t cand = P | (1u << b);
+    int c = 0;
+    if (staged) {
+      for (int s = threadIdx.x; s < p.S; s += blockDim.x) c += keys_s[s] >= cand ? 1 : 0;
+    } else {
+      for (int s = threadIdx.x; s < p.S; s += blockDim.x) c += order_key(x[s]) >= cand ? 1 : 0;
+    }
+    c = __reduce_add_sync(kFull, c);
+    const int slot = b & 1;  // alternate counters: one is cleared while the other is summed
+    if ((threadIdx.x & 31) == 0) atomicAdd(&count[slot], c);
     __syncthreads();
-    if (threadIdx.x == 0) pick_bin(hist, above, j, &sel[0], &sel[1]);
-    __syncthreads();
-    prefix = (prefix << 8) | static_cast<uint32_t>(sel[0]);
-    above = sel[1];
+    const int tot = count[slot];
+    if (threadIdx.x == 0) count[slot ^ 1] = 0;
+    if (tot >= j) P = cand;
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    p.pivot[m] = prefix;
+    p.pivot[m] = P;
     p.cnt[m] = 0u;
   }
 }
@@ -352,7 +559,7 @@ __global__ void __launch_bounds__(kSelThreads) lmhead_select_kernel(const LmPara
   extern __shared__ __align__(1024) unsigned char sel_raw[];
   uint64_t* words = reinterpret_cast<uint64_t*>(sel_raw);             // [cap]
   __shared__ int hist[256];
-  __shared__ int sel[2];
+  __shared__ int sel[3];
   __shared__ int outpos;
   const int m = blockIdx.x;
   const int k = p.k;
@@ -367,26 +574,30 @@ __global__ void __launch_bounds__(kSelThreads) lmhead_select_kernel(const LmPara
     for (int t = threadIdx.x; t < n; t += blockDim.x) words[t] = p.list[static_cast<size_t>(m) * p.cap + t];
     __syncthreads();
     uint64_t prefix = 0;
-    int above = 0;
+    int above = 0, sh = 0;
     for (int pass = 0; pass < 8; ++pass) {
-      const int sh = 56 - 8 * pass;
+      sh = 56 - 8 * pass;
       for (int t = threadIdx.x; t < 256; t += blockDim.x) hist[t] = 0;
+      if (threadIdx.x == 0) { sel[0] = 0; sel[1] = above; sel[2] = 1; }
       __syncthreads();
       for (int t = threadIdx.x; t < n; t += blockDim.x) {
         const uint64_t w = words[t];
         if (pass == 0 || (w >> (sh + 8)) == prefix) atomicAdd(&hist[(w >> sh) & 0xFFu], 1);
       }
       __syncthreads();
-      if (threadIdx.x == 0) pick_bin(hist, above, k, &sel[0], &sel[1]);
+      if (threadIdx.x < 32) pick_bin(hist, above, k, sel);
       __syncthreads();
       prefix = (prefix << 8) | static_cast<uint64_t>(sel[0]);
       above = sel[1];
+      const bool done = sel[2] != 0;
       __syncthreads();
+      if (done) break;
     }
-    // words are distinct (one per vocabulary entry): exactly k are >= the k-th largest
+    // words are distinct (one per vocabulary entry): exactly k are >= the threshold
+    const uint64_t thr = prefix << sh;
     for (int t = threadIdx.x; t < n; t += blockDim.x) {
       const uint64_t w = words[t];
-      if (w >= prefix) {
+      if (w >= thr) {
         const int pos = atomicAdd(&outpos, 1);
         cand[pos] = unpack_idx(w);
         cbase[pos] = key_value(static_cast<uint32_t>(w >> 32));
@@ -398,24 +609,30 @@ __global__ void __launch_bounds__(kSelThreads) lmhead_select_kernel(const LmPara
   // exact path: radix selection of the k-th largest key over the whole recomputed row,
   // then an index-ordered pass taking keys above it and the first ties
   uint32_t prefix = 0;
-  int above = 0;
+  int above = 0, sh = 0;
+  bool all_of_bin = false;
   for (int pass = 0; pass < 4; ++pass) {
-    const int sh = 24 - 8 * pass;
+    sh = 24 - 8 * pass;
     for (int t = threadIdx.x; t < 256; t += blockDim.x) hist[t] = 0;
+    if (threadIdx.x == 0) { sel[0] = 0; sel[1] = above; sel[2] = 1; }
     __syncthreads();
     for (int64_t v = threadIdx.x; v < p.V; v += blockDim.x) {
       const uint32_t key = order_key(dot_row(p, m, v));
       if (pass == 0 || (key >> (sh + 8)) == prefix) atomicAdd(&hist[(key >> sh) & 0xFFu], 1);
     }
     __syncthreads();
-    if (threadIdx.x == 0) pick_bin(hist, above, k, &sel[0], &sel[1]);
+    if (threadIdx.x < 32) pick_bin(hist, above, k, sel);
     __syncthreads();
     prefix = (prefix << 8) | static_cast<uint32_t>(sel[0]);
     above = sel[1];
+    all_of_bin = sel[2] != 0;
     __syncthreads();
+    if (all_of_bin) break;
   }
-  const uint32_t thr = prefix;
-  const int need_eq = k - above;  // entries equal to thr still to take (>= 1)
+  // all_of_bin: every key >= thr is taken (exactly k). Otherwise thr is the k-th largest
+  // key and the first k - above of the keys equal to it, in index order, are taken.
+  const uint32_t thr = prefix << sh;
+  const int need_eq = all_of_bin ? 0 : k - above;
   __shared__ int eq_seen;
   if (threadIdx.x == 0) eq_seen = 0;
   __syncthreads();
@@ -433,7 +650,7 @@ __global__ void __launch_bounds__(kSelThreads) lmhead_select_kernel(const LmPara
     int before = eq_seen;
     for (int w = 0; w < warp; ++w) before += warp_eq[w];
     before += __popc(ball & ((1u << lane) - 1u));
-    const bool take = (v < p.V) && (key > thr || (eq && before < need_eq));
+    const bool take = (v < p.V) && (all_of_bin ? key >= thr : (key > thr || (eq && before < need_eq)));
     if (take) {
       const int pos = atomicAdd(&outpos, 1);
       cand[pos] = static_cast<int32_t>(v);
@@ -451,25 +668,67 @@ __global__ void __launch_bounds__(kSelThreads) lmhead_select_kernel(const LmPara
 
 size_t lmhead_select_smem(int cap) { return static_cast<size_t>(cap) * 8; }
 
+namespace {
+
+// Grid of a GEMM pass: whole clusters, no more than can be resident at once (one CTA per
+// SM) and no more than there are cluster steps of work.
+template <int MODE>
+cudaError_t launch_gemm(LmParams& p, int sms, size_t smem, int units, cudaStream_t stream) {
+  auto fn = lmhead_gemm_kernel<MODE>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  if (p.cluster <= 1) {
+    fn<<<std::max(1, std::min(sms, units)), kLmThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kLmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(p.cluster * (sms / p.cluster)));
+  int max_clusters = 0;
+  if ((e = cudaOccupancyMaxActiveClusters(&max_clusters, fn, &cfg)) != cudaSuccess) return e;
+  if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+  const int groups = std::max(1, units);  // cluster steps
+  cfg.gridDim = dim3(static_cast<unsigned>(p.cluster * std::min(max_clusters, groups)));
+  return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+}  // namespace
+
 cudaError_t launch_lmhead(LmParams& p, int sms, int pivot_rank, cudaStream_t stream) {
-  const size_t smem = 1024 + kLmStages * (kLmAStageBytes + kLmBStageBytes) + 4 * 512 * 4 + 6 * 8 + 16;
+  const size_t smem = static_cast<size_t>(lm_gemm_smem(p.M));
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(lmhead_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(lmhead_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) != cudaSuccess)
-    return e;
   const size_t ssmem = lmhead_select_smem(p.cap);
   if ((e = cudaFuncSetAttribute(lmhead_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssmem))) != cudaSuccess)
     return e;
+  const size_t psmem = p.S <= kPivotSmemKeys ? static_cast<size_t>(p.S) * 4 : 0;
+  if ((e = cudaFuncSetAttribute(lmhead_pivot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kPivotSmemKeys * 4)) != cudaSuccess)
+    return e;
   const int mchunks = (p.M + 511) / 512;
-  const int units0 = static_cast<int>((p.S + kLmTile - 1) / kLmTile) * mchunks;
-  const int units1 = static_cast<int>((p.V + kLmTile - 1) / kLmTile) * mchunks;
-  lmhead_gemm_kernel<0><<<min(sms, units0), 192, smem, stream>>>(p);
+  const int C = std::max(1, p.cluster);
+  const int units0 = static_cast<int>(((p.S + kLmTile - 1) / kLmTile + C - 1) / C) * mchunks;
+  const int units1 = static_cast<int>(((p.V + kLmTile - 1) / kLmTile + C - 1) / C) * mchunks;
+  // the sample pass has few tiles: split d so that every cluster has work, the parts
+  // summed by fp32 atomics into the zeroed sample rows (the pivot needs no exact sums)
+  const int nk = p.d / kLmChunk;
+  p.ksplit = std::max(1, std::min(std::min(nk, 8), (sms / C) / std::max(1, units0)));
+  if (p.ksplit > 1 &&
+      (e = cudaMemsetAsync(p.sample, 0, static_cast<size_t>(p.M) * p.S * sizeof(float), stream)) != cudaSuccess)
+    return e;
+  if ((e = launch_gemm<0>(p, sms, smem, units0 * p.ksplit, stream)) != cudaSuccess) return e;
+  p.ksplit = 1;
+  lmhead_pivot_kernel<<<p.M, kSelThreads, psmem, stream>>>(p, pivot_rank);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  lmhead_pivot_kernel<<<p.M, kSelThreads, 0, stream>>>(p, pivot_rank);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  lmhead_gemm_kernel<1><<<min(sms, units1), 192, smem, stream>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_gemm<1>(p, sms, smem, units1, stream)) != cudaSuccess) return e;
   lmhead_select_kernel<<<p.M, kSelThreads, ssmem, stream>>>(p);
   return cudaGetLastError();
 }
