@@ -514,7 +514,7 @@ int32_t dspark_lmhead_topk(const dspark_lmhead_args* a, dspark_stream_t stream) 
   p.sample = reinterpret_cast<float*>(ws);
   p.pivot = reinterpret_cast<uint32_t*>(ws + lm_ws_sample(a->M, a->V));
   p.cnt = reinterpret_cast<uint32_t*>(ws + lm_ws_sample(a->M, a->V) + lm_align(4ull * a->M));
-  p.list = reinterpret_cast<uint64_t*>(ws + lm_ws_sample(a->M, a->V) + 2 * lm_align(4ull * a->M));
+  p.list = reinterpret_cast<uint64_t*>(ws + lm_ws_sample(a->M, a->V) + lm_align(4ull * a->M) + lm_ws_cnt(a->M));
   p.cand = a->cand;
   p.cand_base = a->cand_base;
   p.stats = a->stats_dev;

@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_gemm_kernel(const __grid
         uint32_t pos[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          if (i < nq) pos[i] = atomicAdd(p.cnt + m0 + static_cast<int>(e[i] >> 32), 1u);
+          if (i < nq) pos[i] = atomicAdd(p.cnt + static_cast<size_t>(m0 + static_cast<int>(e[i] >> 32)) * kLmCntStride, 1u);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           if (i < nq && pos[i] < static_cast<uint32_t>(p.cap))
@@ -475,6 +475,73 @@ __device__ __forceinline__ void pick_bin(const int* hist, int above, int rank, i
   }
 }
 
+__device__ __forceinline__ uint64_t shfl_xor64(uint64_t v, int m) {
+  const uint32_t lo = __shfl_xor_sync(kFull, static_cast<uint32_t>(v), m);
+  const uint32_t hi = __shfl_xor_sync(kFull, static_cast<uint32_t>(v >> 32), m);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+__device__ __forceinline__ int high_bit(uint64_t x) { return 63 - __clzll(static_cast<long long>(x)); }
+
+// Block-wide radix selection over the n words (uint32_t or uint64_t) in shared memory:
+// returns T with at least `rank` words >= T and, when the words are distinct, exactly
+// `rank`. The digits start at the highest bit where the smallest and largest word differ
+// (the bits above are common to all words and need no pass), eight bits a pass, and the
+// selection stops as soon as a bin holds exactly the words still needed. `hist` [256],
+// `sel` [3] and `mm` [2] are shared scratch; every thread of the block calls it.
+template <typename W>
+__device__ W block_select(const W* words, int n, int rank, int* hist, int* sel, unsigned long long* mm) {
+  constexpr int kBits = 8 * sizeof(W);
+  uint64_t lo = ~0ull, hi = 0ull;
+  for (int t = threadIdx.x; t < n; t += blockDim.x) {
+    const uint64_t w = words[t];
+    lo = w < lo ? w : lo;
+    hi = w > hi ? w : hi;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t a = shfl_xor64(lo, o), b = shfl_xor64(hi, o);
+    lo = a < lo ? a : lo;
+    hi = b > hi ? b : hi;
+  }
+  if (threadIdx.x == 0) { mm[0] = ~0ull; mm[1] = 0ull; }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) {
+    atomicMin(&mm[0], static_cast<unsigned long long>(lo));
+    atomicMax(&mm[1], static_cast<unsigned long long>(hi));
+  }
+  __syncthreads();
+  lo = mm[0];
+  hi = mm[1];
+  __syncthreads();
+  if (lo == hi) return static_cast<W>(lo);
+  int top = high_bit(lo ^ hi);                  // highest bit that differs
+  uint64_t prefix = top + 1 < kBits ? (lo >> (top + 1)) : 0ull;  // common bits above it
+  int above = 0, low = 0;
+  while (top >= 0) {
+    low = top >= 7 ? top - 7 : 0;
+    const int width = top - low + 1;
+    const uint64_t mask = (1ull << width) - 1ull;
+    for (int t = threadIdx.x; t < 256; t += blockDim.x) hist[t] = 0;
+    if (threadIdx.x == 0) { sel[0] = 0; sel[1] = above; sel[2] = 1; }
+    __syncthreads();
+    for (int t = threadIdx.x; t < n; t += blockDim.x) {
+      const uint64_t w = words[t];
+      const uint64_t up = top + 1 < kBits ? (w >> (top + 1)) : 0ull;
+      if (up == prefix) atomicAdd(&hist[static_cast<int>((w >> low) & mask)], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) pick_bin(hist, above, rank, sel);
+    __syncthreads();
+    prefix = (prefix << width) | static_cast<uint64_t>(sel[0]);
+    above = sel[1];
+    const bool done = sel[2] != 0;
+    __syncthreads();
+    if (done) break;
+    top = low - 1;
+  }
+  return static_cast<W>(prefix << low);
+}
+
 // fp32 dot product of hidden row m and LM-head row v on CUDA cores (fixed order).
 __device__ __forceinline__ float dot_row(const LmParams& p, int m, int64_t v) {
   const uint4* h = reinterpret_cast<const uint4*>(p.hidden + static_cast<size_t>(m) * p.d);
@@ -494,76 +561,56 @@ __device__ __forceinline__ float dot_row(const LmParams& p, int m, int64_t v) {
 
 }  // namespace
 
-// Per hidden row: the pivot P, the largest key with at least j of the row's sampled keys
-// at or above it, resolved to its top kPivotBits bits (one CTA per row). Bitwise binary
-// search: starting from P = 0, each step sets the next bit when the sampled keys at or
-// above the candidate still number j or more (a count by every thread over its keys, a
-// warp sum and one shared-memory add per warp). At least j sampled keys are >= P; the
-// low bits left at zero let a few more through (those sharing P's top bits), which the
-// list capacity absorbs. The row's list counter is zeroed. Keys are staged in shared
-// memory when they fit (kPivotSmemKeys), else re-read from the sample rows.
+// Per hidden row: the pivot P, a key with at least j of the row's sampled keys at or
+// above it (the j-th largest, or the lower edge of a radix bin holding exactly the keys
+// still needed), by a block radix selection over the keys staged in shared memory (one
+// CTA per row); the row's list counter is zeroed. Rows of more than kPivotSmemKeys
+// samples use their first kPivotSmemKeys with j scaled alike (the pivot only steers the
+// list's size; the list itself is exact).
 constexpr int kPivotSmemKeys = 40960;
-constexpr int kPivotBits = 20;
 
 __global__ void __launch_bounds__(kSelThreads) lmhead_pivot_kernel(const LmParams p, int j) {
   extern __shared__ __align__(16) uint32_t keys_s[];
-  __shared__ int count[2];
+  __shared__ int hist[256];
+  __shared__ int sel[3];
+  __shared__ unsigned long long mm[2];
   const int m = blockIdx.x;
   const float* x = p.sample + static_cast<size_t>(m) * p.S;
-  const bool staged = p.S <= kPivotSmemKeys;
-  if (staged) {
-    for (int s0 = threadIdx.x; s0 < p.S; s0 += 8 * blockDim.x) {
-      float xv[8];
+  const int n = p.S < kPivotSmemKeys ? p.S : kPivotSmemKeys;
+  int rank = n == p.S ? j : static_cast<int>((static_cast<int64_t>(j) * n) / p.S);
+  rank = rank < 1 ? 1 : (rank > n ? n : rank);
+  for (int s0 = threadIdx.x; s0 < n; s0 += 8 * blockDim.x) {
+    float xv[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int s = s0 + i * blockDim.x;
-        xv[i] = s < p.S ? x[s] : 0.f;
-      }
+    for (int i = 0; i < 8; ++i) {
+      const int s = s0 + i * blockDim.x;
+      xv[i] = s < n ? x[s] : 0.f;
+    }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int s = s0 + i * blockDim.x;
-        if (s < p.S) keys_s[s] = order_key(xv[i]);
-      }
+    for (int i = 0; i < 8; ++i) {
+      const int s = s0 + i * blockDim.x;
+      if (s < n) keys_s[s] = order_key(xv[i]);
     }
   }
-  if (threadIdx.x < 2) count[threadIdx.x] = 0;
   __syncthreads();
-  uint32_t P = 0;
-  for (int b = 31; b >= 32 - kPivotBits; --b) {
-    const uint32_t cand = P | (1u << b);
-    int c = 0;
-    if (staged) {
-      for (int s = threadIdx.x; s < p.S; s += blockDim.x) c += keys_s[s] >= cand ? 1 : 0;
-    } else {
-      for (int s = threadIdx.x; s < p.S; s += blockDim.x) c += order_key(x[s]) >= cand ? 1 : 0;
-    }
-    c = __reduce_add_sync(kFull, c);
-    const int slot = b & 1;  // alternate counters: one is cleared while the other is summed
-    if ((threadIdx.x & 31) == 0) atomicAdd(&count[slot], c);
-    __syncthreads();
-    const int tot = count[slot];
-    if (threadIdx.x == 0) count[slot ^ 1] = 0;
-    if (tot >= j) P = cand;
-    __syncthreads();
-  }
+  const uint32_t P = block_select<uint32_t>(keys_s, n, rank, hist, sel, mm);
   if (threadIdx.x == 0) {
     p.pivot[m] = P;
-    p.cnt[m] = 0u;
+    p.cnt[static_cast<size_t>(m) * kLmCntStride] = 0u;
   }
 }
 
-// Per hidden row: the k largest packed words of its list (one CTA per row, the list in
-// shared memory, radix selection over eight bytes), or the exact path over the whole
-// row when the list is short, overflowed or the fallback is forced.
+// Per hidden row: the k largest packed words of its list (one CTA per row, the list read
+// from L2, block radix selection), or the exact path over the whole row when the list is
+// short, overflowed or the fallback is forced.
 __global__ void __launch_bounds__(kSelThreads) lmhead_select_kernel(const LmParams p) {
-  extern __shared__ __align__(1024) unsigned char sel_raw[];
-  uint64_t* words = reinterpret_cast<uint64_t*>(sel_raw);             // [cap]
   __shared__ int hist[256];
   __shared__ int sel[3];
+  __shared__ unsigned long long mm[2];
   __shared__ int outpos;
   const int m = blockIdx.x;
   const int k = p.k;
-  const uint32_t n_all = p.cnt[m];
+  const uint32_t n_all = p.cnt[static_cast<size_t>(m) * kLmCntStride];
   const bool exact = (p.flags & kLmForceExact) || n_all < static_cast<uint32_t>(k) ||
                      n_all > static_cast<uint32_t>(p.cap);
   int32_t* cand = p.cand + static_cast<size_t>(m) * k;
@@ -571,34 +618,20 @@ __global__ void __launch_bounds__(kSelThreads) lmhead_select_kernel(const LmPara
   if (threadIdx.x == 0) outpos = 0;
   if (!exact) {
     const int n = static_cast<int>(n_all);
-    for (int t = threadIdx.x; t < n; t += blockDim.x) words[t] = p.list[static_cast<size_t>(m) * p.cap + t];
-    __syncthreads();
-    uint64_t prefix = 0;
-    int above = 0, sh = 0;
-    for (int pass = 0; pass < 8; ++pass) {
-      sh = 56 - 8 * pass;
-      for (int t = threadIdx.x; t < 256; t += blockDim.x) hist[t] = 0;
-      if (threadIdx.x == 0) { sel[0] = 0; sel[1] = above; sel[2] = 1; }
-      __syncthreads();
-      for (int t = threadIdx.x; t < n; t += blockDim.x) {
-        const uint64_t w = words[t];
-        if (pass == 0 || (w >> (sh + 8)) == prefix) atomicAdd(&hist[(w >> sh) & 0xFFu], 1);
-      }
-      __syncthreads();
-      if (threadIdx.x < 32) pick_bin(hist, above, k, sel);
-      __syncthreads();
-      prefix = (prefix << 8) | static_cast<uint64_t>(sel[0]);
-      above = sel[1];
-      const bool done = sel[2] != 0;
-      __syncthreads();
-      if (done) break;
-    }
-    // words are distinct (one per vocabulary entry): exactly k are >= the threshold
-    const uint64_t thr = prefix << sh;
-    for (int t = threadIdx.x; t < n; t += blockDim.x) {
-      const uint64_t w = words[t];
-      if (w >= thr) {
-        const int pos = atomicAdd(&outpos, 1);
+    const uint64_t* words = p.list + static_cast<size_t>(m) * p.cap;  // read where the filter pass left them (L2)
+    const uint64_t thr = block_select<uint64_t>(words, n, k, hist, sel, mm);
+    // words are distinct (one per vocabulary entry): exactly k are >= the threshold,
+    // written in list order (positions by a warp ballot and one shared add per warp)
+    for (int t0 = threadIdx.x & ~31; t0 < n; t0 += blockDim.x) {
+      const int t = t0 + (threadIdx.x & 31);
+      const uint64_t w = t < n ? words[t] : 0ull;
+      const bool take = t < n && w >= thr;
+      const uint32_t ball = __ballot_sync(kFull, take);
+      int base = 0;
+      if ((threadIdx.x & 31) == 0 && ball) base = atomicAdd(&outpos, __popc(ball));
+      base = __shfl_sync(kFull, base, 0);
+      if (take) {
+        const int pos = base + __popc(ball & ((1u << (threadIdx.x & 31)) - 1u));
         cand[pos] = unpack_idx(w);
         cbase[pos] = key_value(static_cast<uint32_t>(w >> 32));
       }
@@ -666,7 +699,6 @@ __global__ void __launch_bounds__(kSelThreads) lmhead_select_kernel(const LmPara
   }
 }
 
-size_t lmhead_select_smem(int cap) { return static_cast<size_t>(cap) * 8; }
 
 namespace {
 
@@ -706,10 +738,7 @@ cudaError_t launch_gemm(LmParams& p, int sms, size_t smem, int units, cudaStream
 cudaError_t launch_lmhead(LmParams& p, int sms, int pivot_rank, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(lm_gemm_smem(p.M));
   cudaError_t e;
-  const size_t ssmem = lmhead_select_smem(p.cap);
-  if ((e = cudaFuncSetAttribute(lmhead_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssmem))) != cudaSuccess)
-    return e;
-  const size_t psmem = p.S <= kPivotSmemKeys ? static_cast<size_t>(p.S) * 4 : 0;
+  const size_t psmem = static_cast<size_t>(std::min(p.S, kPivotSmemKeys)) * 4;
   if ((e = cudaFuncSetAttribute(lmhead_pivot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kPivotSmemKeys * 4)) != cudaSuccess)
     return e;
@@ -729,7 +758,7 @@ cudaError_t launch_lmhead(LmParams& p, int sms, int pivot_rank, cudaStream_t str
   lmhead_pivot_kernel<<<p.M, kSelThreads, psmem, stream>>>(p, pivot_rank);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = launch_gemm<1>(p, sms, smem, units1, stream)) != cudaSuccess) return e;
-  lmhead_select_kernel<<<p.M, kSelThreads, ssmem, stream>>>(p);
+  lmhead_select_kernel<<<p.M, kSelThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -51,7 +51,7 @@ struct LmParams {
   int32_t cap;               // list capacity per hidden row
   float* sample;             // [M, S] sampled logits
   uint32_t* pivot;           // [M] pivot keys
-  uint32_t* cnt;             // [M] list lengths
+  uint32_t* cnt;             // [M] list lengths, at cnt[m * kLmCntStride]
   uint64_t* list;            // [M, cap] packed {key, 2^32-1-v}
   int32_t* cand;             // out [M, k] candidate vocabulary ids
   float* cand_base;          // out [M, k] their logits
@@ -74,8 +74,12 @@ __host__ __device__ inline int32_t lm_samples(int64_t V) {
 __host__ __device__ inline int32_t lm_cap(int32_t k) { return 3 * k + 1024; }
 __host__ __device__ inline size_t lm_align(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 __host__ __device__ inline size_t lm_ws_sample(int32_t M, int64_t V) { return lm_align(4ull * M * lm_samples(V)); }
+// List counters: one per hidden row, each on its own 128-byte line (the filter pass's
+// appends to different rows do not queue behind one another in L2).
+constexpr int kLmCntStride = 32;
+__host__ __device__ inline size_t lm_ws_cnt(int32_t M) { return lm_align(4ull * kLmCntStride * M); }
 __host__ __device__ inline size_t lm_ws_total(int32_t M, int64_t V, int32_t k) {
-  return lm_ws_sample(M, V) + 2 * lm_align(4ull * M) + lm_align(8ull * M * lm_cap(k));
+  return lm_ws_sample(M, V) + lm_align(4ull * M) + lm_ws_cnt(M) + lm_align(8ull * M * lm_cap(k));
 }
 
 }  // namespace dspark
