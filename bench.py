@@ -145,6 +145,21 @@ def floors(cfg, peaks, sms: int, resident_rows: int, l2_gbs: float):
     return out
 
 
+# One grid-wide exchange of the walk (every CTA's packed atomicMax, the arrival counter,
+# the acquire polling until all 152 CTAs have arrived): ~1.4 us, measured on this GPU with
+# a probe kernel doing only that exchange, back to back.
+GRID_EXCHANGE_US = 1.4
+
+
+def chain_floor_us(cfg, fl) -> float:
+    """Informational latency floor of the walk: position i + 1's contraction needs
+    position i's winner, so the K grid exchanges and the contraction are serial; this is
+    K exchanges plus the contraction floor (the top-k walk: K exchanges plus its L2 and
+    FMA floors' larger). Not part of the roofline (a chain of latencies, not a resource)."""
+    work = max(v for k, v in fl.items() if k in ("tensor_us", "fma_us", "l2_us" if cfg["top_k"] else "tensor_us"))
+    return cfg["K"] * GRID_EXCHANGE_US + work
+
+
 def gumbel_floor_us(cfg, peaks, sms: int) -> float | None:
     """Informational floor of the Gumbel draws of a sampled walk (None when greedy)."""
     if cfg["mode"] != 1:
@@ -690,7 +705,8 @@ def main():
     floor_rec = {k: round(v, 3) for k, v in fl.items()}
     floor_rec.update({"floor_us": round(floor_us, 3), "frac_of_floor": floor_us / us,
                       "resident_w2_rows": res_rows, "l2_gbs_live": round(l2_gbs, 1),
-                      "hbm_bytes": hbm_bytes(cfg), "gumbel_us_informational": gumbel_floor_us(cfg, peaks, sms)})
+                      "hbm_bytes": hbm_bytes(cfg), "gumbel_us_informational": gumbel_floor_us(cfg, peaks, sms),
+                      "chain_us_informational": round(chain_floor_us(cfg, fl), 3)})
 
     variants = []
     if not a.no_variants:
@@ -710,7 +726,8 @@ def main():
                              "floor_us": vfloor, "frac_of_floor": vfloor / vus,
                              "bound": vr["bound"], "frac": vr["frac"],
                              "floors_us": {k: round(v, 3) for k, v in vfl.items()},
-                             "gumbel_us_informational": gumbel_floor_us(vc, peaks, sms)})
+                             "gumbel_us_informational": gumbel_floor_us(vc, peaks, sms),
+                             "chain_us_informational": round(chain_floor_us(vc, vfl), 3)})
 
     cpu = None
     if rank == 0 and not a.no_cpu_baseline:

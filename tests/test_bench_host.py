@@ -93,3 +93,16 @@ def test_reference_arm_prints_one_contract_line():
     assert d["config"]["workload"] == bench.MAIN["name"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_chain_floor_adds_the_grid_exchanges_to_the_contraction():
+    """K serial grid exchanges plus the contraction floor (informational)."""
+    cfg = dict(bench.MAIN, bs=1)
+    fl = bench.floors(cfg, PEAKS, sms=152, resident_rows=150_000, l2_gbs=20_000.0)
+    assert bench.chain_floor_us(cfg, fl) == pytest.approx(7 * bench.GRID_EXCHANGE_US + fl["fma_us"])
+    tc = dict(bench.MAIN)
+    fl = bench.floors(tc, PEAKS, sms=152, resident_rows=100_000, l2_gbs=20_000.0)
+    assert bench.chain_floor_us(tc, fl) == pytest.approx(7 * bench.GRID_EXCHANGE_US + fl["tensor_us"])
+    tk = dict(bench.MAIN, top_k=4096, int8=False, mode=1)
+    fl = bench.floors(tk, PEAKS, sms=152, resident_rows=0, l2_gbs=8_000.0)
+    assert bench.chain_floor_us(tk, fl) == pytest.approx(7 * bench.GRID_EXCHANGE_US + max(fl["l2_us"], fl["fma_us"]))
