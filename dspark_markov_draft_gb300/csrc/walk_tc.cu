@@ -11,25 +11,32 @@
 // and their load latency falls in the window of the grid exchange, when the tensor
 // cores wait for the next tokens anyway.
 //
-// Warp roles (21 warps):
+// Warp roles (24 warps; setmaxnreg moves registers from the producers and the issue
+// warps to the epilogue, a split checked on the host against the launch's registers):
 //   * warps 0-3, producers: warp q fills tensor-memory lanes 32q..32q+31 of each tile's
 //     A operand; a thread converts one W2 row (int8 codes become exact fp16 integers
 //     through a byte permute with 0x64 exponent bytes and one packed subtract; bf16 rows
-//     are copied). A does not depend on the tokens, so the producers run ahead across
-//     positions, limited only by the two A buffers.
+//     are copied). Streamed rows are read from L2 with an evict-last hint, resident rows
+//     from the swizzled shared-memory copy. A does not depend on the tokens, so the
+//     producers run ahead across positions, limited only by the three A buffers.
 //   * warps 4-19, epilogue: warp 4 + 4c + q reads tensor-memory lanes 32q.. (warp % 4 ==
 //     q) and the N/4 request columns of column group c. Thread = one vocabulary row of
-//     the tile: it adds the base logit (loaded from global memory one tile ahead) to
+//     the tile: it adds the base logit (from the staged copy of the tile) to
 //     scale_v 2^-s D, scores the entry (greedy: l; probabilistic: bf16(l)/T plus Gumbel
 //     noise whose Philox blocks are drawn once per lane quad and exchanged by a 4 x 4
 //     transpose), and keeps per column the running maximum and the tile where it was
 //     first reached. At the end of a position the same warps reduce the columns, run
 //     the grid exchange, gather the next embeddings and build the next B operand.
-//   * warp 20, MMA issue: lane 0 issues the 16 MMAs (M = 128, N, K = 16, A in tensor
-//     memory, B in shared memory) of each tile into one of four D buffers, in K order.
-// Producers, issuer and epilogue hand tiles over through mbarriers (two A buffers, four
-// D buffers, one B-ready barrier per position). Every wait is bounded by wall-clock
-// time and watches a CTA fail flag, so a timeout anywhere ends every role.
+//   * warps 20 and 21, MMA issue: they take alternate tiles; lane 0 issues the 16 MMAs
+//     (M = 128, N, K = 16, A in tensor memory, B in shared memory) of a tile into one of
+//     the D buffers, in K order.
+//   * warp 22, base-logit copies: tensor-map copies of each tile's base logits for all
+//     request columns into a ring of stages, running ahead of the epilogue across
+//     positions (the next position's boxes are prefetched to L2).
+// Producers, issuers, copier and epilogue hand tiles over through mbarriers (three A
+// buffers, two or four D buffers, the base stages, one B-ready barrier per position).
+// Every wait is bounded by wall-clock time and watches a CTA fail flag, so a timeout
+// anywhere ends every role.
 #include <cstdint>
 #include <cuda_fp16.h>
 #include <type_traits>
