@@ -520,7 +520,6 @@ int32_t dspark_lmhead_topk(const dspark_lmhead_args* a, dspark_stream_t stream) 
   p.stats = a->stats_dev;
   p.status_dev = a->status_dev;
   p.flags = (a->flags & DSPARK_LMHEAD_FLAG_EXACT) ? kLmForceExact : 0;
-  p.cluster = kLmCluster;
   p.timeout_ns = 1000ull * (a->timeout_us ? a->timeout_us : 1000000u);
   auto map2d = [&](CUtensorMap* m, const void* ptr, cuuint64_t inner, cuuint64_t rows, cuuint64_t stride_bytes,
                    cuuint32_t box_rows) {

@@ -52,24 +52,32 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   d |= static_cast<uint64_t>(2) << 61;
   return d;
 }
-// kind::f16 instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, M = 128.
-__host__ __device__ constexpr uint32_t bf16_idesc(int N) {
+// kind::f16 instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, M x N.
+__host__ __device__ constexpr uint32_t bf16_idesc(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(kLmTile >> 4) << 24);
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
+// CLUSTER: acquire at cluster scope (arrivals that come from the other CTA of the pair).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try(uint64_t* mbar, uint32_t parity) {
   uint32_t done;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-      : "=r"(done) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
+  if (CLUSTER)
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
+  else
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
   return done != 0;
 }
 // Bounded wait; on timeout sets the CTA fail flag and reports DSPARK_ERR_TIMEOUT.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, const LmParams& p, volatile int* fail) {
-  if (mbar_try(mbar, parity)) return true;
+  if (mbar_try<CLUSTER>(mbar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try(mbar, parity)) return true;
+    if (mbar_try<CLUSTER>(mbar, parity)) return true;
     if ((it & 15u) == 0u) {
       if (*fail) return false;
       if (globaltimer_ns() - t0 > p.timeout_ns) {
@@ -79,9 +87,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, const
       }
     }
   }
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(mbar)) : "memory");
 }
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -98,45 +103,40 @@ __device__ __forceinline__ uint32_t cluster_count() {
   asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
   return r;
 }
-// Every thread of every CTA of the cluster (a launch without clusters is a cluster of one).
+// Every thread of both CTAs of the pair.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Tensor-map copy of one 2-D box into this CTA's shared memory (leader lane only).
-__device__ __forceinline__ void tma_2d_if(uint32_t leader, void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "{ .reg .pred q; setp.ne.b32 q, %5, 0; "
-      "@q cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4]; }"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "r"(leader)
-      : "memory");
+// Shared-memory address of `p`'s counterpart in the pair's CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
 }
-// The same box written to the same offsets in every CTA of `mask`, each CTA's barrier at
-// `bar`'s offset receiving the bytes.
-__device__ __forceinline__ void tma_2d_mc_if(uint32_t leader, void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                             uint16_t mask) {
+// Tensor-map copy of one 2-D box into this CTA's shared memory, its bytes counted on a
+// barrier of either CTA of the pair (`bar`: shared::cluster address); leader lane only.
+__device__ __forceinline__ void tma_2d_pair_if(uint32_t leader, void* dst, const CUtensorMap* map, int x, int y,
+                                               uint32_t bar) {
   asm volatile(
       "{ .reg .pred q; setp.ne.b32 q, %5, 0; "
-      "@q cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%2, %3}], [%4], %6; }"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "r"(leader),
-        "h"(mask)
+      "@q cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 "
+      "[%0], [%1, {%2, %3}], [%4]; }"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "r"(leader)
       : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_2d_if(uint32_t leader, const CUtensorMap* map, int x, int y) {
   asm volatile("{ .reg .pred q; setp.ne.b32 q, %3, 0; @q cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}]; }"
                ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(leader) : "memory");
 }
-// Arrive on `bar` once the MMAs issued so far complete: in this CTA only, or at the same
-// offset in every CTA of `mask`.
-__device__ __forceinline__ void mma_commit_if(uint32_t leader, uint64_t* bar) {
+// Arrive on `bar` in both CTAs of the pair once the paired MMAs issued so far complete.
+__device__ __forceinline__ void mma_commit_pair_if(uint32_t leader, uint64_t* bar) {
   asm volatile("{ .reg .pred q; setp.ne.b32 q, %1, 0; "
-               "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0]; }"
-               ::"r"(smem_u32(bar)), "r"(leader) : "memory");
+               "@q tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %2; }"
+               ::"r"(smem_u32(bar)), "r"(leader), "h"(static_cast<uint16_t>(3)) : "memory");
 }
-__device__ __forceinline__ void mma_commit_mc_if(uint32_t leader, uint64_t* bar, uint16_t mask) {
-  asm volatile("{ .reg .pred q; setp.ne.b32 q, %1, 0; "
-               "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %2; }"
-               ::"r"(smem_u32(bar)), "r"(leader), "h"(mask) : "memory");
+// Arrive on a barrier of either CTA of the pair (`bar`: shared::cluster address).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // Inverse of order_key (the key of -0 is the key of +0: it returns +0).
@@ -175,68 +175,70 @@ __device__ __forceinline__ LmUnit lm_unit(const LmParams& p, int u, int mchunks,
 // MODE 0: sample pass (rows r * stride of the LM head, logits stored); MODE 1: filter
 // pass (every row, logits at or above the row's pivot appended to its list).
 //
-// Clusters of p.cluster CTAs share the hidden-row chunks: CTA rank c of a cluster copies
-// the 32-row boxes b with b % cluster == c, multicast to every CTA of the cluster, and a
-// stage is refilled only after the MMAs of every CTA of the cluster have read it (each
-// CTA's commit arrives on the stage's empty barrier in all of them). The CTAs of a
-// cluster walk the same sequence of hidden-row chunks; each has its own LM-head tile.
+// Launched as clusters of two CTAs that run one MMA of M = 256 together (tcgen05
+// cta_group::2): CTA rank c of the pair stages its own 128-row LM-head tile (A rows
+// 128c..) and half of each hidden-row part (B split along N), and its tensor memory
+// receives its tile's 128 x N accumulators. Rank 0 issues the MMAs; both CTAs' copies
+// count their bytes on rank 0's stage barrier, rank 0's commits release the stage in
+// both CTAs, and both CTAs' epilogue warps release the accumulator on rank 0's barrier.
 template <int MODE>
 __global__ void __launch_bounds__(kLmThreads, 1) lmhead_gemm_kernel(const __grid_constant__ LmParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int NS = lm_stages(p.M);
   const uint32_t stage_bytes = static_cast<uint32_t>(lm_stage_bytes(p.M));
+  const int h0 = lm_box0(p.M), h1 = lm_box1(p.M);  // hidden rows per CTA in parts 0 and 1
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + NS * stage_bytes);
-  uint64_t* full = mbar;                     // [NS] 1 arrival + bytes
-  uint64_t* empty = mbar + NS;               // [NS] one commit from each CTA of the cluster
-  uint64_t* dfull = mbar + 2 * NS;           // 1 commit
-  uint64_t* dempty = mbar + 2 * NS + 1;      // kLmEpiWarps arrivals
+  uint64_t* full = mbar;                     // [NS] rank 0: 1 arrival + both CTAs' bytes
+  uint64_t* empty = mbar + NS;               // [NS] 1 commit (multicast by rank 0)
+  uint64_t* dfull = mbar + 2 * NS;           // 1 commit (multicast by rank 0)
+  uint64_t* dempty = mbar + 2 * NS + 1;      // rank 0: the epilogue warps of both CTAs
   uint32_t* tbase_s = reinterpret_cast<uint32_t*>(mbar + 2 * kLmMaxStages + 2);
   volatile int* fail = reinterpret_cast<volatile int*>(tbase_s + 1);
   float* thr_s = reinterpret_cast<float*>(smem + NS * stage_bytes + 128);  // [epilogue warp][4 x 32]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int C = p.cluster;
-  const int crank = C > 1 ? static_cast<int>(cluster_rank()) : 0;
-  const int cid = C > 1 ? static_cast<int>(cluster_id()) : static_cast<int>(blockIdx.x);
-  const int ncl = C > 1 ? static_cast<int>(cluster_count()) : static_cast<int>(gridDim.x);
-  const uint16_t cmask = static_cast<uint16_t>((1u << C) - 1u);
+  const int crank = static_cast<int>(cluster_rank());
+  const bool lead = crank == 0;
+  const int cid = static_cast<int>(cluster_id());
+  const int ncl = static_cast<int>(cluster_count());
   const int64_t rows = MODE == 0 ? p.S : p.V;                       // LM-head rows of this pass
   const int tiles = static_cast<int>((rows + kLmTile - 1) / kLmTile);
-  const int groups = (tiles + C - 1) / C;                           // tiles of one cluster step
+  const int groups = (tiles + 1) / 2;                               // tile pairs
   const int mchunks = (p.M + 511) / 512;
-  const int units = groups * mchunks * p.ksplit;                    // per cluster
+  const int units = groups * mchunks * p.ksplit;                    // per pair
   const int nk = p.d / kLmChunk;
 
   if (tid == 0) {
     for (int b = 0; b < 2 * NS + 2; ++b) {
-      const uint32_t cnt = b == 2 * NS + 1 ? static_cast<uint32_t>(kLmEpiWarps)
-                                           : (b >= NS && b < 2 * NS ? static_cast<uint32_t>(C) : 1u);
+      const uint32_t cnt = b == 2 * NS + 1 ? static_cast<uint32_t>(2 * kLmEpiWarps) : 1u;
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&mbar[b])), "r"(cnt));
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *fail = 0;
   }
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+  if (warp == 0) {  // one warp of each CTA of the pair allocates, together
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
                  ::"r"(smem_u32(tbase_s)), "r"(kLmTmemCols) : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  cluster_sync();  // every CTA's barriers are initialised before any copy lands in it
+  cluster_sync();  // both CTAs' barriers are initialised before any copy or arrival lands in them
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tbase_s;
   const CUtensorMap* amap = MODE == 0 ? &p.ws_map : &p.w_map;
+  const uint32_t full0 = peer_addr(full, 0);      // rank 0's full[0]; full[s] is 8 s further
+  const uint32_t dempty0 = peer_addr(dempty, 0);  // rank 0's dempty
 
   if (warp == 0) {
     // ------------------------------------------------------------ tensor-map copies
     const uint32_t leader = lane == 0;
+    const uint32_t bytes = 2 * kLmAStageBytes + 2 * 128 * (h0 + h1);  // both CTAs' boxes
     int g = 0;  // global chunk counter
     for (int u = cid; u < units && !__any_sync(kFull, *fail); u += ncl) {
-      const LmUnit w = lm_unit(p, u, mchunks, C, crank, nk);
+      const LmUnit w = lm_unit(p, u, mchunks, 2, crank, nk);
       const int tile = w.tile, m0 = w.m0;
-      const uint32_t bytes = kLmAStageBytes + lm_b_rows(p.M) * 128;  // both boxes, rows past M filled
       // the first chunks of this tile go to L2 now (the rest are prefetched as it runs)
       const uint32_t pf = leader && static_cast<int64_t>(tile) * kLmTile < rows;  // tile holds rows
       for (int kc = w.kbeg; kc < min(w.kend, w.kbeg + NS); ++kc) tma_prefetch_2d_if(pf, amap, kc * kLmChunk, tile * kLmTile);
@@ -246,82 +248,74 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_gemm_kernel(const __grid
         if (g >= NS && (ok = !__any_sync(kFull, !mbar_wait(&empty[s], ((g / NS) - 1) & 1, p, fail))) == false) break;
         if (kc + NS < w.kend) tma_prefetch_2d_if(pf, amap, (kc + NS) * kLmChunk, tile * kLmTile);
         unsigned char* st = smem + s * stage_bytes;
-        asm volatile(
-            "{ .reg .pred q; setp.ne.b32 q, %2, 0; @q mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1; }"
-            ::"r"(smem_u32(&full[s])), "r"(bytes), "r"(leader) : "memory");
-        tma_2d_if(leader, st, amap, kc * kLmChunk, tile * kLmTile, &full[s]);
-        // box 0 from cluster rank 0, box 1 from rank 1 (or 0 without a cluster)
-        const int nbox = lm_box1(p.M) > 0 ? 2 : 1;
-        for (int b = crank; b < nbox; b += C) {
-          unsigned char* dst = st + kLmAStageBytes + b * 256 * 128;
-          const CUtensorMap* hm = b == 0 ? &p.h_map0 : &p.h_map1;
-          if (C > 1)
-            tma_2d_mc_if(leader, dst, hm, kc * kLmChunk, m0 + 256 * b, &full[s], cmask);
-          else
-            tma_2d_if(leader, dst, hm, kc * kLmChunk, m0 + 256 * b, &full[s]);
-        }
+        const uint32_t bar = full0 + 8u * static_cast<uint32_t>(s);
+        if (lead)
+          asm volatile(
+              "{ .reg .pred q; setp.ne.b32 q, %2, 0; @q mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1; }"
+              ::"r"(smem_u32(&full[s])), "r"(bytes), "r"(leader) : "memory");
+        tma_2d_pair_if(leader, st, amap, kc * kLmChunk, tile * kLmTile, bar);
+        tma_2d_pair_if(leader, st + kLmAStageBytes, &p.h_map0, kc * kLmChunk, m0 + crank * h0, bar);
+        if (h1 > 0)
+          tma_2d_pair_if(leader, st + kLmAStageBytes + h0 * 128, &p.h_map1, kc * kLmChunk, m0 + 256 + crank * h1, bar);
       }
       if (!ok) break;
     }
-    // copies still in flight land before the CTA leaves (bounded)
+    // the last stages were consumed (so their copies landed) before the CTA leaves (bounded)
     for (int s = 0; s < NS; ++s) {
       if (g - 1 - s < 0) continue;
       const int gl = g - 1 - s;
       const uint64_t t0 = globaltimer_ns();
-      while (!__all_sync(kFull, mbar_try(&full[gl % NS], (gl / NS) & 1)) &&
+      while (!__all_sync(kFull, mbar_try(&empty[gl % NS], (gl / NS) & 1)) &&
              !__any_sync(kFull, globaltimer_ns() - t0 >= p.timeout_ns)) {}
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issue
+    // ------------------------------------------------------------ MMA issue (rank 0)
     const uint32_t leader = lane == 0;
+    const int n0 = 2 * h0, n1 = 2 * h1;
     int g = 0, un = 0, last = -1;
-    for (int u = cid; u < units && !__any_sync(kFull, *fail); u += ncl, ++un) {
-      const LmUnit w = lm_unit(p, u, mchunks, C, crank, nk);
-      const int mrows = w.mrows;
-      const int n0 = (min(256, mrows) + 15) & ~15;
-      const int n1 = mrows > 256 ? ((mrows - 256 + 15) & ~15) : 0;
-      if (un >= 1 && __any_sync(kFull, !mbar_wait(dempty, (un - 1) & 1, p, fail))) break;
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      bool ok = true;
-      for (int kc = w.kbeg; kc < w.kend; ++kc, ++g) {
-        const int s = g % NS;
-        if (__any_sync(kFull, !mbar_wait(&full[s], (g / NS) & 1, p, fail))) { ok = false; break; }
+    if (lead) {
+      for (int u = cid; u < units && !__any_sync(kFull, *fail); u += ncl, ++un) {
+        const LmUnit w = lm_unit(p, u, mchunks, 2, crank, nk);
+        if (un >= 1 && __any_sync(kFull, !mbar_wait<true>(dempty, (un - 1) & 1, p, fail))) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t a0 = smem_u32(smem + s * stage_bytes), b0 = a0 + kLmAStageBytes;
+        bool ok = true;
+        for (int kc = w.kbeg; kc < w.kend; ++kc, ++g) {
+          const int s = g % NS;
+          if (__any_sync(kFull, !mbar_wait(&full[s], (g / NS) & 1, p, fail))) { ok = false; break; }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t a0 = smem_u32(smem + s * stage_bytes), b0 = a0 + kLmAStageBytes;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = sw128_desc(a0 + kk * 32);
-          const uint32_t acc = (kc > w.kbeg || kk > 0) ? 1u : 0u;
-          for (int part = 0; part < 2; ++part) {
-            const int np = part == 0 ? n0 : n1;
-            if (np == 0) continue;
-            const uint64_t bd = sw128_desc(b0 + part * 256 * 128 + kk * 32);
-            asm volatile(
-                "{ .reg .pred p, q; setp.ne.b32 p, %4, 0; setp.ne.b32 q, %5, 0; "
-                "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
-                ::"r"(tmem + part * 256), "l"(ad), "l"(bd), "r"(bf16_idesc(np)), "r"(acc), "r"(leader)
-                : "memory");
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sw128_desc(a0 + kk * 32);
+            const uint32_t acc = (kc > w.kbeg || kk > 0) ? 1u : 0u;
+            for (int part = 0; part < 2; ++part) {
+              const int np = part == 0 ? n0 : n1;
+              if (np == 0) continue;
+              const uint64_t bd = sw128_desc(b0 + part * h0 * 128 + kk * 32);
+              asm volatile(
+                  "{ .reg .pred p, q; setp.ne.b32 p, %4, 0; setp.ne.b32 q, %5, 0; "
+                  "@q tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p; }"
+                  ::"r"(tmem + part * 256), "l"(ad), "l"(bd), "r"(bf16_idesc(2 * kLmTile, np)), "r"(acc), "r"(leader)
+                  : "memory");
+            }
           }
+          mma_commit_pair_if(leader, &empty[s]);
         }
-        if (C > 1)
-          mma_commit_mc_if(leader, &empty[s], cmask);
-        else
-          mma_commit_if(leader, &empty[s]);
+        if (!ok) break;
+        mma_commit_pair_if(leader, dfull);
+        last = un;
       }
-      if (!ok) break;
-      mma_commit_if(leader, dfull);
-      last = un;
-    }
-    // before tensor memory and the stages go (bounded): the last unit's MMAs are done,
-    // and every CTA of the cluster has released the stages (no arrival still to come)
-    const uint64_t t0 = globaltimer_ns();
-    if (last >= 0)
-      while (!__all_sync(kFull, mbar_try(dfull, last & 1)) && !__any_sync(kFull, globaltimer_ns() - t0 >= p.timeout_ns)) {}
-    for (int s = 0; s < NS; ++s) {
-      if (g - 1 - s < 0) continue;
-      const int gl = g - 1 - s;
-      while (!__all_sync(kFull, mbar_try(&empty[gl % NS], (gl / NS) & 1)) &&
-             !__any_sync(kFull, globaltimer_ns() - t0 >= p.timeout_ns)) {}
+      // before tensor memory and the stages go (bounded): the last unit's MMAs are done
+      // and every stage's release has arrived
+      const uint64_t t0 = globaltimer_ns();
+      if (last >= 0)
+        while (!__all_sync(kFull, mbar_try(dfull, last & 1)) && !__any_sync(kFull, globaltimer_ns() - t0 >= p.timeout_ns)) {}
+      for (int s = 0; s < NS; ++s) {
+        if (g - 1 - s < 0) continue;
+        const int gl = g - 1 - s;
+        while (!__all_sync(kFull, mbar_try(&empty[gl % NS], (gl / NS) & 1)) &&
+               !__any_sync(kFull, globaltimer_ns() - t0 >= p.timeout_ns)) {}
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -330,7 +324,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_gemm_kernel(const __grid
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
     int un = 0;
     for (int u = cid; u < units && !__any_sync(kFull, *fail); u += ncl, ++un) {
-      const LmUnit w = lm_unit(p, u, mchunks, C, crank, nk);
+      const LmUnit w = lm_unit(p, u, mchunks, 2, crank, nk);
       const int tile = w.tile, m0 = w.m0, mrows = w.mrows;
       // this warp's column thresholds (step i: columns 32 cg + 128 i + j at thr_w[32 i + j]),
       // read before the accumulator is ready: a logit passes when !(x < threshold)
@@ -423,16 +417,16 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_gemm_kernel(const __grid
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(dempty);
+      if (lane == 0) mbar_arrive_cluster(dempty0);  // rank 0's MMAs may overwrite the accumulator
       if (MODE == 1 && nq > 0) flush();
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  cluster_sync();  // no CTA leaves while a peer may still write into it
+  cluster_sync();  // no CTA leaves while its pair may still write into it or arrive on it
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kLmTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kLmTmemCols) : "memory");
 }
 
 namespace {
@@ -702,21 +696,17 @@ __global__ void __launch_bounds__(kSelThreads) lmhead_select_kernel(const LmPara
 
 namespace {
 
-// Grid of a GEMM pass: whole clusters, no more than can be resident at once (one CTA per
-// SM) and no more than there are cluster steps of work.
+// Grid of a GEMM pass: CTA pairs (clusters of two), no more than can be resident at once
+// (one CTA per SM) and no more than there are pair steps of work.
 template <int MODE>
 cudaError_t launch_gemm(LmParams& p, int sms, size_t smem, int units, cudaStream_t stream) {
   auto fn = lmhead_gemm_kernel<MODE>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  if (p.cluster <= 1) {
-    fn<<<std::max(1, std::min(sms, units)), kLmThreads, smem, stream>>>(p);
-    return cudaGetLastError();
-  }
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+  attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(kLmThreads);
@@ -724,12 +714,11 @@ cudaError_t launch_gemm(LmParams& p, int sms, size_t smem, int units, cudaStream
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(p.cluster * (sms / p.cluster)));
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * (sms / 2)));
   int max_clusters = 0;
   if ((e = cudaOccupancyMaxActiveClusters(&max_clusters, fn, &cfg)) != cudaSuccess) return e;
   if (max_clusters < 1) return cudaErrorInvalidConfiguration;
-  const int groups = std::max(1, units);  // cluster steps
-  cfg.gridDim = dim3(static_cast<unsigned>(p.cluster * std::min(max_clusters, groups)));
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * std::min(max_clusters, std::max(1, units))));
   return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
@@ -743,13 +732,12 @@ cudaError_t launch_lmhead(LmParams& p, int sms, int pivot_rank, cudaStream_t str
                                 kPivotSmemKeys * 4)) != cudaSuccess)
     return e;
   const int mchunks = (p.M + 511) / 512;
-  const int C = std::max(1, p.cluster);
-  const int units0 = static_cast<int>(((p.S + kLmTile - 1) / kLmTile + C - 1) / C) * mchunks;
-  const int units1 = static_cast<int>(((p.V + kLmTile - 1) / kLmTile + C - 1) / C) * mchunks;
+  const int units0 = static_cast<int>(((p.S + kLmTile - 1) / kLmTile + 1) / 2) * mchunks;  // pair steps
+  const int units1 = static_cast<int>(((p.V + kLmTile - 1) / kLmTile + 1) / 2) * mchunks;
   // the sample pass has few tiles: split d so that every cluster has work, the parts
   // summed by fp32 atomics into the zeroed sample rows (the pivot needs no exact sums)
   const int nk = p.d / kLmChunk;
-  p.ksplit = std::max(1, std::min(std::min(nk, 8), (sms / C) / std::max(1, units0)));
+  p.ksplit = std::max(1, std::min(std::min(nk, 8), (sms / 2) / std::max(1, units0)));
   if (p.ksplit > 1 &&
       (e = cudaMemsetAsync(p.sample, 0, static_cast<size_t>(p.M) * p.S * sizeof(float), stream)) != cudaSuccess)
     return e;

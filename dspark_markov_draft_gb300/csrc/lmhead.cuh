@@ -19,21 +19,22 @@ constexpr int kLmEpiWarps = 16;
 constexpr int kLmThreads = (2 + kLmEpiWarps) * 32;
 constexpr int kLmAStageBytes = 128 * 128;   // 128 LM-head rows x 64 bf16 of d
 constexpr int kLmMaxStages = 6;
-constexpr int kLmCluster = 2;               // CTAs sharing each hidden-row chunk
+
 constexpr int kLmSmemLimit = 232448;        // opt-in dynamic shared memory per block
 // After the stages: barriers (128 bytes) and each epilogue warp's column thresholds
 // (4 steps x 32 floats).
 constexpr int kLmTailBytes = 128 + kLmEpiWarps * 4 * 32 * 4;
 
-// Hidden rows staged per chunk (a multiple of 32, at most 512), copied as two boxes:
-// rows [0, lm_box0) and [256, 256 + lm_box1) of the chunk.
+// Hidden rows of a chunk (a multiple of 32, at most 512): part 0 = rows [0, n0) with
+// n0 = min(256, rows), part 1 = rows [256, 256 + n1). The two CTAs of a pair each stage
+// half of each part (lm_box0 and lm_box1 rows), as the paired MMA splits B along N.
 __host__ __device__ inline int lm_b_rows(int32_t M) {
   const int m = M < 512 ? M : 512;
   return (m + 31) & ~31;
 }
-__host__ __device__ inline int lm_box0(int32_t M) { return lm_b_rows(M) < 256 ? lm_b_rows(M) : 256; }
-__host__ __device__ inline int lm_box1(int32_t M) { return lm_b_rows(M) > 256 ? lm_b_rows(M) - 256 : 0; }
-__host__ __device__ inline int lm_stage_bytes(int32_t M) { return kLmAStageBytes + 128 * lm_b_rows(M); }
+__host__ __device__ inline int lm_box0(int32_t M) { return (lm_b_rows(M) < 256 ? lm_b_rows(M) : 256) / 2; }
+__host__ __device__ inline int lm_box1(int32_t M) { return (lm_b_rows(M) > 256 ? lm_b_rows(M) - 256 : 0) / 2; }
+__host__ __device__ inline int lm_stage_bytes(int32_t M) { return kLmAStageBytes + 64 * lm_b_rows(M); }
 __host__ __device__ inline int lm_stages(int32_t M) {
   const int n = (kLmSmemLimit - 1024 - kLmTailBytes) / lm_stage_bytes(M);
   return n < kLmMaxStages ? n : kLmMaxStages;
@@ -58,7 +59,6 @@ struct LmParams {
   int32_t* stats;            // optional [2]: rows on the exact path, rows whose list overflowed
   int32_t* status_dev;
   int32_t flags;
-  int32_t cluster;           // CTAs per cluster sharing each hidden-row chunk (1, 2 or 4)
   int32_t ksplit;            // sample pass: parts of d per tile, summed by fp32 atomics (1: stored)
   uint64_t timeout_ns;
   CUtensorMap w_map;         // LM head [V][d], box 64 x 128 rows, 128-byte swizzle
