@@ -404,10 +404,17 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_gemm_kernel(const __grid
           while (pass) {
             const int j = __ffs(pass) - 1;
             pass &= pass - 1;
-            uint32_t x = 0;
+            // v[j] for a lane-dependent j: a five-level selection on the bits of j
+            uint32_t x16[16], x8[8], x4[4], x2[2];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
-              if (jj == j) x = v[jj];
+            for (int t = 0; t < 16; ++t) x16[t] = (j & 16) ? v[t + 16] : v[t];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) x8[t] = (j & 8) ? x16[t + 8] : x16[t];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) x4[t] = (j & 4) ? x8[t + 4] : x8[t];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) x2[t] = (j & 2) ? x4[t + 2] : x4[t];
+            const uint32_t x = (j & 1) ? x2[1] : x2[0];
             if (nq == 4) flush();
             q3 = q2; q2 = q1; q1 = q0;
             q0 = (static_cast<uint64_t>(c0 + j) << 32) | order_key(__uint_as_float(x));
