@@ -444,27 +444,41 @@ def time_lmhead(dev, flush, peaks, steps, V=151936, K=7, bs=64, d=2048, k=512):
 
 def time_e2e(cfg, t, args, steps, dev):
     """Walk through dspark_walk_from_host: per-step H2D of base/prev/seeds from pinned
-    host memory, the walk, D2H of the tokens; timed with events around all of it."""
+    host memory, the walk, D2H of the tokens; timed with events around all of it. Two
+    sets of device buffers on two streams, steps alternating between them (double
+    buffering by the caller), so that one step's copies run while the other's walk runs;
+    the copy engine is shared, so the copies themselves stay in sequence."""
     from dspark_markov_draft_gb300 import capi
     inp = t["inp"]
     base_h = inp.base.pin_memory()
     prev_h = inp.prev.pin_memory()
     seeds_h = inp.seeds.pin_memory()
-    tok_h = torch.empty((cfg["bs"], cfg["K"]), dtype=torch.int32).pin_memory()
-    stream = torch.cuda.current_stream()
-    for _ in range(2):
-        capi.walk_from_host(args, base_h, prev_h, seeds_h, tok_h, None, stream)
+    tok_h = [torch.empty((cfg["bs"], cfg["K"]), dtype=torch.int32).pin_memory() for _ in range(2)]
+    t2 = dict(inp=inp, w1=t["w1"], w2=t.get("w2"), w2q=t.get("w2q"), scales=t.get("scales"),
+              base=torch.empty_like(t["base"]), prev=torch.empty_like(t["prev"]), seeds=torch.empty_like(t["seeds"]))
+    args2 = make_walk_args(cfg, t2, dev)
+    arg_sets = [args, args2]
+    main = torch.cuda.current_stream()
+    streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
+    for j in range(2):
+        capi.walk_from_host(arg_sets[j], base_h, prev_h, seeds_h, tok_h[j], None, streams[j])
     torch.cuda.synchronize()
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
-    s.record(stream)
-    for _ in range(steps):
-        capi.walk_from_host(args, base_h, prev_h, seeds_h, tok_h, None, stream)
-    e.record(stream)
+    s.record(main)
+    for st in streams:
+        st.wait_event(s)
+    for j in range(steps):
+        capi.walk_from_host(arg_sets[j % 2], base_h, prev_h, seeds_h, tok_h[j % 2], None, streams[j % 2])
+    for st in streams:
+        ev = torch.cuda.Event()
+        ev.record(st)
+        main.wait_event(ev)
+    e.record(main)
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / steps
     h2d = base_h.numel() * 2 + prev_h.numel() * 4 + seeds_h.numel() * 8
-    d2h = tok_h.numel() * 4
+    d2h = tok_h[0].numel() * 4
     return ms, h2d, d2h
 
 
@@ -761,7 +775,8 @@ def main():
             "lmhead_topk": lmhead,
             "cpu_baseline": cpu,
             "e2e": {"value": world * toks / (e2e_ms * 1e-3), "unit": UNIT,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "pipelining": "two buffer sets on two streams, steps alternating"},
             "parity": parity,
             "gpu_launches": a.steps * kernels_per_walk(cfg),
             "clocks": clk.summary(),
