@@ -9,7 +9,7 @@
 namespace dspark {
 
 // Every kLmSampleStride-th LM-head row is scored in the sample pass.
-constexpr int kLmSampleStride = 32;
+constexpr int kLmSampleStride = 16;
 // Flag: every row takes the exact path (testing).
 constexpr int32_t kLmForceExact = 1;
 
