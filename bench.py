@@ -314,10 +314,11 @@ def time_walks(cfg, steps, warmup, dev, flush):
     return times, t, args
 
 
-def time_graph(args, steps, flush):
+def time_graph(args, steps, flush, cold=True):
     """The same walk captured once in a CUDA graph and replayed: per-replay CUDA-event
     times (ms), the L2 flushed before each replay (outside the events), as the pages'
-    kernel benchmark replays a graph of one walk."""
+    kernel benchmark replays a graph of one walk; cold=False: no flush (warm L2, the
+    inputs of the previous replay still cached where they fit)."""
     from dspark_markov_draft_gb300 import capi
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
@@ -325,14 +326,16 @@ def time_graph(args, steps, flush):
     if st:
         raise RuntimeError(f"walk capture failed: {capi.STATUS.get(st, st)}")
     for _ in range(3):
-        flush.zero_()
+        if cold:
+            flush.zero_()
         g.replay()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
     for s, e in evs:
-        flush.zero_()
+        if cold:
+            flush.zero_()
         s.record(stream)
         g.replay()
         e.record(stream)
@@ -497,6 +500,30 @@ def job_throughput(ms_max: float, world: int, tokens_per_rank: int) -> float:
     return world * tokens_per_rank / (ms_max * 1e-3)
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (and architecture), for the oracle baseline."""
+    import platform
+    name = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                name = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not name:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith("model name"):
+                        name = ln.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return f"{name or 'unknown'} ({platform.machine()})"
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -564,7 +591,7 @@ def cpu_baseline(cfg, gpu_tokens=None, target_s: float = 10.0, single_s: float =
     reps = 1 if rows < cfg["bs"] else int(min(20, max(1, target_s / max(rows * t1, 1e-6))))
     dt = sum(runner.run(rows, cores) for _ in range(reps))
     toks = reps * rows * cfg["K"]
-    out = {"value": toks / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+    out = {"value": toks / dt, "unit": UNIT, "cores": cores, "kind": "oracle", "cpu": cpu_model(),
            "sample": f"{reps} x {rows} of {cfg['bs']} request rows, all {cfg['K']} positions, "
                      f"{dt:.1f} s of oracle time"}
     s1 = runner.run(1, 1)
@@ -705,7 +732,8 @@ def main():
     value = job_throughput(ms, world, toks)
 
     e2e_ms, h2d, d2h = (float("nan"), 0, 0) if a.no_e2e else time_e2e(cfg, t, args, max(3, a.steps // 2), dev)
-    graph_times = time_graph(args, max(5, a.steps), flush)  # outside the timed region
+    graph_times = time_graph(args, max(200, a.steps), flush)  # outside the timed region
+    graph_warm = time_graph(args, max(200, a.steps), flush, cold=False)
     verify = None if a.no_verify else time_verify(dev, flush, peaks, max(5, a.steps))
     lmhead = [] if a.no_lmhead else [time_lmhead(dev, flush, peaks, max(5, a.steps), d=d_, k=k_)
                                      for d_, k_ in LMHEAD_CASES]
@@ -717,7 +745,8 @@ def main():
     roof["kernel"] = kernel_name(cfg)
     floor_us = max(fl.values())
     floor_rec = {k: round(v, 3) for k, v in fl.items()}
-    floor_rec.update({"floor_us": round(floor_us, 3), "frac_of_floor": floor_us / us,
+    floor_rec.update({"floor_us": round(floor_us, 3), "floor_sum_us": round(sum(fl.values()), 3),
+                      "frac_of_floor": floor_us / us,
                       "resident_w2_rows": res_rows, "l2_gbs_live": round(l2_gbs, 1),
                       "hbm_bytes": hbm_bytes(cfg), "gumbel_us_informational": gumbel_floor_us(cfg, peaks, sms),
                       "chain_us_informational": round(chain_floor_us(cfg, fl), 3)})
@@ -768,7 +797,11 @@ def main():
                        "parallelism": f"replicas x{world}"},
             "us_per_walk": us,
             "graph": {"us_per_walk": 1000 * statistics.median(graph_times), "replays": len(graph_times),
-                      "l2": "flushed before every replay"},
+                      "l2": "flushed before every replay",
+                      "warm_us_per_walk": 1000 * statistics.median(graph_warm),
+                      "warm": "no flush between replays"},
+            "device": {"name": torch.cuda.get_device_name(dev), "sms_used": sms,
+                       "sharing": "one process on the GPU"},
             "roofline": roof,
             "floors": floor_rec,
             "verify": verify,
