@@ -501,6 +501,11 @@ int32_t dspark_lmhead_topk(const dspark_lmhead_args* a, dspark_stream_t stream) 
   if ((st = current_caps(&caps)) != DSPARK_OK) return st;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return DSPARK_ERR_UNSUPPORTED;
+  // The GEMM passes take all 512 tensor-memory columns of their SM: their shared memory
+  // must fit the device and keep a second CTA off the SM (more than half of it).
+  const size_t gemm_smem = static_cast<size_t>(lm_gemm_smem(a->M));
+  if (gemm_smem > static_cast<size_t>(caps.smem_optin) || 2 * gemm_smem <= static_cast<size_t>(caps.smem_per_sm))
+    return DSPARK_ERR_UNSUPPORTED;
   LmParams p{};
   p.hidden = a->hidden;
   p.lm_head = a->lm_head;
