@@ -639,7 +639,10 @@ __global__ void __launch_bounds__(kSelThreads) lmhead_select_kernel(const LmPara
     }
     return;
   }
-  if (threadIdx.x == 0 && p.stats) atomicAdd(p.stats + (n_all > static_cast<uint32_t>(p.cap) ? 1 : 0), 1);
+  if (threadIdx.x == 0 && p.stats) {  // every exact-path row, and separately the overflowed ones
+    atomicAdd(p.stats, 1);
+    if (n_all > static_cast<uint32_t>(p.cap)) atomicAdd(p.stats + 1, 1);
+  }
   // exact path: radix selection of the k-th largest key over the whole recomputed row,
   // then an index-ordered pass taking keys above it and the first ties
   uint32_t prefix = 0;

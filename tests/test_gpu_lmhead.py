@@ -87,6 +87,41 @@ def test_lmhead_ties_resolve_to_smaller_indices(oracle):
             np.testing.assert_array_equal(cbase[m].cpu().double().numpy(), ref[m][cand[m].cpu().numpy()])
 
 
+def test_lmhead_all_equal_logits_overflow_to_the_exact_path(oracle):
+    """Zero hidden states: every logit is 0, every entry reaches the pivot, each row's
+    list overflows (V > 3k + 1024) and the exact path must return the k smallest indices
+    with value 0 (equal values in index order)."""
+    M, d, V, k = 3, 128, 5000, 100
+    hidden = torch.zeros((M, d), dtype=torch.bfloat16)
+    _, head = synth.lmhead(M, d, V, seed=11)
+    stats = torch.zeros(2, dtype=torch.int32, device=DEV)
+    cand, cbase = capi.lmhead_topk(hidden.to(DEV), head.to(DEV), k, stats=stats)
+    torch.cuda.synchronize()
+    assert int(stats[0]) == M and int(stats[1]) == M  # every row: exact path, by overflow
+    ref = oracle.lmhead_logits(bits(hidden), bits(head))
+    assert np.all(ref == 0.0)
+    for m in range(M):
+        assert sorted(cand[m].cpu().tolist()) == list(range(k))
+    assert np.all(cbase.cpu().numpy() == 0.0)
+
+
+def test_lmhead_nan_row_takes_the_smallest_indices(oracle):
+    """A NaN in one hidden row makes all its logits NaN: NaN counts as the largest value,
+    so its candidates are the k smallest indices, with NaN logits; the other rows are
+    unaffected."""
+    M, d, V, k = 4, 128, 3001, 64
+    hidden, head = synth.lmhead(M, d, V, seed=12)
+    hidden[2, 5] = float("nan")
+    cand, cbase = capi.lmhead_topk(hidden.to(DEV), head.to(DEV), k)
+    torch.cuda.synchronize()
+    ref = oracle.lmhead_logits(bits(hidden), bits(head))
+    assert np.all(np.isnan(ref[2]))
+    assert sorted(cand[2].cpu().tolist()) == list(range(k))
+    assert np.all(np.isnan(cbase[2].cpu().numpy()))
+    rows = [0, 1, 3]
+    check_sets(ref[rows], cand.cpu().numpy()[rows], cbase.cpu().double().numpy()[rows], k, VAL_TOL)
+
+
 @pytest.mark.parametrize("mode,T", [(capi.GREEDY, 1.0), (capi.PROBABILISTIC, 1.0), (capi.PROBABILISTIC, 0.7)])
 def test_walk_on_fused_candidates(oracle, mode, T):
     """LM head -> top-k candidates -> the top-k walk on them (no dense base logits):
