@@ -87,6 +87,21 @@ def test_lmhead_ties_resolve_to_smaller_indices(oracle):
             np.testing.assert_array_equal(cbase[m].cpu().double().numpy(), ref[m][cand[m].cpu().numpy()])
 
 
+@pytest.mark.parametrize("M,d,V,k", [(1, 64, 50, 10), (2, 64, 1000, 1000), (513, 64, 300, 5), (7, 192, 129, 128)])
+def test_lmhead_edge_shapes(oracle, M, d, V, k):
+    """A single hidden row and a vocabulary smaller than one 128-row tile; k = V (every
+    entry is a candidate); 513 hidden rows (a second 512-row chunk of one row); a
+    vocabulary one row past a tile with k one below it. Sets and values as above."""
+    hidden, head = synth.lmhead(M, d, V, seed=M + d + V + k)
+    cand, cbase = capi.lmhead_topk(hidden.to(DEV), head.to(DEV), k)
+    torch.cuda.synchronize()
+    ref = oracle.lmhead_logits(bits(hidden), bits(head), nthreads=16)
+    check_sets(ref, cand.cpu().numpy(), cbase.cpu().double().numpy(), k, VAL_TOL)
+    if k == V:
+        for m in range(M):
+            assert sorted(cand[m].cpu().tolist()) == list(range(V))
+
+
 def test_lmhead_all_equal_logits_overflow_to_the_exact_path(oracle):
     """Zero hidden states: every logit is 0, every entry reaches the pivot, each row's
     list overflows (V > 3k + 1024) and the exact path must return the k smallest indices
