@@ -115,7 +115,10 @@ typedef struct dspark_walk_args {
      together, top_k > 0): the candidates of every (b, i) and their base logits, e.g. from
      dspark_lmhead_topk. The walk then skips its own selection and base_logits may be
      NULL. */
-  const int32_t* topk_cand;  /* int32 [bs, K, top_k] vocabulary ids in [0, V), any order */
+  const int32_t* topk_cand;  /* int32 [bs, K, top_k] distinct vocabulary ids in [0, V), any
+                                order; an id outside [0, V) is clamped into it (the walk
+                                stays in bounds, its result for that (b, i) is then not a
+                                walk over the given set) */
   const float* topk_base;    /* fp32 [bs, K, top_k] their base logits */
 } dspark_walk_args;
 
