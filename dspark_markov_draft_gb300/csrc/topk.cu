@@ -32,6 +32,38 @@ namespace dspark {
 
 namespace {
 
+// L2 policies of the candidate walk: W2 rows are read again at later positions (evict
+// last); candidate ids and their base logits are read once (evict first, no L1 line).
+__device__ __forceinline__ uint64_t l2_policy_keep() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_once() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 ld_keep_u4(const void* ptr, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(ptr), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_once_b32(const void* ptr, uint64_t pol) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(v) : "l"(ptr), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_once_u16(const uint16_t* ptr, uint64_t pol) {
+  uint16_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u16 %0, [%1], %2;" : "=h"(v) : "l"(ptr), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void prefetch_l2_keep(const void* ptr) {
+  asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(ptr));
+}
+
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelCap = 8192;    // entries collected by the fast path
@@ -417,6 +449,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
                                   : reinterpret_cast<const unsigned char*>(p.w2);
   constexpr int kRowBytes = INT8 ? kRank : 2 * kRank;
   constexpr int kLaneChunks = kRowBytes / 16 / 8;  // 16-byte chunks j8 + 8 c of a row per lane
+  const uint64_t keep = l2_policy_keep(), once = l2_policy_once();
 
   for (int t = tid; t < p.bs; t += blockDim.x) {
     const int32_t tok = p.prev[t];
@@ -435,11 +468,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
       const int e = static_cast<int>(it - c_lo);
       const int b = static_cast<int>(it / p.top_k);
       const int64_t j = it - static_cast<int64_t>(b) * p.top_k;
-      const int64_t v = min(max(static_cast<int64_t>(p.cand[(static_cast<size_t>(b) * p.K + i) * p.top_k + j]),
+      const size_t ci = (static_cast<size_t>(b) * p.K + i) * p.top_k + j;
+      const int64_t v = min(max(static_cast<int64_t>(static_cast<int32_t>(ld_once_b32(p.cand + ci, once))),
                                 int64_t{0}), p.V - 1);
       it_v[e] = static_cast<int32_t>(v);
-      it_base[e] = p.cand_base ? __ldg(p.cand_base + (static_cast<size_t>(b) * p.K + i) * p.top_k + j)
-                               : bf16_to_f32(__ldg(p.base + (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v));
+      it_base[e] = p.cand_base
+                       ? __uint_as_float(ld_once_b32(p.cand_base + ci, once))
+                       : bf16_to_f32(static_cast<uint16_t>(
+                             ld_once_u16(p.base + (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(p.V) + v, once)));
       float g = 0.f;
       if (row_sampled(p, PROB, b)) {
         const uint4 w = philox_block(p.seeds[b], b, i, static_cast<uint32_t>(v >> 2));
@@ -448,7 +484,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
       it_g[e] = g;
       const unsigned char* row = w2g + static_cast<size_t>(v) * kRowBytes;
 #pragma unroll
-      for (int m = 0; m < kRowBytes / 128; ++m) prefetch_l2(row + 128 * m);
+      for (int m = 0; m < kRowBytes / 128; ++m) prefetch_l2_keep(row + 128 * m);
     }
   };
 
@@ -549,7 +585,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) topk_walk_kernel(const WalkPa
             const unsigned char* row = w2g + static_cast<size_t>(it_v[e0 + min(r, nt - 1)]) * kRowBytes;
 #pragma unroll
             for (int c = 0; c < kLaneChunks; ++c)
-              q[rr][c] = r < nt ? __ldg(reinterpret_cast<const uint4*>(row) + j8 + 8 * c) : make_uint4(0, 0, 0, 0);
+              q[rr][c] = r < nt ? ld_keep_u4(reinterpret_cast<const uint4*>(row) + j8 + 8 * c, keep) : make_uint4(0, 0, 0, 0);
           }
 #pragma unroll
           for (int rr = 0; rr < 4; ++rr) {
