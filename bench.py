@@ -381,7 +381,7 @@ def time_verify(dev, flush, peaks, steps, V=151936, K=7, bs=64, T=1.0):
             "l2": "flushed before every call"}
 
 
-LMHEAD_CASES = [(2048, 512), (2048, 4096), (4096, 512)]
+LMHEAD_CASES = [(2048, 512, 7), (2048, 4096, 7), (4096, 512, 7), (2048, 512, 16)]
 
 
 def time_lmhead(dev, flush, peaks, steps, V=151936, K=7, bs=64, d=2048, k=512):
@@ -735,8 +735,8 @@ def main():
     graph_times = time_graph(args, max(200, a.steps), flush)  # outside the timed region
     graph_warm = time_graph(args, max(200, a.steps), flush, cold=False)
     verify = None if a.no_verify else time_verify(dev, flush, peaks, max(5, a.steps))
-    lmhead = [] if a.no_lmhead else [time_lmhead(dev, flush, peaks, max(5, a.steps), d=d_, k=k_)
-                                     for d_, k_ in LMHEAD_CASES]
+    lmhead = [] if a.no_lmhead else [time_lmhead(dev, flush, peaks, max(5, a.steps), K=K_, d=d_, k=k_)
+                                     for d_, k_, K_ in LMHEAD_CASES]
     fl, res_rows = floors_of(cfg)
     us = 1000 * ms
     roof = roofline(cfg, peaks, fl, us, sms)

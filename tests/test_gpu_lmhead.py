@@ -154,12 +154,13 @@ def test_walk_on_fused_candidates(oracle, mode, T):
                     gpu_logits=lg, base_f64_all=base64)
 
 
-@pytest.mark.parametrize("d,k", [(2048, 512), (2048, 4096), (4096, 512)])
-def test_full_size_lmhead_topk_walk(oracle, d, k):
-    """d in {2048, 4096}, V = 151936, bs = 64, K = 7 (448 hidden rows): the fused selection
-    served by the pivot on every row; candidate sets, values and the walk's tokens checked
-    on sampled request rows (all their positions) against the oracle."""
-    V, K, bs = 151936, 7, 64
+@pytest.mark.parametrize("d,k,K", [(2048, 512, 7), (2048, 4096, 7), (4096, 512, 7), (2048, 512, 16)])
+def test_full_size_lmhead_topk_walk(oracle, d, k, K):
+    """d in {2048, 4096}, V = 151936, bs = 64, K = 7 (448 hidden rows) or K = 16 (1024
+    hidden rows: two 512-row chunks per LM-head tile): the fused selection served by the
+    pivot on every row; candidate sets, values and the walk's tokens checked on sampled
+    request rows (all their positions) against the oracle."""
+    V, bs = 151936, 64
     inp = synth.make(V, bs, K, seed=0)
     hidden, head = synth.lmhead(bs * K, d, V, seed=1)
     stats = torch.zeros(2, dtype=torch.int32, device=DEV)
@@ -175,5 +176,5 @@ def test_full_size_lmhead_topk_walk(oracle, d, k):
     check_sets(ref, cand.cpu().numpy()[hrows], cbase.cpu().double().numpy()[hrows], k, VAL_TOL)
     base64 = np.zeros((bs, K, V))
     base64[rows_b] = ref.reshape(len(rows_b), K, V)
-    check_walk_rows(oracle, inp, tokens, label=f"V=151936 K=7 bs=64 lmhead d={d} top-k {k} (rows {rows_b})",
+    check_walk_rows(oracle, inp, tokens, label=f"V=151936 K={K} bs=64 lmhead d={d} top-k {k} (rows {rows_b})",
                     mode=capi.PROBABILISTIC, top_k=k, base_f64_all=base64, rows_subset=rows_b)
