@@ -26,6 +26,15 @@
 // read the accumulator back; as many stages as shared memory holds (three at 448 hidden
 // rows). The epilogue is short next to a tile's MMAs: each of its warps reads 32 x 32
 // accumulators per step and tests them against per-column pivots broadcast by shuffles.
+//
+// Passes 2-4 are launched as programmatic dependents of the pass before them: a pass may
+// be scheduled once every CTA of the previous one has started (or, after the filter
+// pass, finished its tiles), so its launch and set-up overlap the previous pass's end,
+// and it waits for the previous pass to complete (griddepcontrol.wait) before reading
+// what that pass wrote. In the filter pass only the epilogue waits (it reads the pivots
+// and appends to the lists the pivot pass reset): the copies and MMAs of its first
+// tiles read only the inputs, which the sample pass -- launched in stream order --
+// already found complete.
 #include <algorithm>
 #include <cstdint>
 
@@ -52,6 +61,12 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   d |= static_cast<uint64_t>(2) << 61;
   return d;
 }
+// Programmatic dependent launch: wait for the previous kernel in the stream to complete
+// (its writes visible; a no-op when the kernel was launched in plain stream order), and
+// let the next kernel be scheduled before this one completes.
+__device__ __forceinline__ void wait_previous_pass() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_next_pass() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // kind::f16 instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, M x N.
 __host__ __device__ constexpr uint32_t bf16_idesc(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
@@ -227,6 +242,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_gemm_kernel(const __grid
   cluster_sync();  // both CTAs' barriers are initialised before any copy or arrival lands in them
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tbase_s;
+  if (MODE == 0 && tid == 0) allow_next_pass();
   const CUtensorMap* amap = MODE == 0 ? &p.ws_map : &p.w_map;
   const uint32_t full0 = peer_addr(full, 0);      // rank 0's full[0]; full[s] is 8 s further
   const uint32_t dempty0 = peer_addr(dempty, 0);  // rank 0's dempty
@@ -319,6 +335,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_gemm_kernel(const __grid
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    if (MODE == 1) wait_previous_pass();       // the pivots and the reset list counters
     const int q = warp & 3;                    // tensor-memory lane quadrant
     const int cg = (warp - 2) >> 2;            // column group: 32-column steps cg, cg + 4, ...
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
@@ -430,6 +447,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_gemm_kernel(const __grid
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
+  if (MODE == 1 && tid == 0) allow_next_pass();
   cluster_sync();  // no CTA leaves while its pair may still write into it or arrive on it
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   if (warp == 0)
@@ -575,6 +593,8 @@ __global__ void __launch_bounds__(kSelThreads) lmhead_pivot_kernel(const LmParam
   __shared__ int hist[256];
   __shared__ int sel[3];
   __shared__ unsigned long long mm[2];
+  if (threadIdx.x == 0) allow_next_pass();
+  wait_previous_pass();  // the sampled logits
   const int m = blockIdx.x;
   const float* x = p.sample + static_cast<size_t>(m) * p.S;
   const int n = p.S < kPivotSmemKeys ? p.S : kPivotSmemKeys;
@@ -609,6 +629,7 @@ __global__ void __launch_bounds__(kSelThreads) lmhead_select_kernel(const LmPara
   __shared__ int sel[3];
   __shared__ unsigned long long mm[2];
   __shared__ int outpos;
+  wait_previous_pass();  // the lists and their counters
   const int m = blockIdx.x;
   const int k = p.k;
   const uint32_t n_all = p.cnt[static_cast<size_t>(m) * kLmCntStride];
@@ -714,22 +735,43 @@ cudaError_t launch_gemm(LmParams& p, int sms, size_t smem, int units, cudaStream
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // the filter pass follows the pivot pass as a programmatic dependent; the sample pass
+  // starts the call in plain stream order (it reads the caller's inputs)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kLmThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = MODE == 1 ? 2 : 1;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * (sms / 2)));
   int max_clusters = 0;
   if ((e = cudaOccupancyMaxActiveClusters(&max_clusters, fn, &cfg)) != cudaSuccess) return e;
   if (max_clusters < 1) return cudaErrorInvalidConfiguration;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * std::min(max_clusters, std::max(1, units))));
   return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+// The pivot and select passes: one CTA per hidden row, launched as programmatic
+// dependents of the pass before them.
+template <typename... Args>
+cudaError_t launch_dependent(void (*fn)(Args...), unsigned grid, size_t smem, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, args...);
 }
 
 }  // namespace
@@ -753,11 +795,11 @@ cudaError_t launch_lmhead(LmParams& p, int sms, int pivot_rank, cudaStream_t str
     return e;
   if ((e = launch_gemm<0>(p, sms, smem, units0 * p.ksplit, stream)) != cudaSuccess) return e;
   p.ksplit = 1;
-  lmhead_pivot_kernel<<<p.M, kSelThreads, psmem, stream>>>(p, pivot_rank);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_dependent(lmhead_pivot_kernel, static_cast<unsigned>(p.M), psmem, stream, p, pivot_rank)) !=
+      cudaSuccess)
+    return e;
   if ((e = launch_gemm<1>(p, sms, smem, units1, stream)) != cudaSuccess) return e;
-  lmhead_select_kernel<<<p.M, kSelThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(lmhead_select_kernel, static_cast<unsigned>(p.M), 0, stream, p);
 }
 
 }  // namespace dspark
