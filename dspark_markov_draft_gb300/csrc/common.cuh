@@ -163,6 +163,11 @@ __host__ __device__ inline size_t ws_total(int K, int bs, int top_k) {
   return ws_cand_off(K, bs) + 4ull * bs * K * static_cast<size_t>(top_k);
 }
 
+// Programmatic dependent launch: wait until the previous kernel in the stream has
+// completed and its writes are visible (a no-op for a kernel launched in plain stream
+// order).
+__device__ __forceinline__ void wait_previous_kernel() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }

@@ -13,7 +13,8 @@
 // verify_accept_kernel: one CTA per (draft position i, row b): the softmax normalisers
 // of the two rows (one pass, running maximum) and the acceptance bit of d_i (atomicOr
 // into the row's word).
-// verify_emit_kernel: a cluster of kEmitCtas CTAs per row, each on a vocabulary slice:
+// verify_emit_kernel: a cluster of kEmitCtas CTAs per row, each on a vocabulary slice
+// (launched as a programmatic dependent of the acceptance kernel, which it waits for):
 // the accepted prefix from the bits, then the sample at the first rejected position
 // (or the bonus) -- only there -- with the slices' partial normalisers and argmax words
 // exchanged through distributed shared memory; rank 0 writes the emitted sequence.
@@ -224,6 +225,7 @@ __global__ void __cluster_dims__(kEmitCtas, 1, 1) __launch_bounds__(kVerifyThrea
   __shared__ Softmax part_t, part_d;  // this slice's normalisers
   __shared__ uint64_t part_best[2];   // this slice's argmax word, per sampling round
   __shared__ int part_any;            // this slice holds an entry with p > q
+  wait_previous_kernel();  // the acceptance bits (launched as the acceptance pass's dependent)
   cg::cluster_group cl = cg::this_cluster();
   const int r = static_cast<int>(cl.block_rank()), b = blockIdx.y, tid = threadIdx.x;
   const int64_t V = p.V, v0 = emit_slice(r, V), v1 = emit_slice(r + 1, V);
@@ -338,8 +340,20 @@ int32_t verify_launch(const uint16_t* target, const uint16_t* draft, const int32
   cudaError_t e = cudaMemsetAsync(accepted, 0, sizeof(int32_t) * static_cast<size_t>(bs), stream);
   if (e != cudaSuccess) return static_cast<int32_t>(e);
   verify_accept_kernel<<<dim3(K, bs), kVerifyThreads, 0, stream>>>(p);
-  verify_emit_kernel<<<dim3(kEmitCtas, bs), kVerifyThreads, 0, stream>>>(p);
-  return static_cast<int32_t>(cudaGetLastError());
+  if ((e = cudaGetLastError()) != cudaSuccess) return static_cast<int32_t>(e);
+  // the sample pass as a programmatic dependent of the acceptance pass: its launch
+  // overlaps the acceptance pass's end; it waits for the bits before reading them
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(kEmitCtas, bs);
+  cfg.blockDim = dim3(kVerifyThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return static_cast<int32_t>(cudaLaunchKernelEx(&cfg, verify_emit_kernel, p));
 }
 
 }  // namespace dspark
