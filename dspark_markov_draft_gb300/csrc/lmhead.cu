@@ -61,10 +61,8 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   d |= static_cast<uint64_t>(2) << 61;
   return d;
 }
-// Programmatic dependent launch: wait for the previous kernel in the stream to complete
-// (its writes visible; a no-op when the kernel was launched in plain stream order), and
-// let the next kernel be scheduled before this one completes.
-__device__ __forceinline__ void wait_previous_pass() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Programmatic dependent launch: let the next pass be scheduled before this one
+// completes (it waits for this pass with wait_previous_kernel before reading its output).
 __device__ __forceinline__ void allow_next_pass() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // kind::f16 instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, M x N.
@@ -335,7 +333,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_gemm_kernel(const __grid
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    if (MODE == 1) wait_previous_pass();       // the pivots and the reset list counters
+    if (MODE == 1) wait_previous_kernel();       // the pivots and the reset list counters
     const int q = warp & 3;                    // tensor-memory lane quadrant
     const int cg = (warp - 2) >> 2;            // column group: 32-column steps cg, cg + 4, ...
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
@@ -594,7 +592,7 @@ __global__ void __launch_bounds__(kSelThreads) lmhead_pivot_kernel(const LmParam
   __shared__ int sel[3];
   __shared__ unsigned long long mm[2];
   if (threadIdx.x == 0) allow_next_pass();
-  wait_previous_pass();  // the sampled logits
+  wait_previous_kernel();  // the sampled logits
   const int m = blockIdx.x;
   const float* x = p.sample + static_cast<size_t>(m) * p.S;
   const int n = p.S < kPivotSmemKeys ? p.S : kPivotSmemKeys;
@@ -629,7 +627,7 @@ __global__ void __launch_bounds__(kSelThreads) lmhead_select_kernel(const LmPara
   __shared__ int sel[3];
   __shared__ unsigned long long mm[2];
   __shared__ int outpos;
-  wait_previous_pass();  // the lists and their counters
+  wait_previous_kernel();  // the lists and their counters
   const int m = blockIdx.x;
   const int k = p.k;
   const uint32_t n_all = p.cnt[static_cast<size_t>(m) * kLmCntStride];
