@@ -22,7 +22,7 @@ int32_t verify_launch(const uint16_t* target, const uint16_t* draft, const int32
                       int32_t* accepted, int32_t* out_tokens, cudaStream_t stream);
 size_t topk_walk_smem(int bs);
 cudaError_t launch_topk_select(const uint16_t* base, int64_t V, int k, int rows, int32_t* cand,
-                               uint16_t* logits, cudaStream_t stream);
+                               float* cand_base, uint16_t* logits, cudaStream_t stream);
 cudaError_t launch_quantize_w2(const uint16_t* w2, int64_t V, int8_t* q, float* scales,
                                int32_t* status_dev, cudaStream_t stream);
 cudaError_t launch_gumbel_noise(const uint64_t* seeds, int bs, int K, int64_t V, uint32_t* words,
@@ -432,8 +432,11 @@ int32_t dspark_walk_topk(const dspark_walk_args* a, dspark_stream_t stream) {
       if (e != cudaSuccess) return cuda_fail(e, "fill_neg_inf_kernel launch");
     }
   } else {
+    float* cand_base = reinterpret_cast<float*>(static_cast<char*>(a->workspace) +
+                                                ws_cand_base_off(a->K, a->bs, a->top_k));
+    p.cand_base = cand_base;
     const cudaError_t e = launch_topk_select(a->base_logits, a->V, a->top_k, rows,
-                                             const_cast<int32_t*>(p.cand), a->draft_logits, s);
+                                             const_cast<int32_t*>(p.cand), cand_base, a->draft_logits, s);
     if (e != cudaSuccess) return cuda_fail(e, "topk_select_kernel launch");
   }
   const size_t smem = topk_walk_smem(a->bs);

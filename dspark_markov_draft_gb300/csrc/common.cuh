@@ -144,6 +144,7 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 //   [256, 256 + 128*K)       per-step arrival counters, one 128-byte line each
 //   next 8*K*bs              per-step argmax words slot[i][b]
 //   next (aligned to 256)    top-k candidate lists int32 [bs, K, top_k]
+//   next (aligned to 256)    their base logits fp32 [bs, K, top_k]
 struct WsHeader {
   uint32_t abort;
   uint32_t exit_count;
@@ -159,8 +160,12 @@ __host__ __device__ inline size_t ws_cand_off(int K, int bs) {
   const size_t end = ws_slots_off(K) + 8ull * K * bs;
   return (end + 255) & ~static_cast<size_t>(255);
 }
+__host__ __device__ inline size_t ws_cand_base_off(int K, int bs, int top_k) {
+  const size_t end = ws_cand_off(K, bs) + 4ull * bs * K * static_cast<size_t>(top_k);
+  return (end + 255) & ~static_cast<size_t>(255);
+}
 __host__ __device__ inline size_t ws_total(int K, int bs, int top_k) {
-  return ws_cand_off(K, bs) + 4ull * bs * K * static_cast<size_t>(top_k);
+  return ws_cand_base_off(K, bs, top_k) + 4ull * bs * K * static_cast<size_t>(top_k);
 }
 
 // Programmatic dependent launch: wait until the previous kernel in the stream has

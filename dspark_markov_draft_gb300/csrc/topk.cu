@@ -198,18 +198,21 @@ __device__ __forceinline__ int warp_append(int c, int* counter) {
 }
 
 __global__ void __launch_bounds__(kSelThreads, 3) topk_select_kernel(const uint16_t* base, int64_t V,
-                                                                  int k, int32_t* cand,
+                                                                  int k, int32_t* cand, float* cand_base,
                                                                   uint16_t* logits) {
   extern __shared__ __align__(16) unsigned char sel_smem[];
   int* hist = reinterpret_cast<int*>(sel_smem);                           // [kSelBins]
   uint32_t* lidx = reinterpret_cast<uint32_t*>(hist + kSelBins);           // [kSelCap]
-  uint16_t* lkey = reinterpret_cast<uint16_t*>(lidx + kSelCap);            // [kSelCap]
-  int* scan_sh = reinterpret_cast<int*>(lkey + kSelCap);                   // [80]
+  uint16_t* lval = reinterpret_cast<uint16_t*>(lidx + kSelCap);            // [kSelCap] bf16 bits
+  int* scan_sh = reinterpret_cast<int*>(lval + kSelCap);                   // [80]
   int* sel = scan_sh + 80;                                                 // [8]
   const int tid = threadIdx.x;
   const size_t row = blockIdx.x;
   const uint16_t* x = base + row * static_cast<size_t>(V);
   int32_t* out = cand + row * static_cast<size_t>(k);
+  // the candidates' base logits beside their ids (fp32 of the bf16 bits): the walk then
+  // reads them contiguously instead of one scattered entry of the dense row each
+  float* out_base = cand_base + row * static_cast<size_t>(k);
 
   if (logits) {  // -inf everywhere; the walk overwrites the candidates
     uint16_t* lr = logits + row * static_cast<size_t>(V);
@@ -272,7 +275,7 @@ __global__ void __launch_bounds__(kSelThreads, 3) topk_select_kernel(const uint1
       const int64_t v = index_of(t);
       if (pos < kSelCap) {
         lidx[pos] = static_cast<uint32_t>(v);
-        lkey[pos] = static_cast<uint16_t>(key16(x[v]));
+        lval[pos] = x[v];
       }
       ++pos;
     }
@@ -360,7 +363,7 @@ __global__ void __launch_bounds__(kSelThreads, 3) topk_select_kernel(const uint1
       for (int t = tid; t < 256; t += kSelThreads) hist[t] = 0;
       __syncthreads();
       for (int e = tid; e < n; e += kSelThreads) {
-        const uint32_t kk = lkey[e];
+        const uint32_t kk = key16(lval[e]);
         if (pass == 0) atomicAdd(&hist[kk >> 8], 1);
         else if ((kk >> 8) == prefix) atomicAdd(&hist[kk & 0xFFu], 1);
       }
@@ -386,6 +389,8 @@ __global__ void __launch_bounds__(kSelThreads, 3) topk_select_kernel(const uint1
   }
   if (exact) {
     select_exact(x, V, k, out, hist, scan_sh, sel);
+    __syncthreads();  // the block's ids are written
+    for (int j = tid; j < k; j += kSelThreads) out_base[j] = bf16_to_f32(x[out[j]]);
     return;
   }
   const int need_eq = k - above;  // 1 <= need_eq <= n_eq
@@ -399,10 +404,13 @@ __global__ void __launch_bounds__(kSelThreads, 3) topk_select_kernel(const uint1
   const bool all_ties = need_eq == n_eq;
   for (int e0 = 0; e0 < n; e0 += kSelThreads) {
     const int e = e0 + tid;
-    const uint32_t kk = e < n ? lkey[e] : 0u;
+    const uint32_t kk = e < n ? key16(lval[e]) : 0u;
     const bool take = e < n && (kk > T || (kk == T && all_ties));
     const int pos = warp_append(take ? 1 : 0, n_out);
-    if (take && pos < k) out[pos] = static_cast<int32_t>(lidx[e]);
+    if (take && pos < k) {
+      out[pos] = static_cast<int32_t>(lidx[e]);
+      out_base[pos] = bf16_to_f32(lval[e]);
+    }
     if (!all_ties) {
       const bool tie = e < n && kk == T;
       const int tp = warp_append(tie ? 1 : 0, n_tie);
@@ -415,7 +423,10 @@ __global__ void __launch_bounds__(kSelThreads, 3) topk_select_kernel(const uint1
       const uint32_t me = ties[e];
       int rank = 0;
       for (int f = 0; f < n_eq; ++f) rank += ties[f] < me ? 1 : 0;
-      if (rank < need_eq && *n_out + rank < k) out[*n_out + rank] = static_cast<int32_t>(me);
+      if (rank < need_eq && *n_out + rank < k) {
+        out[*n_out + rank] = static_cast<int32_t>(me);
+        out_base[*n_out + rank] = bf16_to_f32(x[me]);
+      }
     }
   }
 }
@@ -700,7 +711,7 @@ const void* topk_walk_kernel_ptr(bool int8, bool prob, bool logits) {
 }
 
 cudaError_t launch_topk_select(const uint16_t* base, int64_t V, int k, int rows, int32_t* cand,
-                               uint16_t* logits, cudaStream_t stream) {
+                               float* cand_base, uint16_t* logits, cudaStream_t stream) {
   constexpr size_t smem = kSelBins * 4 + kSelCap * 6 + 96 * 4;
   static bool attr = false;
   if (!attr) {
@@ -709,7 +720,7 @@ cudaError_t launch_topk_select(const uint16_t* base, int64_t V, int k, int rows,
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  topk_select_kernel<<<rows, kSelThreads, smem, stream>>>(base, V, k, cand, logits);
+  topk_select_kernel<<<rows, kSelThreads, smem, stream>>>(base, V, k, cand, cand_base, logits);
   return cudaGetLastError();
 }
 

@@ -214,9 +214,9 @@ int32_t dspark_walk_from_host(const dspark_walk_args* args, const uint16_t* base
                               dspark_stream_t stream);
 
 /* Bytes of scratch workspace a walk of this shape needs (argmax slots, barrier
- * counters, status words, top-k candidate lists). Part of the walk's C interface
- * specified with dspark_walk (caller-owned workspace, no allocation in the library);
- * the pages have no counterpart. Returns 0 for bs < 1, K < 1 or top_k < 0. */
+ * counters, status words, top-k candidate lists and their base logits). Part of the
+ * walk's C interface specified with dspark_walk (caller-owned workspace, no allocation
+ * in the library); the pages have no counterpart. Returns 0 for bs < 1, K < 1 or top_k < 0. */
 size_t dspark_walk_workspace_size(int64_t V, int32_t bs, int32_t K, int32_t top_k);
 
 /*
