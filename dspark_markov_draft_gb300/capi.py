@@ -66,6 +66,7 @@ class VerifyArgs(C.Structure):
         ("target_logits", C.c_void_p), ("draft_logits", C.c_void_p), ("draft_tokens", C.c_void_p),
         ("seeds", C.c_void_p), ("V", C.c_int64), ("bs", C.c_int32), ("K", C.c_int32),
         ("temperature", C.c_float), ("accepted", C.c_void_p), ("out_tokens", C.c_void_p),
+        ("norms", C.c_void_p),
     ]
 
 
@@ -281,9 +282,11 @@ def walk_from_host(args: WalkArgs, base_host, prev_host, seeds_host, tokens_host
 
 
 def verify(target_logits, draft_logits, draft_tokens, seeds, temperature=1.0, *, accepted=None,
-           out_tokens=None, stream=None):
+           out_tokens=None, reuse_norms=True, stream=None):
     """dspark_verify: speculative-sampling verification. target_logits bf16 [bs, K+1, V],
-    draft_logits bf16 [bs, K, V], draft_tokens int32 [bs, K], seeds [bs].
+    draft_logits bf16 [bs, K, V], draft_tokens int32 [bs, K], seeds [bs]. reuse_norms:
+    pass the normaliser scratch (the sample pass reuses the acceptance pass's softmax
+    normalisers); False: NULL, recomputed.
     Returns (accepted int32 [bs], out_tokens int32 [bs, K+1])."""
     bs, K1, V = target_logits.shape
     dev = target_logits.device
@@ -299,9 +302,10 @@ def verify(target_logits, draft_logits, draft_tokens, seeds, temperature=1.0, *,
         out_tokens = torch.empty((bs, K1), dtype=torch.int32, device=dev)
     _expect(accepted, (bs,), (torch.int32,), "accepted", dev)
     _expect(out_tokens, (bs, K1), (torch.int32,), "out_tokens", dev)
+    norms = torch.empty((bs, K1 - 1, 4), dtype=torch.float32, device=dev) if reuse_norms else None
     a = VerifyArgs(_dev_ptr(target_logits), _dev_ptr(draft_logits), _dev_ptr(draft_tokens),
                    _dev_ptr(seeds), V, bs, K1 - 1, temperature, _dev_ptr(accepted),
-                   _dev_ptr(out_tokens))
+                   _dev_ptr(out_tokens), _dev_ptr(norms) if norms is not None else None)
     _check(lib().dspark_verify(C.byref(a), _stream(stream)), "dspark_verify")
     return accepted, out_tokens
 

@@ -19,7 +19,7 @@ const void* walk_tc_kernel_ptr(bool int8, bool prob, bool logits, int nq, bool r
 const void* topk_walk_kernel_ptr(bool int8, bool prob, bool logits);
 int32_t verify_launch(const uint16_t* target, const uint16_t* draft, const int32_t* dtok,
                       const uint64_t* seeds, int64_t V, int32_t bs, int32_t K, float temperature,
-                      int32_t* accepted, int32_t* out_tokens, cudaStream_t stream);
+                      int32_t* accepted, int32_t* out_tokens, float* norms, cudaStream_t stream);
 size_t topk_walk_smem(int bs);
 cudaError_t launch_topk_select(const uint16_t* base, int64_t V, int k, int rows, int32_t* cand,
                                float* cand_base, uint16_t* logits, cudaStream_t stream);
@@ -565,8 +565,9 @@ int32_t dspark_verify(const dspark_verify_args* a, dspark_stream_t stream) {
   if (a->V <= 0 || a->V > DSPARK_MAX_V || a->bs < 1 || a->bs > DSPARK_MAX_BS || a->K < 1 || a->K > DSPARK_MAX_K)
     return DSPARK_ERR_INVALID_ARG;
   if (!(a->temperature > 0.f) || !(a->temperature < 3.4e38f)) return DSPARK_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(a->norms) & 15u) return DSPARK_ERR_INVALID_ARG;
   const int32_t e = verify_launch(a->target_logits, a->draft_logits, a->draft_tokens, a->seeds, a->V,
-                                  a->bs, a->K, a->temperature, a->accepted, a->out_tokens,
+                                  a->bs, a->K, a->temperature, a->accepted, a->out_tokens, a->norms,
                                   reinterpret_cast<cudaStream_t>(stream));
   return e == 0 ? DSPARK_OK : cuda_fail(static_cast<cudaError_t>(e), "verify kernels launch");
 }

@@ -66,6 +66,7 @@ struct VerifyParams {
   float inv_t;              // 1 / T rounded to fp32
   int32_t* accepted;        // [bs]: acceptance bits, then the accepted count
   int32_t* out_tokens;      // [bs, K+1]
+  float4* norms;            // [bs, K]: (target max, target sum, draft max, draft sum), or null
 };
 
 // Softmax of row / T as a running maximum m of the raw values and z = sum 2^((x - m) c),
@@ -197,6 +198,8 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) verify_accept_kernel(const 
   const uint16_t* drow = p.draft + (static_cast<size_t>(b) * p.K + i) * static_cast<size_t>(V);
   Softmax st, sd;
   softmax_pair<4>(trow, drow, V, 0, V, c, sh, st, sd);
+  // the normalisers of both rows, for the sample pass at this row's emitting position
+  if (p.norms && threadIdx.x == 0) p.norms[static_cast<size_t>(b) * p.K + i] = make_float4(st.m, st.z, sd.m, sd.z);
   if (threadIdx.x == 0) {
     const int32_t d = p.dtok[static_cast<size_t>(b) * p.K + i];
     const bool in = d >= 0 && static_cast<int64_t>(d) < V;
@@ -242,14 +245,22 @@ __global__ void __cluster_dims__(kEmitCtas, 1, 1) __launch_bounds__(kVerifyThrea
   // an all -inf row, so that its probabilities are 0 and not NaN)
   float mt = 0.f, zt = 0.f, md = 0.f, zd = 0.f;
   if (residual) {
-    Softmax pt, pd;
-    softmax_pair<2>(trow, drow, V, v0, v1, c, sh, pt, pd);
-    if (tid == 0) { part_t = pt; part_d = pd; }
-    cl.sync();
     Softmax st{-INFINITY, 0.f}, sd{-INFINITY, 0.f};
-    for (int q = 0; q < kEmitCtas; ++q) {  // every CTA combines in the same order
-      st = sm_combine(st, *cl.map_shared_rank(&part_t, q), c);
-      sd = sm_combine(sd, *cl.map_shared_rank(&part_d, q), c);
+    if (p.norms) {
+      // the acceptance pass's normalisers of this position's two rows (uniform over the
+      // cluster, so every CTA skips the same cluster barrier)
+      const float4 nv = p.norms[static_cast<size_t>(b) * p.K + n];
+      st = Softmax{nv.x, nv.y};
+      sd = Softmax{nv.z, nv.w};
+    } else {
+      Softmax pt, pd;
+      softmax_pair<2>(trow, drow, V, v0, v1, c, sh, pt, pd);
+      if (tid == 0) { part_t = pt; part_d = pd; }
+      cl.sync();
+      for (int q = 0; q < kEmitCtas; ++q) {  // every CTA combines in the same order
+        st = sm_combine(st, *cl.map_shared_rank(&part_t, q), c);
+        sd = sm_combine(sd, *cl.map_shared_rank(&part_d, q), c);
+      }
     }
     if (st.z > 0.f) { mt = st.m; zt = __frcp_rn(st.z); }
     if (sd.z > 0.f) { md = sd.m; zd = __frcp_rn(sd.z); }
@@ -334,9 +345,10 @@ __global__ void __cluster_dims__(kEmitCtas, 1, 1) __launch_bounds__(kVerifyThrea
 
 int32_t verify_launch(const uint16_t* target, const uint16_t* draft, const int32_t* dtok,
                       const uint64_t* seeds, int64_t V, int32_t bs, int32_t K, float temperature,
-                      int32_t* accepted, int32_t* out_tokens, cudaStream_t stream) {
+                      int32_t* accepted, int32_t* out_tokens, float* norms, cudaStream_t stream) {
   const float inv_t = static_cast<float>(1.0 / static_cast<double>(temperature));
-  VerifyParams p{target, draft, dtok, seeds, V, bs, K, inv_t, accepted, out_tokens};
+  VerifyParams p{target, draft, dtok, seeds, V, bs, K, inv_t, accepted, out_tokens,
+                 reinterpret_cast<float4*>(norms)};
   cudaError_t e = cudaMemsetAsync(accepted, 0, sizeof(int32_t) * static_cast<size_t>(bs), stream);
   if (e != cudaSuccess) return static_cast<int32_t>(e);
   verify_accept_kernel<<<dim3(K, bs), kVerifyThreads, 0, stream>>>(p);

@@ -288,9 +288,14 @@ int32_t dspark_walk_noalloc(const dspark_walk_args* args, dspark_stream_t stream
  *   [bs, K+1] (the accepted drafts, the emitted sample, then -1). All device memory
  *   owned by the caller; asynchronous on `stream`. A draft token outside [0, V) is
  *   rejected. No alignment is required (16- and 8-byte loads are used where the rows
- *   allow them). Returns DSPARK_ERR_INVALID_ARG for null pointers, V outside
- *   1..DSPARK_MAX_V, bs outside 1..DSPARK_MAX_BS, K outside 1..DSPARK_MAX_K, or T not
- *   > 0 and finite; DSPARK_ERR_CUDA if a launch fails.
+ *   allow them). norms (optional, caller-owned scratch, fp32 [bs, K, 4], 16-byte
+ *   aligned): the acceptance pass leaves there the softmax normalisers (running
+ *   maximum, sum) of the target and draft rows of every (row, position), and the
+ *   sample pass reads those of the emitting position instead of recomputing them over
+ *   the two rows; with NULL they are recomputed (the same values up to the summation
+ *   order). Returns DSPARK_ERR_INVALID_ARG for null pointers, V outside
+ *   1..DSPARK_MAX_V, bs outside 1..DSPARK_MAX_BS, K outside 1..DSPARK_MAX_K, T not
+ *   > 0 and finite, or norms not 16-byte aligned; DSPARK_ERR_CUDA if a launch fails.
  */
 typedef struct dspark_verify_args {
   const uint16_t* target_logits;
@@ -303,6 +308,7 @@ typedef struct dspark_verify_args {
   float temperature;
   int32_t* accepted;
   int32_t* out_tokens;
+  float* norms;        /* optional scratch fp32 [bs, K, 4], 16-byte aligned, or NULL */
 } dspark_verify_args;
 int32_t dspark_verify(const dspark_verify_args* args, dspark_stream_t stream);
 

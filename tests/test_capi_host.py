@@ -110,6 +110,13 @@ def test_invalid_arguments_rejected_on_host(L):
         for k, val in d.items():
             setattr(x, k, val)
         assert L.dspark_verify(C.byref(x), None) == 1, bad
+    # the optional normaliser scratch must be 16-byte aligned
+    d = dict(target_logits=fake, draft_logits=fake, draft_tokens=fake, seeds=fake, V=100,
+             bs=2, K=3, temperature=1.0, accepted=fake, out_tokens=fake, norms=fake + 4)
+    x = capi.VerifyArgs()
+    for k, val in d.items():
+        setattr(x, k, val)
+    assert L.dspark_verify(C.byref(x), None) == 1
 
 
 def test_verify_binding_refuses_mismatched_buffers():

@@ -55,8 +55,11 @@ def check_verify(O, tgt, drf, dtok, seeds, T, acc_g, out_g):
     return boundary
 
 
+@pytest.mark.parametrize("reuse_norms", [True, False])
 @pytest.mark.parametrize("V,K,bs,T", [(5003, 4, 8, 1.0), (3001, 2, 16, 0.7), (130, 7, 5, 1.3)])
-def test_verify_matches_oracle(oracle, V, K, bs, T):
+def test_verify_matches_oracle(oracle, V, K, bs, T, reuse_norms):
+    """Both ways to the sample pass's normalisers (the acceptance pass's, through the
+    norms scratch, or recomputed by the sample pass) match the oracle."""
     g = torch.Generator().manual_seed(V + K)
     drf = (torch.randn(bs, K, V, generator=g) * 3).to(torch.bfloat16)
     # targets near the drafts so that acceptances and rejections both occur
@@ -65,7 +68,7 @@ def test_verify_matches_oracle(oracle, V, K, bs, T):
     q = torch.softmax(drf.float() / T, -1)
     dtok = torch.stack([torch.multinomial(q[:, i], 1, generator=g)[:, 0] for i in range(K)], 1).to(torch.int32)
     seeds = torch.arange(bs, dtype=torch.int64) * 7 + 3
-    acc, out = capi.verify(tgt.to(DEV), drf.to(DEV), dtok.to(DEV), seeds.to(DEV), T)
+    acc, out = capi.verify(tgt.to(DEV), drf.to(DEV), dtok.to(DEV), seeds.to(DEV), T, reuse_norms=reuse_norms)
     torch.cuda.synchronize()
     check_verify(oracle, tgt, drf, dtok, seeds, T, acc, out)
     assert 0 < int(acc.sum()) < bs * K  # both outcomes exercised
