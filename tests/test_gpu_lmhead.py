@@ -178,3 +178,35 @@ def test_full_size_lmhead_topk_walk(oracle, d, k, K):
     base64[rows_b] = ref.reshape(len(rows_b), K, V)
     check_walk_rows(oracle, inp, tokens, label=f"V=151936 K={K} bs=64 lmhead d={d} top-k {k} (rows {rows_b})",
                     mode=capi.PROBABILISTIC, top_k=k, base_f64_all=base64, rows_subset=rows_b)
+
+
+def test_lmhead_topk_captured_in_cuda_graph():
+    """The fused LM head captured in a CUDA graph (its passes chained as programmatic
+    dependents) and replayed: every replay gives the candidate sets and logits of an eager
+    call on the hidden rows the graph's buffer holds at replay time."""
+    M, d, V, k = 40, 256, 7000, 64
+    g0 = torch.Generator().manual_seed(77)
+    hidden = torch.randn(M, d, generator=g0).to(torch.bfloat16).to(DEV)
+    head = (torch.randn(V, d, generator=g0) * (3.0 / d ** 0.5)).to(torch.bfloat16).to(DEV)
+    cand = torch.empty((M, k), dtype=torch.int32, device=DEV)
+    cbase = torch.empty((M, k), dtype=torch.float32, device=DEV)
+    ws = capi.lmhead_workspace(M, V, k, device=DEV)
+    capi.lmhead_topk(hidden, head, k, cand=cand, cand_base=cbase, workspace=ws)  # eager first
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        capi.lmhead_topk(hidden, head, k, cand=cand, cand_base=cbase, workspace=ws,
+                         stream=torch.cuda.current_stream())
+    for step in range(3):
+        if step == 1:  # new hidden rows in the captured buffer
+            hidden.copy_(torch.randn(M, d, generator=g0).to(torch.bfloat16).to(DEV))
+        cand.fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        rc, rb = capi.lmhead_topk(hidden, head, k)
+        torch.cuda.synchronize()
+        # the same candidate sets with the same logits (a row's candidates come in any order)
+        o1, o2 = torch.argsort(cand, dim=1), torch.argsort(rc, dim=1)
+        assert torch.equal(torch.gather(cand, 1, o1), torch.gather(rc, 1, o2)), step
+        assert torch.equal(torch.gather(cbase, 1, o1).view(torch.int32),
+                           torch.gather(rb, 1, o2).view(torch.int32)), step

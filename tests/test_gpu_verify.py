@@ -134,3 +134,31 @@ def test_verify_special_cases():
     assert acc == [3, 3, 2]
     assert list(out[0, :3]) == [1, 2, 3] and 0 <= out[0, 3] < V
     assert list(out[2, :2]) == [7, 8] and 0 <= out[2, 2] < V and out[2, 3] == -1
+
+
+def test_verify_captured_in_cuda_graph():
+    """The verifier captured in a CUDA graph (the sample pass a programmatic dependent of
+    the acceptance pass) and replayed equals an eager call on the same buffers."""
+    V, K, bs, T = 4001, 4, 8, 1.0
+    g0 = torch.Generator().manual_seed(5)
+    drf = (torch.randn(bs, K, V, generator=g0) * 3).to(torch.bfloat16)
+    tgt = (torch.cat([drf.float(), torch.randn(bs, 1, V, generator=g0) * 3], 1)
+           + torch.randn(bs, K + 1, V, generator=g0) * 0.7).to(torch.bfloat16)
+    dtok = torch.randint(0, V, (bs, K), generator=g0, dtype=torch.int32)
+    seeds = torch.arange(bs, dtype=torch.int64) * 11 + 1
+    tgt, drf, dtok, seeds = tgt.to(DEV), drf.to(DEV), dtok.to(DEV), seeds.to(DEV)
+    acc = torch.empty(bs, dtype=torch.int32, device=DEV)
+    out = torch.empty((bs, K + 1), dtype=torch.int32, device=DEV)
+    capi.verify(tgt, drf, dtok, seeds, T, accepted=acc, out_tokens=out)  # eager first
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        capi.verify(tgt, drf, dtok, seeds, T, accepted=acc, out_tokens=out,
+                    stream=torch.cuda.current_stream())
+    for step in range(2):
+        out.fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        ra, ro = capi.verify(tgt, drf, dtok, seeds, T)
+        torch.cuda.synchronize()
+        assert torch.equal(acc, ra) and torch.equal(out, ro), step
