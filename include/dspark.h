@@ -14,7 +14,12 @@
  * Conventions shared by every call:
  *   - Every tensor pointer is a DEVICE pointer owned by the caller; tensors are
  *     contiguous and row-major. bf16 tensors are passed as their 16-bit patterns.
- *   - Every call is asynchronous on the stream it is given and allocates nothing.
+ *   - Every call is asynchronous on the stream it is given and allocates nothing. A
+ *     call's kernels may be launched as programmatic dependents of one another (the
+ *     fused LM head's passes, the verifier's sample pass), never of the caller's
+ *     kernels: work the caller enqueues after a call sees all of its results, and the
+ *     calls can be captured in CUDA graphs (tested for the walk, the top-k walk, the
+ *     fused LM head and the verifier).
  *   - The return value is a dspark_status code for problems found on the host
  *     (arguments, capacity, launch). Problems found on the device while the kernel
  *     runs (an out-of-range token, a wait that timed out, a non-finite W2 entry) are
