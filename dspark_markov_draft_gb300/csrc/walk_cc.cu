@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) walk_cc_kernel(const WalkPara
           const int r_out = rbase + j8;
           const float base_v = base_next;
           if (k + 1 < nblk) base_next = load_base(block_r0(k + 1) + 8 * grp + j8);
-          const float scale_v = (INT8 && r_out < n) ? scale_s[r_out] : 0.f;
+          [[maybe_unused]] const float scale_v = (INT8 && r_out < n) ? scale_s[r_out] : 0.f;
           float fpart[8];
           int hpart[8], mpart[8];
 #pragma unroll

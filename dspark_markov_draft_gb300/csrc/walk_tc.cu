@@ -84,21 +84,8 @@ __host__ __device__ constexpr uint32_t f16_idesc(uint32_t fmt, int N) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
-      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t* mbar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-               ::"r"(smem_u32(mbar)) : "memory");
-}
-
-// The same operations executed by a whole warp and carried out by one lane only (a
-// predicate inside the instruction): the warp's lanes never wait for one another.
+// MMA and commit executed by a whole warp and carried out by one lane only (a predicate
+// inside the instruction): the warp's lanes never wait for one another.
 __device__ __forceinline__ void mma_f16_if(bool leader, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                            uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -311,7 +298,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) walk_tc_kernel(const __grid_con
   constexpr int kRowBytes = INT8 ? kRank : 2 * kRank;
   constexpr int kParts = kRowBytes / 128;            // 128-byte parts of a row (2 or 4)
   constexpr int kBlockBytes = 32 * kRowBytes;        // resident 32-row block
-  constexpr int kPassChunks = INT8 ? 4 : 8;          // 16-byte chunks per 32-column store
   constexpr uint32_t kIdesc = f16_idesc(INT8 ? 0u : 1u, N);
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -744,7 +730,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) walk_tc_kernel(const __grid_con
       // are scored too and never stored.
       auto score_group = [&](auto mask_tag, int t, int h4, float c, bool valid, uint32_t trep) {
         constexpr bool MASK = decltype(mask_tag)::value;
-        const int r = t * kTile + 32 * q + lane;
+        [[maybe_unused]] const int r = t * kTile + 32 * q + lane;  // (the logit store's row)
         float sc[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
